@@ -533,9 +533,10 @@ int orc_wire_encode(int fmt, const float *x, int32_t seq_len, int32_t hidden,
     return 0;
 }
 
-/* Decode.  Reading: the header's seq_len must equal the caller's seq_len and,
- * for i8, every zero_point must be 0 (the format is symmetric); otherwise
- * MALFORMED is set and x is left untouched. */
+/* Decode.  Readings: the header's seq_len must equal the caller's seq_len,
+ * otherwise MALFORMED is set and x is left untouched; for i8, a position
+ * whose zero_point is not 0 is not the symmetric format, so it sets
+ * MALFORMED and that position is left untouched (the others decode). */
 int orc_wire_decode(int fmt, const uint8_t *buf, int64_t buf_bytes, int32_t seq_len,
                     int32_t hidden, float *x, int32_t *err_bits)
 {
@@ -547,16 +548,6 @@ int orc_wire_decode(int fmt, const uint8_t *buf, int64_t buf_bytes, int32_t seq_
         *err_bits |= ORC_ERR_MALFORMED;
         return 0;
     }
-    if (fmt == ORC_WIRE_I8) {
-        for (p = 0; p < seq_len; ++p) {
-            const uint8_t *pos = buf + 16 + p * (8 + (int64_t)hidden);
-            float zp = orc_f32_from_bits(orc_load_u32le(pos + 4));
-            if (zp != 0.0f) {
-                *err_bits |= ORC_ERR_MALFORMED;
-                return 0;
-            }
-        }
-    }
     if (fmt == ORC_WIRE_F32) {
         for (j = 0; j < n; ++j) x[j] = orc_f32_from_bits(orc_load_u32le(buf + 16 + 4 * j));
     } else if (fmt == ORC_WIRE_F16) {
@@ -565,6 +556,11 @@ int orc_wire_decode(int fmt, const uint8_t *buf, int64_t buf_bytes, int32_t seq_
         for (p = 0; p < seq_len; ++p) {
             const uint8_t *pos = buf + 16 + p * (8 + (int64_t)hidden);
             float scale = orc_f32_from_bits(orc_load_u32le(pos));
+            float zp = orc_f32_from_bits(orc_load_u32le(pos + 4));
+            if (zp != 0.0f) {
+                *err_bits |= ORC_ERR_MALFORMED;
+                continue;
+            }
             for (j = 0; j < hidden; ++j) {
                 float q = (float)(int8_t)pos[8 + j];
                 x[p * hidden + j] = q * scale;    /* binary32 multiply */

@@ -439,12 +439,13 @@ def test_wire_i8_nonfinite_and_malformed():
     canary = np.full((2, 16), 7.0, np.float32)
     y, err = orc.wire_decode(orc.WIRE_I8, buf, 2, 16, out=canary.copy())
     assert err == orc.ERR_MALFORMED and np.all(y == 7.0)
-    # non-zero zero_point is not the symmetric format
+    # a non-zero zero_point is not the symmetric format: that position is
+    # flagged and left untouched, the other positions decode
     good, _ = orc.wire_encode(orc.WIRE_I8, np.ones((2, 16), np.float32))
     bad = good.copy()
     bad[16 + 24 + 4:16 + 24 + 8] = np.frombuffer(struct.pack("<f", 0.5), np.uint8)
     y, err = orc.wire_decode(orc.WIRE_I8, bad, 2, 16, out=canary.copy())
-    assert err == orc.ERR_MALFORMED and np.all(y == 7.0)
+    assert err == orc.ERR_MALFORMED and np.all(y[1] == 7.0) and np.all(y[0] == 1.0)
     y, err = orc.wire_decode(orc.WIRE_F16, orc.wire_encode(orc.WIRE_F16, x)[0], 2, 16,
                              out=canary.copy())
     assert err == orc.ERR_MALFORMED and np.all(y == 7.0)
