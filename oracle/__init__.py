@@ -203,17 +203,15 @@ def logits(table: np.ndarray, dtype: int, vocab: int, hidden: int, x,
     rb = row_bytes(dtype, hidden)
     if tb.size < vocab * rb:
         raise ValueError("table too small")
-    # orc_logits writes out[b*vocab + v]: hand it full-width rows.
-    out = np.empty((B, vocab), np.float64)
-    sab = np.empty((B, vocab), np.float64) if with_sumabs else None
+    out = np.empty((B, v1 - v0), np.float64)
+    sab = np.empty((B, v1 - v0), np.float64) if with_sumabs else None
     rc = _load().orc_logits(_ptr(tb), dtype, vocab, hidden, rb, _ptr(x), B, v0, v1,
                             _ptr(out), None if sab is None else _ptr(sab),
                             int(threads))
     if rc:
         raise RuntimeError(f"orc_logits rc={rc}")
-    out = out[:, v0:v1]
     if with_sumabs:
-        return out, sab[:, v0:v1]
+        return out, sab
     return out
 
 

@@ -276,12 +276,12 @@ typedef struct {
     int dtype;
     int32_t hidden;
     int64_t row_bytes;
-    int64_t vocab;
     const float *x;
     int32_t batch;
     double *out;
     double *sumabs;
-    int64_t v0, v1;
+    int64_t base, ld;  /* output row (v0 of the call) and row stride */
+    int64_t v0, v1;    /* this worker's rows */
 } orc_logits_job;
 
 static void *orc_logits_worker(void *arg)
@@ -302,16 +302,17 @@ static void *orc_logits_worker(void *arg)
                 acc += p;
                 aacc += fabs(p);
             }
-            jb->out[(int64_t)b * jb->vocab + v] = acc;
-            if (jb->sumabs) jb->sumabs[(int64_t)b * jb->vocab + v] = aacc;
+            jb->out[(int64_t)b * jb->ld + (v - jb->base)] = acc;
+            if (jb->sumabs) jb->sumabs[(int64_t)b * jb->ld + (v - jb->base)] = aacc;
         }
     }
     free(rowf);
     return NULL;
 }
 
-/* Rows [v0, v1) of the logits; nthreads splits the rows into contiguous
- * ranges (a plain partition, results do not depend on it). */
+/* Rows [v0, v1) of the logits, written to out[b*(v1-v0) + (v-v0)];
+ * nthreads splits the rows into contiguous ranges (a plain partition,
+ * results do not depend on it). */
 int orc_logits(const uint8_t *table, int dtype, int64_t vocab, int32_t hidden,
                int64_t row_bytes, const float *x, int32_t batch, int64_t v0,
                int64_t v1, double *out, double *sumabs, int nthreads)
@@ -330,11 +331,12 @@ int orc_logits(const uint8_t *table, int dtype, int64_t vocab, int32_t hidden,
         jobs[t].dtype = dtype;
         jobs[t].hidden = hidden;
         jobs[t].row_bytes = row_bytes;
-        jobs[t].vocab = vocab;
         jobs[t].x = x;
         jobs[t].batch = batch;
         jobs[t].out = out;
         jobs[t].sumabs = sumabs;
+        jobs[t].base = v0;
+        jobs[t].ld = v1 - v0;
         jobs[t].v0 = v0 + t * span;
         jobs[t].v1 = v0 + (t + 1) * span;
         if (jobs[t].v0 > v1) jobs[t].v0 = v1;
