@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the embed / tied lm_head service hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of the workload:
+  embed gather of the workload's token ids (x sqrt(hidden)),
+  tied lm_head projection with fused top-k (+ probabilities),
+  wire encode + decode of the residual batch in the workload's format.
+Inputs are seeded synthetic data (workloads/), resident in HBM before the
+timed region.  The table is larger than L2, so each step streams it from HBM.
+
+Prints one JSON line.  `value` is lm_head top-k residuals per second for the
+whole job (all ranks).  Under torchrun every rank runs its own replica of the
+workload (weak scaling; the path needs no exchange between GPUs).
+
+  python bench.py [--workload qwen05b] [--steps K] [--warmup W]
+  python bench.py --impl reference      # the CPU oracle, timed on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "lm_head top-k residuals/s + HBM GB/s (% roofline); embed gather rows/s"
+UNIT = "residuals/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="lhs", choices=["lhs", "reference"])
+    ap.add_argument("--workload", default="qwen05b", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None, help="lm_head batch (default: workload's first)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def default_steps(name):
+    # keep the device-timed region around 2-4 s (clock sampling needs >1 s)
+    return {"tiny": 20000, "qwen05b": 20000, "gemma_q8": 20000, "gemma31b": 4000,
+            "batched": 2000}[name]
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: one process per GPU, no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world, device=None) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks and clocks
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", d
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback", {}
+
+
+_REASON_COLS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed
+    region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(_REASON_COLS, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# workload setup
+# ---------------------------------------------------------------------------
+
+class Ctx:
+    pass
+
+
+def setup(name, batch, device):
+    import torch
+
+    import embedding_lookup_tied_gb300 as lhs
+    c = Ctx()
+    c.w = w = wl.WORKLOADS[name]
+    c.B = batch or (w.batches[0] if w.batches else 1)
+    c.k = w.k or 10
+    c.fmt = w.wire[0] if w.wire else wl.WIRE_F16
+    c.n_ids = w.n_ids or 1
+    c.lhs = lhs
+    c.dev = device
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(device)
+
+    c.T_host = wl.table_for(w)
+    c.table = lhs.lhs_table_init(up(c.T_host), w.vocab, w.hidden, w.dtype)
+    c.ids_host = wl.ids_for(w) if w.n_ids else wl.zipf_ids(w.cid, 1, w.vocab)
+    c.R_host = wl.residuals_for(w, c.B)
+    c.ids = up(c.ids_host)
+    c.resid = up(c.R_host)
+    if w.resid_dtype == wl.BF16:
+        c.resid = c.resid.view(torch.bfloat16)
+    c.scale = float(w.embed_scale)
+    H = w.hidden
+    c.emb_out = torch.empty((c.n_ids, H), dtype=torch.float32, device=device)
+    rd = lhs.LHS_F32 if w.resid_dtype == wl.F32 else lhs.LHS_BF16
+    c.rd = rd
+    c.ws = torch.empty(lhs.lhs_logits_topk_workspace(c.table, c.B, c.k, rd), dtype=torch.uint8,
+                       device=device)
+    c.top_ids = torch.empty((c.B, c.k), dtype=torch.int32, device=device)
+    c.top_logits = torch.empty((c.B, c.k), dtype=torch.float32, device=device)
+    c.top_probs = torch.empty((c.B, c.k), dtype=torch.float32, device=device)
+    c.wire_bytes = lhs.lhs_wire_bytes(c.fmt, c.B, H)
+    c.wire_buf = torch.empty(c.wire_bytes, dtype=torch.uint8, device=device)
+    c.dec = torch.empty((c.B, H), dtype=torch.float32, device=device)
+    c.err = torch.zeros(1, dtype=torch.int32, device=device)
+    c.stream = torch.cuda.current_stream(device)
+    c.sptr = c.stream.cuda_stream
+    # direct C-ABI argument lists (no per-call marshalling in the timed loop)
+    import ctypes
+    L = lhs.lib()
+    tb = ctypes.byref(c.table.c)
+    c.calls = [
+        (L.lhs_embed, (tb, c.ids.data_ptr(), c.n_ids, ctypes.c_float(c.scale),
+                       c.emb_out.data_ptr(), c.err.data_ptr(), c.sptr)),
+        (L.lhs_logits_topk, (tb, c.resid.data_ptr(), rd, c.B, c.k, ctypes.c_float(1.0),
+                             c.top_ids.data_ptr(), c.top_logits.data_ptr(),
+                             c.top_probs.data_ptr(), c.ws.data_ptr(), c.ws.numel(),
+                             c.err.data_ptr(), c.sptr)),
+        (L.lhs_wire_encode, (c.fmt, c.resid.data_ptr(), rd, c.B, H, 0, 0, c.k,
+                             c.wire_buf.data_ptr(), c.wire_bytes, c.err.data_ptr(), c.sptr)),
+        (L.lhs_wire_decode, (c.fmt, c.wire_buf.data_ptr(), c.wire_bytes, c.B, H,
+                             c.dec.data_ptr(), c.err.data_ptr(), c.sptr)),
+    ]
+    c.lm_call = c.calls[1]
+    # kernels per step: embed 1; lm_head: per 8-residual pass (prep + GEMV) on
+    # the tensor-core path or GEMV alone on the CUDA-core path, then 1 merge;
+    # wire encode 1; decode 1
+    tc = w.dtype in (wl.F16, wl.BF16) and H % 8 == 0 and H >= 64 and w.vocab >= 128
+    passes = (c.B + 7) // 8
+    c.launches_per_step = 1 + (passes * (2 if tc else 1) + 1) + 1 + 1
+    return c
+
+
+def run_step(c):
+    for fn, args in c.calls:
+        rc = fn(*args)
+        if rc != 0:
+            raise RuntimeError(f"{fn.__name__} -> {rc}")
+
+
+def lm_bytes(c):
+    """Algorithmic bytes of one lm_head call: every table row once, the
+    residuals once, the top-k outputs once."""
+    w = c.w
+    relt = 4 if w.resid_dtype == wl.F32 else 2
+    return w.vocab * w.row_bytes + c.B * w.hidden * relt + c.B * c.k * 12
+
+
+def step_bytes(c):
+    w = c.w
+    relt = 4 if w.resid_dtype == wl.F32 else 2
+    distinct = len(np.unique(c.ids_host)) if w.n_ids else 0
+    embed = c.n_ids * (4 + w.hidden * 4) + distinct * w.row_bytes
+    wire = 2 * (c.B * w.hidden * relt) + 2 * c.wire_bytes
+    return lm_bytes(c) + embed + wire
+
+
+# ---------------------------------------------------------------------------
+# timing
+# ---------------------------------------------------------------------------
+
+def time_device(c, steps, warmup, world):
+    import torch
+    for _ in range(warmup):
+        run_step(c)
+    torch.cuda.synchronize()
+    if int(c.err.item()) != 0:
+        raise RuntimeError(f"error word {int(c.err.item())} during warm-up")
+    # lm_head call alone (the dominant kernel), events on its stream
+    lm_steps = max(50, steps // 4)
+    fn, args = c.lm_call
+    for _ in range(5):
+        fn(*args)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(c.stream)
+    for _ in range(lm_steps):
+        fn(*args)
+    e1.record(c.stream)
+    e1.synchronize()
+    lm_ms = e0.elapsed_time(e1) / lm_steps
+    # whole step
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(c.stream)
+    for _ in range(steps):
+        run_step(c)
+    s1.record(c.stream)
+    s1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop()
+    ms = s0.elapsed_time(s1) / steps
+    if int(c.err.item()) != 0:
+        raise RuntimeError(f"error word {int(c.err.item())} in the timed region")
+    return ms, lm_ms, ck
+
+
+def time_e2e(c, steps):
+    """Same step through the public binding with HOST buffers: each step
+    copies its inputs from pinned host memory and reads its results back."""
+    import torch
+    lhs = c.lhs
+    h_ids = torch.from_numpy(c.ids_host.copy()).pin_memory()
+    rh = c.R_host.view(np.int16) if c.R_host.dtype == np.uint16 else c.R_host
+    h_res = torch.from_numpy(np.ascontiguousarray(rh)).pin_memory()
+    if c.w.resid_dtype == wl.BF16:
+        h_res = h_res.view(torch.bfloat16)
+    h_emb = torch.empty(c.emb_out.shape, dtype=torch.float32).pin_memory()
+    h_tid = torch.empty(c.top_ids.shape, dtype=torch.int32).pin_memory()
+    h_tlg = torch.empty(c.top_logits.shape, dtype=torch.float32).pin_memory()
+    h_tpr = torch.empty(c.top_probs.shape, dtype=torch.float32).pin_memory()
+    h_buf = torch.empty(c.wire_buf.shape, dtype=torch.uint8).pin_memory()
+    h_err = torch.empty(1, dtype=torch.int32).pin_memory()
+    d_ids = torch.empty_like(c.ids)
+    d_res = torch.empty_like(c.resid)
+    h2d = h_ids.numel() * 4 + h_res.numel() * h_res.element_size()
+    d2h = (h_emb.numel() * 4 + h_tid.numel() * 4 + h_tlg.numel() * 4 + h_tpr.numel() * 4
+           + h_buf.numel() + 4)
+
+    def one():
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_res.copy_(h_res, non_blocking=True)
+        c.err.zero_()
+        lhs.lhs_embed(c.table, d_ids, c.scale, out=c.emb_out, err=c.err)
+        lhs.lhs_logits_topk(c.table, d_res, c.k, 1.0, ws=c.ws, ids=c.top_ids,
+                            logits=c.top_logits, probs=c.top_probs, err=c.err)
+        lhs.lhs_wire_encode(c.fmt, d_res, 0, 0, c.k, buf=c.wire_buf, err=c.err)
+        h_emb.copy_(c.emb_out, non_blocking=True)
+        h_tid.copy_(c.top_ids, non_blocking=True)
+        h_tlg.copy_(c.top_logits, non_blocking=True)
+        h_tpr.copy_(c.top_probs, non_blocking=True)
+        h_buf.copy_(c.wire_buf, non_blocking=True)
+        h_err.copy_(c.err, non_blocking=True)
+
+    for _ in range(5):
+        one()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(c.stream)
+    for _ in range(steps):
+        one()
+    e1.record(c.stream)
+    e1.synchronize()
+    if int(h_err.item()) != 0:
+        raise RuntimeError("error word set in the end-to-end loop")
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# the oracle on host cores (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_rate(w, T, ids, R, B, k, fmt, budget_s, threads):
+    """Time the oracle on a bounded sample of one step: the full embed and
+    wire work, and the lm_head over a slice of vocab rows; the lm_head time
+    is scaled up to the full vocabulary.  Returns (residuals/s, sample)."""
+    import oracle as orc
+    xv = R if w.resid_dtype == wl.F32 else orc.bf16_to_f32(R)
+    t0 = time.perf_counter()
+    if w.n_ids:
+        orc.embed(T, w.dtype, w.vocab, w.hidden, ids, w.embed_scale)
+    buf, _ = orc.wire_encode(fmt, xv)
+    orc.wire_decode(fmt, buf, B, w.hidden)
+    t_fixed = time.perf_counter() - t0
+    rows = 64
+    t_lm = 0.0
+    done = 0
+    while True:
+        r0 = (done * 7919) % max(1, w.vocab - rows)
+        t1 = time.perf_counter()
+        L = orc.logits(T, w.dtype, w.vocab, w.hidden, xv, v0=r0, v1=r0 + rows,
+                       threads=threads)
+        for b in range(B):
+            orc.topk_f64(L[b], min(k, rows))
+        t_lm += time.perf_counter() - t1
+        done += rows
+        if t_lm + t_fixed >= budget_s or done >= w.vocab:
+            break
+        rows = min(rows * 2, 1 << 14)
+    t_step = t_fixed + t_lm * (w.vocab / done)
+    sample = (f"1 step: full embed ({w.n_ids} ids) + wire encode/decode; lm_head over "
+              f"{done} of {w.vocab} vocab rows for {B} residual(s), time scaled x{w.vocab / done:.1f}")
+    return B / t_step, sample
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = wl.WORKLOADS[args.workload]
+    B = args.batch or (w.batches[0] if w.batches else 1)
+    k = w.k or 10
+    fmt = w.wire[0] if w.wire else wl.WIRE_F16
+    T = wl.table_for(w)
+    ids = wl.ids_for(w) if w.n_ids else np.zeros(1, np.int32)
+    R = wl.residuals_for(w, B)
+    threads = os.cpu_count() or 1
+    steps = args.steps or 3
+    per_step_budget = max(2.0, min(20.0, 150.0 / max(1, steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rate(w, T, ids, R, B, k, fmt, min(1.0, per_step_budget), threads)
+    rates, sample = [], ""
+    for _ in range(steps):
+        r, sample = oracle_rate(w, T, ids, R, B, k, fmt, per_step_budget, threads)
+        rates.append(r)
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * B / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "vocab": w.vocab, "hidden": w.hidden,
+                       "table_dtype": wl.DTYPE_NAMES[w.dtype], "lm_batch": B, "k": k},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    c = setup(args.workload, args.batch, dev)
+    steps = args.steps or default_steps(args.workload)
+    ms, lm_ms, clocks = time_device(c, steps, max(3, args.warmup), world)
+    ms = max_over_ranks(ms, world, dev)
+    e2e_steps = max(20, min(steps // 10, 2000))
+    e2e_ms, h2d, d2h = time_e2e(c, e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    peak, peak_kind, _ = load_peaks()
+    value = world * c.B / (ms / 1e3)
+    lmb = lm_bytes(c)
+    achieved = lmb / (lm_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {wl.F32: "f32", wl.F16: "f16", wl.BF16: "bf16", wl.Q8_0: "q8_0"}[c.w.dtype]
+                 + "-table/f32-accumulate",
+        "data": "synthetic",
+        "config": {"workload": c.w.name, "vocab": c.w.vocab, "hidden": c.w.hidden,
+                   "table_dtype": wl.DTYPE_NAMES[c.w.dtype], "table_bytes": c.w.table_bytes,
+                   "embed_ids": c.n_ids, "lm_batch": c.B, "k": c.k,
+                   "wire": {0: "f32", 1: "f16", 2: "i8"}[c.fmt],
+                   "l2": "no flush: the table is larger than L2 and is streamed every step",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs_step": world * step_bytes(c) / (ms / 1e3) / 1e9,
+        "embed_rows_per_s": world * c.n_ids / (ms / 1e3),
+        "roofline": {"kernel": "lhs_logits_topk (prep + GEMV/top-k + merge)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": None, "algorithmic_bytes": lmb, "avg_ms": lm_ms},
+        "gpu_launches": c.launches_per_step * steps,
+        "clocks": clocks,
+        "e2e": {"value": world * c.B / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": e2e_ms},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        r, sample = oracle_rate(c.w, c.T_host, c.ids_host, c.R_host, c.B, c.k, c.fmt,
+                                args.cpu_budget_s, threads)
+        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line))
+    barrier(world)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+// lhs_internal.cuh — device helpers and launcher prototypes shared by the
+// kernels of the GB300 embed / tied lm_head library.  sm_103a only.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lhs.h"
+
+namespace lhs {
+
+// ---------------------------------------------------------------------------
+// error word
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_err(int32_t *err, int bits) {
+    atomicOr(reinterpret_cast<int *>(err), bits);
+}
+
+// ---------------------------------------------------------------------------
+// Total order of (logit, token id) used by top-k: logit descending, equal
+// logits by id ascending, +0 == -0, NaN above every number.  The 64-bit key
+// is larger for the better entry; 0 never encodes a real entry.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key32(float v) {
+    uint32_t u = __float_as_uint(v);
+    if (v != v) u = 0x7FC00000u;
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ uint64_t topk_key(float v, int32_t id) {
+    return (static_cast<uint64_t>(order_key32(v)) << 32) |
+           static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(id));
+}
+__device__ __forceinline__ float key_value(uint64_t key) {
+    uint32_t k = static_cast<uint32_t>(key >> 32);
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(u);
+}
+__device__ __forceinline__ int32_t key_id(uint64_t key) {
+    return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses, mbarriers, TMA, bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait until the barrier phase with the given parity completes, for at most
+// timeout_ns.  Returns false when the limit ran out (the caller records
+// LHS_ERRBIT_TIMEOUT and leaves its loop).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// 2-D tiled TMA load global -> shared, completion signalled on `bar` as
+// transaction bytes.  c0 is the innermost (contiguous) coordinate.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Named barrier among `nthreads` threads (multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// constants
+// ---------------------------------------------------------------------------
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s bound on any on-chip wait
+constexpr int kMaxK = 128;                          // largest top-k served
+
+// ---------------------------------------------------------------------------
+// per-device facts (queried once per device)
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int max_smem_optin;
+};
+cudaError_t device_info(DeviceInfo *out);
+
+// ---------------------------------------------------------------------------
+// launchers (host side); each returns cudaSuccess or the launch error
+// ---------------------------------------------------------------------------
+cudaError_t launch_embed(const lhs_table &t, const int32_t *ids, int64_t n, float scale,
+                         float *out, int32_t *err, cudaStream_t stream);
+
+cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_len,
+                               int32_t hidden, uint32_t layer, uint32_t flags, uint32_t top_k,
+                               void *buf, int32_t *err, cudaStream_t stream);
+cudaError_t launch_wire_decode(int fmt, const void *buf, int32_t seq_len, int32_t hidden,
+                               float *x, int32_t *err, cudaStream_t stream);
+
+// lm_head: plan (workspace layout + kernel choice) and launch
+struct LmHeadPlan {
+    int path;          // 0 = tensor-core streaming GEMV (f16/bf16 table, batch <= 8)
+                       // 1 = CUDA-core streaming GEMV (any table dtype)
+    int grid;          // CTAs of the projection kernel (= partial top-k lists)
+    int batch_chunk;   // residuals per pass of the projection
+    int kpad;          // hidden rounded up for the tensor-core operand
+    size_t off_x;      // workspace offsets (bytes)
+    size_t off_keys;
+    size_t off_ms;
+    size_t bytes;      // total workspace
+};
+int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dtype,
+                 const DeviceInfo &dev, LmHeadPlan *plan);
+cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const void *resid,
+                           int32_t resid_dtype, int32_t batch, int32_t k, float temperature,
+                           int32_t *ids, float *logits_out, float *probs, float *raw_logits,
+                           void *ws, int32_t *err, cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(int32_t *err, int64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace lhs

@@ -1,0 +1,911 @@
+// lm_head.cu — steps 2+3: tied lm_head projection with fused top-k.
+//
+// ADR-0008 "Remote Embeddings and lm_head Service", POST /v1/logits: the
+// projection residual @ lm_head.T over every vocab row, answered as top_k
+// {token_id, prob} (or the raw logit vector); Open Question 1: the lm_head
+// is the embedding table itself.  HELIX "Columnar Embedding", §5: the
+// projection needs all vocab rows, so every call streams the whole table.
+//
+// Design (one GPU, the table resident in HBM):
+//  * The vocab is split into G contiguous row ranges, one per CTA (G = SM
+//    count), balanced to 16 rows.  Each CTA streams its rows once.
+//  * f16/bf16 tables, hidden % 8 == 0: tensor-core streaming GEMV.  A
+//    producer warp drives a ring of TMA tiles (128 table rows x 64 k,
+//    128-byte swizzle) plus the matching 16 x 64 operand tile of the
+//    residuals; 8 consumer warps run mma.sync m16n8k16 (f32 accumulate), each
+//    on 16 vocab rows.  The residuals enter as two 16-bit rows each
+//    (hi = rn16(x), lo = rn16(x - hi)), so the product keeps ~16 (bf16) or
+//    ~22 (f16) bits of every f32 residual.
+//  * Other tables (f32, Q8_0, ragged hidden): CUDA-core GEMV, one warp per
+//    row, residuals in shared memory as f32.
+//  * Fused top-k: every logit is offered to a per-CTA candidate list per
+//    residual if it beats that list's current k-th best key; lists are cut
+//    back to k by a radix select when they fill.  An online (max, sum exp)
+//    per residual rides along.  Each CTA writes k candidates and (m, s) per
+//    residual; a merge kernel selects the global top-k, sorts it and
+//    evaluates the probabilities.  The full logit vector is never written
+//    (unless the raw-logits call asks for it, which uses the same kernels
+//    and the same summation order).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "lhs_internal.cuh"
+
+namespace lhs {
+namespace {
+
+// ---------------------------------------------------------------------------
+// tile geometry
+// ---------------------------------------------------------------------------
+constexpr int BM = 128;                   // table rows per block
+constexpr int BK = 64;                    // k per stage: 128 bytes of 16-bit values
+constexpr int kStages = 8;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kTcThreads = kConsumers + 32;  // + one producer warp
+constexpr int kAStageBytes = BM * BK * 2;    // 16 KB
+constexpr int kXStageBytes = 16 * BK * 2;    // 2 KB: 8 hi rows + 8 lo rows
+constexpr int kBoxRowsSmall = 16;            // TMA box for the ragged last block
+constexpr int kCandTotal = 4096;             // candidate keys per CTA (all residuals)
+constexpr int kBatchChunk = 8;               // residuals per projection pass
+constexpr int kBarAll = 5;                   // named barrier: all consumers
+constexpr int kSimtThreads = 256;
+
+// ---------------------------------------------------------------------------
+// shared top-k state (both GEMV kernels)
+// ---------------------------------------------------------------------------
+struct TopkShared {
+    uint64_t cand[kCandTotal];
+    uint64_t scratch[kBatchChunk][kMaxK];
+    uint64_t tau[kBatchChunk];
+    uint64_t tmin[kBatchChunk];
+    unsigned hist[kBatchChunk][256];
+    float2 ms_warp[kConsumerWarps][kBatchChunk];
+    int cnt[kBatchChunk];
+    int nsel[kBatchChunk];
+    int sel_digit[kBatchChunk];
+    int sel_above[kBatchChunk];
+    int need_compact;
+    int abort_flag;
+};
+
+__device__ __forceinline__ int ld_volatile(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
+
+struct Group {  // the threads that own one residual column during selection
+    int gtid, T, bar_id, col;
+};
+
+__device__ __forceinline__ void group_sync(const Group &g) {
+    if (g.T == 32) __syncwarp();
+    else named_bar_sync(g.bar_id, g.T);
+}
+
+// Split `nthreads` consumer threads into pow2(ncols) groups.
+__device__ __forceinline__ Group make_group(int tid, int nthreads, int ncols) {
+    int p = 1;
+    while (p < ncols) p <<= 1;
+    Group g;
+    g.T = nthreads / p;
+    g.col = tid / g.T;
+    g.gtid = tid % g.T;
+    g.bar_id = 1 + g.col;  // ids 1..4 (only used when T > 32, i.e. p <= 4)
+    return g;
+}
+
+// Radix select over 8-bit digits of 64-bit keys: find the kk-th largest of
+// keys[0..cnt) (keys unique) and return (prefix, mask) such that exactly kk
+// keys satisfy (key & mask) >= prefix.  Executed by the T threads of a group.
+__device__ void group_radix_select(const uint64_t *keys, int cnt, int kk, unsigned *hist,
+                                   int *sel_digit, int *sel_above, const Group &g,
+                                   uint64_t &prefix_out, uint64_t &mask_out) {
+    uint64_t prefix = 0, mask = 0;
+    int need = kk;
+    const int lane = g.gtid & 31;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = g.gtid; i < 256; i += g.T) hist[i] = 0;
+        group_sync(g);
+        for (int i = g.gtid; i < cnt; i += g.T) {
+            const uint64_t key = keys[i];
+            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        }
+        group_sync(g);
+        if (g.gtid < 32) {
+            // lane L owns digits 255-8L ... 248-8L (descending)
+            unsigned c[8];
+            unsigned lsum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c[i] = hist[255 - 8 * lane - i];
+                lsum += c[i];
+            }
+            unsigned incl = lsum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const unsigned excl = incl - lsum;
+            if (excl < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= incl) {
+                unsigned run = excl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (run + c[i] >= static_cast<unsigned>(need)) {
+                        *sel_digit = 255 - 8 * lane - i;
+                        *sel_above = static_cast<int>(run);
+                        break;
+                    }
+                    run += c[i];
+                }
+            }
+        }
+        group_sync(g);
+        const int d = *sel_digit;
+        const int above = *sel_above;
+        const int bin = static_cast<int>(hist[d]);
+        need -= above;
+        prefix |= static_cast<uint64_t>(d) << shift;
+        mask |= 0xFFull << shift;
+        group_sync(g);  // everyone has read hist / sel_* before they change
+        if (bin == need) break;
+    }
+    prefix_out = prefix;
+    mask_out = mask;
+}
+
+// Cut keys[0..*cnt) down to its kk best (kk <= kMaxK), in place; *tau
+// becomes the kk-th best key.  Group-collective.
+__device__ void group_compact(uint64_t *keys, int *cnt, uint64_t *tau, int kk, TopkShared &sm,
+                              const Group &g) {
+    const int n = *cnt;
+    if (n <= kk) return;  // uniform across the group
+    uint64_t prefix, mask;
+    group_radix_select(keys, n, kk, sm.hist[g.col], &sm.sel_digit[g.col], &sm.sel_above[g.col], g,
+                       prefix, mask);
+    if (g.gtid == 0) {
+        sm.nsel[g.col] = 0;
+        sm.tmin[g.col] = ~0ull;
+    }
+    group_sync(g);
+    for (int i = g.gtid; i < n; i += g.T) {
+        const uint64_t key = keys[i];
+        if ((key & mask) >= prefix) {
+            const int pos = atomicAdd(&sm.nsel[g.col], 1);
+            sm.scratch[g.col][pos] = key;
+            atomicMin(reinterpret_cast<unsigned long long *>(&sm.tmin[g.col]),
+                      static_cast<unsigned long long>(key));
+        }
+    }
+    group_sync(g);
+    for (int i = g.gtid; i < kk; i += g.T) keys[i] = sm.scratch[g.col][i];
+    if (g.gtid == 0) {
+        *cnt = kk;
+        *tau = sm.tmin[g.col];
+    }
+    group_sync(g);
+}
+
+__device__ __forceinline__ void ms_update(float &m, float &s, float v, float invT) {
+    const float mn = fmaxf(m, v);
+    if (mn == -INFINITY) return;
+    s = s * expf((m - mn) * invT) + expf((v - mn) * invT);
+    m = mn;
+}
+__device__ __forceinline__ float2 ms_combine(float2 a, float2 b, float invT) {
+    const float mn = fmaxf(a.x, b.x);
+    if (mn == -INFINITY) return make_float2(-INFINITY, 0.0f);
+    return make_float2(mn, a.y * expf((a.x - mn) * invT) + b.y * expf((b.x - mn) * invT));
+}
+
+__device__ __forceinline__ void topk_init(TopkShared &sm, int tid, int nthreads) {
+    for (int b = tid; b < kBatchChunk; b += nthreads) {
+        sm.cnt[b] = 0;
+        sm.tau[b] = 0ull;
+    }
+    if (tid == 0) {
+        sm.need_compact = 0;
+        sm.abort_flag = 0;
+    }
+}
+
+// Offer one logit: appended when it beats the column's current k-th best.
+__device__ __forceinline__ void topk_offer(TopkShared &sm, int col, int cap, float v, int32_t id) {
+    const uint64_t key = topk_key(v, id);
+    if (key > sm.tau[col]) {
+        const int pos = atomicAdd(&sm.cnt[col], 1);
+        sm.cand[col * cap + pos] = key;
+    }
+}
+
+// After a round that could add up to `round_max` candidates per column:
+// cut lists that could overflow before the next round.  All consumers call.
+__device__ void topk_round_end(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
+                               int round_max) {
+    named_bar_sync(kBarAll, nthreads);
+    if (tid == 0) {
+        int need = 0;
+        for (int b = 0; b < ncols; ++b) need |= (sm.cnt[b] > cap - round_max);
+        sm.need_compact = need;
+    }
+    named_bar_sync(kBarAll, nthreads);
+    if (sm.need_compact) {
+        const Group g = make_group(tid, nthreads, ncols);
+        if (g.col < ncols) group_compact(sm.cand + g.col * cap, &sm.cnt[g.col], &sm.tau[g.col], k, sm, g);
+        named_bar_sync(kBarAll, nthreads);
+    }
+}
+
+// Final cut to k and write the CTA's partial list and (m, s) per column.
+__device__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
+                            int b_off, int batch_total, uint64_t *part_keys, float2 *part_ms,
+                            float invT) {
+    named_bar_sync(kBarAll, nthreads);
+    {
+        const Group g = make_group(tid, nthreads, ncols);
+        if (g.col < ncols) group_compact(sm.cand + g.col * cap, &sm.cnt[g.col], &sm.tau[g.col], k, sm, g);
+    }
+    named_bar_sync(kBarAll, nthreads);
+    for (int b = 0; b < ncols; ++b) {
+        uint64_t *dst = part_keys + (static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k;
+        const int n = sm.cnt[b];
+        for (int i = tid; i < k; i += nthreads) dst[i] = i < n ? sm.cand[b * cap + i] : 0ull;
+    }
+    if (tid < ncols) {
+        float2 acc = make_float2(-INFINITY, 0.0f);
+        for (int w = 0; w < kConsumerWarps; ++w) acc = ms_combine(acc, sm.ms_warp[w][tid], invT);
+        part_ms[static_cast<size_t>(blockIdx.x) * batch_total + b_off + tid] = acc;
+    }
+}
+
+// Row range of CTA c: 16-row units split evenly.
+__device__ __forceinline__ void cta_rows(int64_t V, int G, int c, int64_t &r0, int64_t &r1) {
+    const int64_t units = (V + 15) / 16;
+    r0 = (units * c / G) * 16;
+    r1 = (units * (c + 1) / G) * 16;
+    if (r1 > V) r1 = V;
+    if (r0 > V) r0 = V;
+}
+
+// ---------------------------------------------------------------------------
+// residual operand prep: x[b][k] (f32 or bf16) -> 16 x Kp rows of the
+// table's 16-bit type: rows 0..7 = hi, rows 8..15 = lo (zero padded)
+// ---------------------------------------------------------------------------
+template <bool BF16T, int XDT>
+__global__ void __launch_bounds__(256)
+    prep_kernel(const void *__restrict__ resid, int Bc, int K, int Kp, uint16_t *__restrict__ xs,
+                int32_t *err) {
+    const int64_t total = static_cast<int64_t>(8) * Kp;
+    int bad = 0;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int b = static_cast<int>(i / Kp);
+        const int kk = static_cast<int>(i % Kp);
+        float v = 0.0f;
+        if (b < Bc && kk < K) {
+            const int64_t src = static_cast<int64_t>(b) * K + kk;
+            if (XDT == LHS_F32) v = __ldg(static_cast<const float *>(resid) + src);
+            else v = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(resid) + src)) << 16);
+        }
+        uint16_t hi, lo;
+        if (BF16T) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(v);
+            hi = __bfloat16_as_ushort(h);
+            lo = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
+        } else {
+            if (!(fabsf(v) < 65504.0f)) bad = 1;
+            const __half h = __float2half_rn(v);
+            hi = __half_as_ushort(h);
+            lo = __half_as_ushort(__float2half_rn(v - __half2float(h)));
+        }
+        xs[static_cast<int64_t>(b) * Kp + kk] = hi;
+        xs[static_cast<int64_t>(8 + b) * Kp + kk] = lo;
+    }
+    if (bad) set_err(err, LHS_ERRBIT_NONFINITE);
+}
+
+// ---------------------------------------------------------------------------
+// tensor-core streaming GEMV
+// ---------------------------------------------------------------------------
+struct TcParams {
+    int64_t V;
+    int K;
+    int nk;          // k stages per block (Kp / 64)
+    int Bc;          // residuals in this pass (<= 8)
+    int b_off;       // first residual of this pass
+    int batch_total;
+    int k;           // top-k (0 = raw mode)
+    float invT;
+    float *raw;      // raw mode: [batch_total x V]
+    uint64_t *part_keys;
+    float2 *part_ms;
+    int32_t *err;
+};
+
+struct TcSmem {
+    uint8_t a[kStages][kAStageBytes];
+    uint8_t x[kStages][kXStageBytes];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    TopkShared tk;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+template <bool BF16T>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    if (BF16T)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <bool BF16T, bool RAW>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a16,
+                   const __grid_constant__ CUtensorMap tm_x, const TcParams p) {
+    extern __shared__ uint8_t dyn_smem[];
+    TcSmem &sm = *reinterpret_cast<TcSmem *>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    int q = 1;
+    while (q < p.Bc) q <<= 1;
+    const int cap = kCandTotal / q;  // candidate slots per residual
+
+    int64_t r0, r1;
+    cta_rows(p.V, gridDim.x, blockIdx.x, r0, r1);
+    const int nblk = static_cast<int>((r1 - r0 + BM - 1) / BM);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    if (tid < kConsumers) topk_init(sm.tk, tid, kConsumers);
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            tma_prefetch_map(&tm_a);
+            tma_prefetch_map(&tm_a16);
+            tma_prefetch_map(&tm_x);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int blk = 0; blk < nblk && ok; ++blk) {
+                const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
+                const int rows = static_cast<int>((r1 - row0) < BM ? (r1 - row0) : BM);
+                const int n16 = (rows + kBoxRowsSmall - 1) / kBoxRowsSmall;
+                const uint32_t abytes = rows == BM ? kAStageBytes : n16 * kBoxRowsSmall * BK * 2;
+                for (int kc = 0; kc < p.nk; ++kc, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    if (!mbar_wait(&sm.empty[s], ph ^ 1, kWaitTimeoutNs)) {
+                        // consumers stopped releasing slots; they record
+                        // their own timeout and leave together
+                        set_err(p.err, LHS_ERRBIT_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    if (ld_volatile(&sm.tk.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.full[s], abytes + kXStageBytes);
+                    if (rows == BM) {
+                        tma_load_2d(sm.a[s], &tm_a, &sm.full[s], kc * BK, static_cast<int32_t>(row0));
+                    } else {
+                        for (int u = 0; u < n16; ++u)
+                            tma_load_2d(sm.a[s] + u * kBoxRowsSmall * BK * 2, &tm_a16, &sm.full[s],
+                                        kc * BK, static_cast<int32_t>(row0 + u * kBoxRowsSmall));
+                    }
+                    tma_load_2d(sm.x[s], &tm_x, &sm.full[s], kc * BK, 0);
+                }
+            }
+            // drain: every issued stage must land before the CTA exits
+            const uint32_t issued = it;
+            for (uint32_t j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
+                const int s = j % kStages;
+                if (!mbar_wait(&sm.full[s], (j / kStages) & 1, kWaitTimeoutNs)) {
+                    set_err(p.err, LHS_ERRBIT_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int g = lane >> 2, t = lane & 3;
+    const int a_row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int a_csel = lane >> 4;
+    const int x_row = (lane & 7) + ((lane >> 4) << 3);
+    const int x_csel = (lane >> 3) & 1;
+    float m_st[2] = {-INFINITY, -INFINITY}, s_st[2] = {0.0f, 0.0f};
+    uint32_t it = 0;
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
+        const int rows = static_cast<int>((r1 - row0) < BM ? (r1 - row0) : BM);
+        const bool active = warp * 16 < rows;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kc = 0; kc < p.nk; ++kc, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1;
+            if (!ld_volatile(&sm.tk.abort_flag)) {
+                if (!mbar_wait(&sm.full[s], ph, kWaitTimeoutNs)) {
+                    if (lane == 0) {
+                        set_err(p.err, LHS_ERRBIT_TIMEOUT);
+                        sm.tk.abort_flag = 1;
+                    }
+                } else if (active) {
+                    const uint32_t abase = smem_u32(sm.a[s]);
+                    const uint32_t xbase = smem_u32(sm.x[s]);
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        const int ca = 2 * ks + a_csel;
+                        const int cx = 2 * ks + x_csel;
+                        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                        ldsm_x4(abase + a_row * 128 + ((ca ^ (a_row & 7)) << 4), a0, a1, a2, a3);
+                        ldsm_x4(xbase + x_row * 128 + ((cx ^ (x_row & 7)) << 4), b0, b1, b2, b3);
+                        mma16816<BF16T>(acc, a0, a1, a2, a3, b0, b1);  // hi
+                        mma16816<BF16T>(acc, a0, a1, a2, a3, b2, b3);  // lo
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+        }
+        // epilogue: thread holds rows (g, g+8) x columns (2t, 2t+1)
+        if (active && !ld_volatile(&sm.tk.abort_flag)) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int64_t v = row0 + warp * 16 + g + 8 * r;
+                if (v < r1) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int b = 2 * t + c;
+                        if (b < p.Bc) {
+                            const float val = acc[2 * r + c];
+                            if (RAW) {
+                                p.raw[static_cast<int64_t>(p.b_off + b) * p.V + v] = val;
+                            } else {
+                                ms_update(m_st[c], s_st[c], val, p.invT);
+                                topk_offer(sm.tk, b, cap, val, static_cast<int32_t>(v));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (!RAW) topk_round_end(sm.tk, tid, kConsumers, p.Bc, p.k, cap, BM);
+        else named_bar_sync(kBarAll, kConsumers);
+        // the flag only changes inside the main loop, before the barrier
+        // above, so every consumer reads the same value here
+        if (ld_volatile(&sm.tk.abort_flag)) break;
+    }
+    if (RAW || ld_volatile(&sm.tk.abort_flag)) return;
+    // per-warp (m, s) for columns 2t, 2t+1: reduce over g (lanes t, t+4, ...)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        float2 ms = make_float2(m_st[c], s_st[c]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            float2 other;
+            other.x = __shfl_xor_sync(0xFFFFFFFFu, ms.x, o);
+            other.y = __shfl_xor_sync(0xFFFFFFFFu, ms.y, o);
+            ms = ms_combine(ms, other, p.invT);
+        }
+        if (g == 0 && 2 * t + c < kBatchChunk) sm.tk.ms_warp[warp][2 * t + c] = ms;
+    }
+    topk_finish(sm.tk, tid, kConsumers, p.Bc, p.k, cap, p.b_off, p.batch_total, p.part_keys,
+                p.part_ms, p.invT);
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core streaming GEMV (f32 / Q8_0 / ragged-hidden tables)
+// ---------------------------------------------------------------------------
+struct SimtParams {
+    const uint8_t *table;
+    int64_t V;
+    int K;
+    int64_t row_bytes;
+    const void *resid;  // first residual of this pass
+    int resid_dtype;
+    int Bc, b_off, batch_total, k;
+    float invT;
+    float *raw;
+    uint64_t *part_keys;
+    float2 *part_ms;
+    int32_t *err;
+};
+
+template <int DT>
+__device__ __forceinline__ float table_elem(const uint8_t *row, int j) {
+    if (DT == LHS_F32) return __ldg(reinterpret_cast<const float *>(row) + j);
+    if (DT == LHS_F16)
+        return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(row) + j)));
+    if (DT == LHS_BF16)
+        return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(row) + j)) << 16);
+    const uint8_t *blk = row + (j >> 5) * 34;
+    const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(blk))));
+    return __fmul_rn(d, static_cast<float>(static_cast<int8_t>(__ldg(blk + 2 + (j & 31)))));
+}
+
+template <int DT, bool RAW>
+__global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtParams p) {
+    extern __shared__ uint8_t dyn_smem[];
+    TopkShared &tk = *reinterpret_cast<TopkShared *>(dyn_smem);
+    float *xs = reinterpret_cast<float *>(dyn_smem + ((sizeof(TopkShared) + 15) & ~size_t(15)));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int q = 1;
+    while (q < p.Bc) q <<= 1;
+    const int cap = kCandTotal / q;
+
+    for (int64_t i = tid; i < static_cast<int64_t>(p.Bc) * p.K; i += kSimtThreads) {
+        float v;
+        if (p.resid_dtype == LHS_F32) v = __ldg(static_cast<const float *>(p.resid) + i);
+        else v = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(p.resid) + i)) << 16);
+        xs[i] = v;
+    }
+    topk_init(tk, tid, kSimtThreads);
+    __syncthreads();
+
+    int64_t r0, r1;
+    cta_rows(p.V, gridDim.x, blockIdx.x, r0, r1);
+    const int nblk = static_cast<int>((r1 - r0 + BM - 1) / BM);
+    float m_st = -INFINITY, s_st = 0.0f;  // lane b < Bc: column b
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
+        for (int rr = 0; rr < 16; ++rr) {
+            const int64_t v = row0 + warp * 16 + rr;
+            if (v >= r1) break;
+            const uint8_t *row = p.table + v * p.row_bytes;
+            float acc[kBatchChunk];
+#pragma unroll
+            for (int b = 0; b < kBatchChunk; ++b) acc[b] = 0.0f;
+            for (int j = lane; j < p.K; j += 32) {
+                const float e = table_elem<DT>(row, j);
+#pragma unroll
+                for (int b = 0; b < kBatchChunk; ++b)
+                    if (b < p.Bc) acc[b] = fmaf(e, xs[b * p.K + j], acc[b]);
+            }
+#pragma unroll
+            for (int b = 0; b < kBatchChunk; ++b) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xFFFFFFFFu, acc[b], o);
+            }
+            float mine = 0.0f;
+#pragma unroll
+            for (int b = 0; b < kBatchChunk; ++b)
+                if (lane == b) mine = acc[b];
+            if (lane < p.Bc) {
+                if (RAW) {
+                    p.raw[static_cast<int64_t>(p.b_off + lane) * p.V + v] = mine;
+                } else {
+                    ms_update(m_st, s_st, mine, p.invT);
+                    topk_offer(tk, lane, cap, mine, static_cast<int32_t>(v));
+                }
+            }
+        }
+        if (!RAW) topk_round_end(tk, tid, kSimtThreads, p.Bc, p.k, cap, BM);
+    }
+    if (RAW) return;
+    if (lane < kBatchChunk) tk.ms_warp[warp][lane] = make_float2(m_st, s_st);
+    topk_finish(tk, tid, kSimtThreads, p.Bc, p.k, cap, p.b_off, p.batch_total, p.part_keys,
+                p.part_ms, p.invT);
+}
+
+// ---------------------------------------------------------------------------
+// merge: global top-k per residual from G partial lists, sorted, + probs
+// ---------------------------------------------------------------------------
+struct MergeSmemHead {
+    uint64_t sel[kMaxK];
+    uint64_t tmin;
+    unsigned hist[256];
+    float2 ms;
+    int nsel, sel_digit, sel_above;
+};
+
+__global__ void __launch_bounds__(256)
+    merge_kernel(const uint64_t *__restrict__ part_keys, const float2 *__restrict__ part_ms, int G,
+                 int batch_total, int k, float invT, int32_t *__restrict__ out_ids,
+                 float *__restrict__ out_logits, float *__restrict__ out_probs) {
+    extern __shared__ uint8_t dyn_smem[];
+    MergeSmemHead &h = *reinterpret_cast<MergeSmemHead *>(dyn_smem);
+    uint64_t *keys = reinterpret_cast<uint64_t *>(dyn_smem + ((sizeof(MergeSmemHead) + 15) & ~size_t(15)));
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int n = G * k;
+    for (int i = tid; i < n; i += 256) {
+        const int gi = i / k, j = i % k;
+        keys[i] = part_keys[(static_cast<size_t>(gi) * batch_total + b) * k + j];
+    }
+    if (tid < 32) {
+        float2 acc = make_float2(-INFINITY, 0.0f);
+        for (int gi = tid; gi < G; gi += 32)
+            acc = ms_combine(acc, part_ms[static_cast<size_t>(gi) * batch_total + b], invT);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float2 other;
+            other.x = __shfl_xor_sync(0xFFFFFFFFu, acc.x, o);
+            other.y = __shfl_xor_sync(0xFFFFFFFFu, acc.y, o);
+            acc = ms_combine(acc, other, invT);
+        }
+        if (tid == 0) h.ms = acc;
+    }
+    __syncthreads();
+    Group g;
+    g.gtid = tid;
+    g.T = 256;
+    g.bar_id = 1;
+    g.col = 0;
+    uint64_t prefix, mask;
+    group_radix_select(keys, n, k, h.hist, &h.sel_digit, &h.sel_above, g, prefix, mask);
+    if (tid == 0) h.nsel = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += 256) {
+        const uint64_t key = keys[i];
+        if ((key & mask) >= prefix) h.sel[atomicAdd(&h.nsel, 1)] = key;
+    }
+    __syncthreads();
+    // rank sort (keys unique): position = number of larger keys
+    if (tid < k) {
+        const uint64_t mine = h.sel[tid];
+        int rank = 0;
+        for (int j = 0; j < k; ++j) rank += h.sel[j] > mine;
+        const size_t o = static_cast<size_t>(b) * k + rank;
+        const float v = key_value(mine);
+        out_ids[o] = key_id(mine);
+        out_logits[o] = v;
+        if (out_probs) out_probs[o] = expf((v - h.ms.x) * invT) / h.ms.y;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host helpers
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D map over a row-major [rows x cols] 16-bit matrix with a given row
+// pitch; box = box_cols x box_rows, 128-byte swizzle, zero fill outside.
+bool make_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                    uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, bool bf16) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                          const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr size_t kTcSmemBytes = sizeof(TcSmem) + 1024;
+constexpr size_t kSimtXBytesMax = 96 * 1024;
+
+size_t simt_smem_bytes(int Bc, int K) {
+    return ((sizeof(TopkShared) + 15) & ~size_t(15)) + static_cast<size_t>(Bc) * K * 4;
+}
+size_t merge_smem_bytes(int G, int k) {
+    return ((sizeof(MergeSmemHead) + 15) & ~size_t(15)) + static_cast<size_t>(G) * k * 8;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dtype,
+                 const DeviceInfo &dev, LmHeadPlan *plan) {
+    (void)resid_dtype;
+    LmHeadPlan p{};
+    // tensor-core path: 16-bit table, TMA-able rows (16-byte pitch), and at
+    // least one full box in each dimension
+    const bool tc = (t.dtype == LHS_F16 || t.dtype == LHS_BF16) && (t.hidden % 8 == 0) &&
+                    t.hidden >= BK && t.vocab >= BM;
+    p.path = tc ? 0 : 1;
+    const int64_t units = (t.vocab + 15) / 16;
+    p.grid = static_cast<int>(units < dev.num_sms ? units : dev.num_sms);
+    p.kpad = static_cast<int>(align_up(t.hidden, BK));
+    if (tc) {
+        p.batch_chunk = kBatchChunk;
+        if (kTcSmemBytes > static_cast<size_t>(dev.max_smem_optin)) return LHS_ERR_UNSUPPORTED;
+    } else {
+        int bc = static_cast<int>(kSimtXBytesMax / (static_cast<size_t>(t.hidden) * 4));
+        if (bc > kBatchChunk) bc = kBatchChunk;
+        if (bc < 1) bc = 1;
+        p.batch_chunk = bc;
+        if (simt_smem_bytes(bc, t.hidden) > static_cast<size_t>(dev.max_smem_optin))
+            return LHS_ERR_UNSUPPORTED;
+    }
+    const int kk = k > 0 ? k : 1;
+    if (k > 0 && merge_smem_bytes(p.grid, k) > static_cast<size_t>(dev.max_smem_optin))
+        return LHS_ERR_UNSUPPORTED;
+    size_t off = 0;
+    p.off_x = off;
+    off += tc ? align_up(static_cast<size_t>(16) * p.kpad * 2, 1024) : 0;
+    p.off_keys = off;
+    off += align_up(static_cast<size_t>(p.grid) * batch * kk * 8, 256);
+    p.off_ms = off;
+    off += align_up(static_cast<size_t>(p.grid) * batch * 8, 256);
+    p.bytes = off;
+    *plan = p;
+    return LHS_OK;
+}
+
+cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const void *resid,
+                           int32_t resid_dtype, int32_t batch, int32_t k, float temperature,
+                           int32_t *ids, float *logits_out, float *probs, float *raw_logits,
+                           void *ws, int32_t *err, cudaStream_t stream) {
+    DeviceInfo dev;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return e;
+    const bool raw = raw_logits != nullptr;
+    const float invT = 1.0f / temperature;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    uint64_t *part_keys = reinterpret_cast<uint64_t *>(wsb + plan.off_keys);
+    float2 *part_ms = reinterpret_cast<float2 *>(wsb + plan.off_ms);
+    const size_t relt = resid_dtype == LHS_F32 ? 4 : 2;
+
+    if (plan.path == 0) {
+        const bool bf16 = t.dtype == LHS_BF16;
+        uint16_t *xs = reinterpret_cast<uint16_t *>(wsb + plan.off_x);
+        CUtensorMap tm_a, tm_a16, tm_x;
+        if (!make_map_16bit(&tm_a, t.data, t.hidden, t.vocab, t.row_bytes, BK, BM, bf16) ||
+            !make_map_16bit(&tm_a16, t.data, t.hidden, t.vocab, t.row_bytes, BK, kBoxRowsSmall, bf16) ||
+            !make_map_16bit(&tm_x, xs, plan.kpad, 16, static_cast<uint64_t>(plan.kpad) * 2, BK, 16, bf16))
+            return cudaErrorInvalidValue;
+        auto kern = bf16 ? (raw ? gemv_tc_kernel<true, true> : gemv_tc_kernel<true, false>)
+                         : (raw ? gemv_tc_kernel<false, true> : gemv_tc_kernel<false, false>);
+        {
+            // one attribute flag per instantiation
+            static std::mutex mu;
+            static bool done[4][64] = {};
+            const int which = (bf16 ? 2 : 0) + (raw ? 1 : 0);
+            std::lock_guard<std::mutex> lock(mu);
+            if (!done[which][dev.device]) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kTcSmemBytes));
+                if (e != cudaSuccess) return e;
+                done[which][dev.device] = true;
+            }
+        }
+        for (int c0 = 0; c0 < batch; c0 += plan.batch_chunk) {
+            const int Bc = batch - c0 < plan.batch_chunk ? batch - c0 : plan.batch_chunk;
+            const void *rc = static_cast<const uint8_t *>(resid) + static_cast<size_t>(c0) * t.hidden * relt;
+            const int pgrid = static_cast<int>((static_cast<int64_t>(8) * plan.kpad + 255) / 256);
+            if (bf16) {
+                if (resid_dtype == LHS_F32)
+                    prep_kernel<true, LHS_F32><<<pgrid, 256, 0, stream>>>(rc, Bc, t.hidden, plan.kpad, xs, err);
+                else
+                    prep_kernel<true, LHS_BF16><<<pgrid, 256, 0, stream>>>(rc, Bc, t.hidden, plan.kpad, xs, err);
+            } else {
+                if (resid_dtype == LHS_F32)
+                    prep_kernel<false, LHS_F32><<<pgrid, 256, 0, stream>>>(rc, Bc, t.hidden, plan.kpad, xs, err);
+                else
+                    prep_kernel<false, LHS_BF16><<<pgrid, 256, 0, stream>>>(rc, Bc, t.hidden, plan.kpad, xs, err);
+            }
+            TcParams p;
+            p.V = t.vocab;
+            p.K = t.hidden;
+            p.nk = plan.kpad / BK;
+            p.Bc = Bc;
+            p.b_off = c0;
+            p.batch_total = batch;
+            p.k = k;
+            p.invT = invT;
+            p.raw = raw_logits;
+            p.part_keys = part_keys;
+            p.part_ms = part_ms;
+            p.err = err;
+            kern<<<plan.grid, kTcThreads, kTcSmemBytes, stream>>>(tm_a, tm_a16, tm_x, p);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+    } else {
+        const size_t smem = simt_smem_bytes(plan.batch_chunk, t.hidden);
+        void (*kern)(const SimtParams);
+        switch (t.dtype) {
+        case LHS_F32: kern = raw ? gemv_simt_kernel<LHS_F32, true> : gemv_simt_kernel<LHS_F32, false>; break;
+        case LHS_F16: kern = raw ? gemv_simt_kernel<LHS_F16, true> : gemv_simt_kernel<LHS_F16, false>; break;
+        case LHS_BF16: kern = raw ? gemv_simt_kernel<LHS_BF16, true> : gemv_simt_kernel<LHS_BF16, false>; break;
+        default: kern = raw ? gemv_simt_kernel<LHS_Q8_0, true> : gemv_simt_kernel<LHS_Q8_0, false>; break;
+        }
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        for (int c0 = 0; c0 < batch; c0 += plan.batch_chunk) {
+            const int Bc = batch - c0 < plan.batch_chunk ? batch - c0 : plan.batch_chunk;
+            SimtParams p;
+            p.table = static_cast<const uint8_t *>(t.data);
+            p.V = t.vocab;
+            p.K = t.hidden;
+            p.row_bytes = t.row_bytes;
+            p.resid = static_cast<const uint8_t *>(resid) + static_cast<size_t>(c0) * t.hidden * relt;
+            p.resid_dtype = resid_dtype;
+            p.Bc = Bc;
+            p.b_off = c0;
+            p.batch_total = batch;
+            p.k = k;
+            p.invT = invT;
+            p.raw = raw_logits;
+            p.part_keys = part_keys;
+            p.part_ms = part_ms;
+            p.err = err;
+            kern<<<plan.grid, kSimtThreads, smem, stream>>>(p);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+    }
+    if (raw) return cudaSuccess;
+    const size_t msmem = merge_smem_bytes(plan.grid, k);
+    {
+        static std::mutex mu;
+        static bool done[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev.device]) {
+            e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     dev.max_smem_optin);
+            if (e != cudaSuccess) return e;
+            done[dev.device] = true;
+        }
+    }
+    merge_kernel<<<batch, 256, msmem, stream>>>(part_keys, part_ms, plan.grid, batch, k, invT, ids,
+                                                 logits_out, probs);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// bounded-wait self test
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void selftest_wait_kernel(int32_t *err, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // nothing ever arrives on `bar`: phase 0 never completes
+        if (!mbar_wait(&bar, 0, timeout_ns)) set_err(err, LHS_ERRBIT_TIMEOUT);
+    }
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(int32_t *err, int64_t timeout_ns, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(err, static_cast<uint64_t>(timeout_ns));
+    return cudaGetLastError();
+}
+
+}  // namespace lhs

@@ -1,0 +1,202 @@
+/*
+ * lhs.h — C-ABI of the GB300 embed / tied lm_head service hot path.
+ *
+ * The library implements the compute behind the embed service described in
+ * "ADR-0008 — Remote Embeddings and lm_head Service" (POST /v1/embed,
+ * POST /v1/logits, error contract) over the row-addressed table of
+ * "HELIX Columnar Embedding — Design Proposal" (§3), with the Q8_0 table and
+ * sqrt(hidden) input scale of "embedding-inference — Port Specification"
+ * (Tensor inventory, Forward graph), and the residual wire codecs of
+ * "ADR-0009 — Wire Format Evolution: f16 Default + i8 Quantised Residuals"
+ * (Wire Layout).
+ *
+ * Conventions shared by every call:
+ *  - Pointers named d_* are DEVICE pointers owned by the caller and only
+ *    borrowed for the call.  The library allocates no device memory, keeps
+ *    no state between calls (beyond per-device kernel attributes set on first
+ *    use) and never synchronises: work is enqueued on `stream`
+ *    (a cudaStream_t; NULL = the legacy default stream) and the call returns.
+ *  - Alignment: tables, embed outputs, residuals, workspaces, wire buffers
+ *    and decoded residuals must be 16-byte aligned; id arrays, top-k outputs
+ *    and d_err 4-byte aligned.  Violations return LHS_ERR_INVALID_ARG.
+ *  - Return value: LHS_OK or a negative LHS_ERR_* for problems detectable on
+ *    the host (bad arguments, sizes, unsupported shapes, a failed launch).
+ *    Nothing is enqueued when a call returns an error.
+ *  - d_err: a device int32 the caller zeroes before the request; kernels
+ *    OR LHS_ERRBIT_* bits into it in stream order for data-dependent errors.
+ *    Any nonzero bit means the request failed as a whole (the single error
+ *    envelope of ADR-0008's error contract).
+ *  - Calls are thread-safe; calls on different streams may run concurrently
+ *    when they use disjoint outputs and workspaces.
+ */
+#ifndef LHS_H_
+#define LHS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LHS_API __attribute__((visibility("default")))
+#else
+#define LHS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (host-detectable errors) ----------------------------- */
+#define LHS_OK 0
+#define LHS_ERR_INVALID_ARG (-1)      /* null pointer, bad size/enum, misalignment */
+#define LHS_ERR_BUFFER_TOO_SMALL (-2) /* workspace or wire buffer below the size query */
+#define LHS_ERR_UNSUPPORTED (-3)      /* valid request this build does not serve */
+#define LHS_ERR_CUDA (-4)             /* a CUDA runtime call or launch failed */
+
+/* ---- data-dependent error bits OR-ed into *d_err ----------------------- */
+#define LHS_ERRBIT_BAD_TOKEN 1  /* a token id < 0 or >= vocab; its row is zero */
+#define LHS_ERRBIT_MALFORMED 2  /* wire message header / zero_point mismatch */
+#define LHS_ERRBIT_NONFINITE 4  /* i8 encode of a non-finite value; f16-table
+                                   lm_head residual outside the f16 range */
+#define LHS_ERRBIT_TIMEOUT 8    /* a bounded on-device wait gave up */
+
+/* ---- table element types and wire formats ------------------------------ */
+typedef enum {
+    LHS_F32 = 0,   /* IEEE binary32, little-endian */
+    LHS_F16 = 1,   /* IEEE binary16 ("f16 store", ADR-0008 memory footprint) */
+    LHS_BF16 = 2,  /* bfloat16 */
+    LHS_Q8_0 = 3   /* blocks of 32: [f16 d (LE)][32 x int8 q], value d*q (Port Spec) */
+} lhs_dtype;
+
+typedef enum {
+    LHS_WIRE_F32 = 0, /* application/x-larql-ffn     : binary32 payload      */
+    LHS_WIRE_F16 = 1, /* application/x-larql-ffn-f16 : binary16 payload      */
+    LHS_WIRE_I8 = 2   /* application/x-larql-ffn-i8  : per position
+                         [scale f32][zero_point f32][hidden x int8]          */
+} lhs_wire;
+
+/* A static vocab x hidden table, row-major: row i occupies bytes
+ * [i*row_bytes, (i+1)*row_bytes) of `data` (HELIX §3; no framing, no
+ * index).  row_bytes = hidden*itemsize, or hidden/32*34 for Q8_0.
+ * Tied lm_head (ADR-0008, Open Question 1): the same table serves the
+ * embedding lookup and the output projection. */
+typedef struct {
+    const void *data;  /* device pointer, 16-byte aligned, caller-owned */
+    int64_t vocab;     /* rows; 1 <= vocab <= 2^31-1 (token ids are int32) */
+    int32_t hidden;    /* elements per row; >= 1; multiple of 32 for Q8_0 */
+    int32_t dtype;     /* lhs_dtype */
+    int64_t row_bytes; /* filled by lhs_table_init */
+} lhs_table;
+
+/* Fill *t after checking the arguments.  Does not touch device memory.
+ * Errors: LHS_ERR_INVALID_ARG for a null/misaligned pointer, vocab or
+ * hidden out of range, unknown dtype, or Q8_0 with hidden % 32 != 0. */
+LHS_API int lhs_table_init(lhs_table *t, const void *d_table, int64_t vocab, int32_t hidden,
+                   int32_t dtype);
+
+/* The /v1/stats figures of ADR-0008: vocab, hidden, row bytes and table
+ * bytes (vocab * row_bytes).  Any output pointer may be NULL. */
+LHS_API int lhs_table_info(const lhs_table *t, int64_t *vocab, int32_t *hidden,
+                   int64_t *row_bytes, int64_t *total_bytes);
+
+/* Step 1 — embed gather (ADR-0008 POST /v1/embed: one row lookup per token;
+ * a prefill of n tokens is n independent lookups, Open Question 2;
+ * Port Spec forward graph: x = token_embd[ids] * sqrt(768)).
+ *   d_out[t*hidden + j] = f32(element(row ids[t], j) * scale)
+ * element() is the exact f32 value stored (f16/bf16 widened; Q8_0 = d*q,
+ * exact), then ONE binary32 multiply by `scale` (pass sqrt(hidden) rounded
+ * to binary32 for the Gemma profile, 1.0f for an unscaled lookup).
+ *   d_ids : int32 [n]            d_out : f32 [n x hidden], row-major
+ * An id outside [0, vocab) yields a zero row and LHS_ERRBIT_BAD_TOKEN.
+ * n == 0 enqueues nothing.  Errors: LHS_ERR_INVALID_ARG (n < 0, null or
+ * misaligned pointers, non-finite scale). */
+LHS_API int lhs_embed(const lhs_table *t, const int32_t *d_ids, int64_t n, float scale,
+              float *d_out, int32_t *d_err, void *stream);
+
+/* Workspace bytes lhs_logits_topk / lhs_logits need for this table, batch,
+ * k (0 for the raw-logits call) and residual dtype.  Depends on the current
+ * device's SM count.  Errors as for lhs_logits_topk. */
+LHS_API int lhs_logits_topk_workspace(const lhs_table *t, int32_t batch, int32_t k,
+                              int32_t resid_dtype, size_t *bytes);
+
+/* Steps 2+3 — tied lm_head projection with fused top-k (ADR-0008
+ * POST /v1/logits: residual @ lm_head.T over every vocab row, top_k entries
+ * {token_id, prob}; HELIX §5: the projection needs all vocab rows).
+ *   logit[b][v] = sum_j element(row v, j) * x[b][j], f32 accumulation
+ *   d_resid : [batch x hidden] of resid_dtype (LHS_F32 or LHS_BF16)
+ *   d_ids   : int32 [batch x k]  token ids, logit descending, equal logits by
+ *             id ascending (a NaN logit ranks above every number)
+ *   d_logits: f32 [batch x k]    the selected logits
+ *   d_probs : f32 [batch x k] or NULL: softmax(logit / temperature) over the
+ *             FULL vocabulary, evaluated for the selected ids
+ * The full logits vector is never written.  1 <= k <= min(128, vocab);
+ * temperature finite and > 0; batch >= 1.  d_ws/ws_bytes: caller-owned
+ * scratch of at least lhs_logits_topk_workspace() bytes; its contents on
+ * entry do not matter and are overwritten.  Errors: LHS_ERR_INVALID_ARG,
+ * LHS_ERR_BUFFER_TOO_SMALL, LHS_ERR_UNSUPPORTED (table dtype / residual
+ * dtype pair not served), LHS_ERR_CUDA.  An f16 table with a residual whose
+ * magnitude reaches 65504 sets LHS_ERRBIT_NONFINITE. */
+LHS_API int lhs_logits_topk(const lhs_table *t, const void *d_resid, int32_t resid_dtype,
+                    int32_t batch, int32_t k, float temperature, int32_t *d_ids,
+                    float *d_logits, float *d_probs, void *d_ws, size_t ws_bytes,
+                    int32_t *d_err, void *stream);
+
+/* Raw-logits mode (ADR-0008 POST /v1/logits, "raw logits mode for beam
+ * search / sampling"): d_logits f32 [batch x vocab].  Computed by the same
+ * kernels and in the same summation order as lhs_logits_topk, so the top-k
+ * of these logits equals the fused call's result bit for bit.  Workspace:
+ * lhs_logits_topk_workspace(t, batch, 0, resid_dtype, ...). */
+LHS_API int lhs_logits(const lhs_table *t, const void *d_resid, int32_t resid_dtype,
+               int32_t batch, float *d_logits, void *d_ws, size_t ws_bytes,
+               int32_t *d_err, void *stream);
+
+/* Step 4 — residual wire codecs (ADR-0009 Wire Layout).
+ * Message = 16-byte header [layer u32][seq_len u32][flags u32][top_k u32]
+ * (little-endian) followed by the payload:
+ *   LHS_WIRE_F32: binary32[seq_len*hidden]
+ *   LHS_WIRE_F16: binary16[seq_len*hidden]; round to nearest even; a finite
+ *                 value beyond the f16 range saturates to +-65504
+ *                 (ADR-0009 Trade-offs, clamp-to-max); inf stays inf; NaN
+ *                 becomes 0x7E00
+ *   LHS_WIRE_I8 : per position [scale f32][zero_point f32 = 0][int8 x hidden],
+ *                 scale = f32(max|x| / 127), q = clamp(rne(f32(x / scale)),
+ *                 -127, 127); decode x^ = f32(q * scale).  An all-zero
+ *                 position has scale 0.  A position with a non-finite value
+ *                 sets LHS_ERRBIT_NONFINITE and is written as scale 0, q 0.
+ * lhs_wire_bytes returns the message size, or -1 for bad arguments. */
+LHS_API int64_t lhs_wire_bytes(int32_t fmt, int32_t seq_len, int32_t hidden);
+
+/* Encode d_x [seq_len x hidden] of x_dtype (LHS_F32 or LHS_BF16) into d_buf
+ * (buf_bytes >= lhs_wire_bytes).  Errors: LHS_ERR_INVALID_ARG,
+ * LHS_ERR_BUFFER_TOO_SMALL, LHS_ERR_CUDA. */
+LHS_API int lhs_wire_encode(int32_t fmt, const void *d_x, int32_t x_dtype, int32_t seq_len,
+                    int32_t hidden, uint32_t layer, uint32_t flags, uint32_t top_k,
+                    void *d_buf, size_t buf_bytes, int32_t *d_err, void *stream);
+
+/* Decode d_buf into d_x f32 [seq_len x hidden].  If the header's seq_len
+ * differs from `seq_len`, LHS_ERRBIT_MALFORMED is set and d_x is not
+ * written.  For i8, a position whose zero_point is not 0 is flagged
+ * LHS_ERRBIT_MALFORMED and left unwritten.  Errors: LHS_ERR_INVALID_ARG,
+ * LHS_ERR_BUFFER_TOO_SMALL (buf_bytes < lhs_wire_bytes), LHS_ERR_CUDA. */
+LHS_API int lhs_wire_decode(int32_t fmt, const void *d_buf, size_t buf_bytes, int32_t seq_len,
+                    int32_t hidden, float *d_x, int32_t *d_err, void *stream);
+
+/* Diagnostic: launch one tiny kernel whose wait on an on-chip barrier is
+ * never satisfied, bounded by timeout_ns; the kernel gives up, sets
+ * LHS_ERRBIT_TIMEOUT in *d_err and exits normally.  This exercises the same
+ * bounded-wait routine the lm_head pipeline uses, without a hang. */
+LHS_API int lhs_selftest_bounded_wait(int32_t *d_err, int64_t timeout_ns, void *stream);
+
+/* Message for a status code; never NULL. */
+LHS_API const char *lhs_strerror(int status);
+
+/* The cudaError_t of the last LHS_ERR_CUDA returned on this host thread. */
+LHS_API int lhs_last_cuda_error(void);
+
+/* Library version string. */
+LHS_API const char *lhs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LHS_H_ */

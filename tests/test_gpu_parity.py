@@ -1,0 +1,321 @@
+"""GPU parity: the CUDA path through the C-ABI against the oracle.
+
+Bit-exact for the gather, Q8_0 dequant, wire codecs and top-k selection;
+lm_head logits within RTOL * sum|T x| of the binary64 oracle; probabilities
+within 1e-5 (relative) of the oracle evaluated on the GPU's own logits.
+"""
+import functools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import embedding_lookup_tied_gb300 as lhs
+import oracle as orc
+import workloads as wl
+from gpu_util import (PROB_RTOL, RTOL, bits16, canaries_intact, check_topk_against_fp64,
+                      guarded, resid_values, to_dev, upload_table)
+
+pytestmark = pytest.mark.gpu
+
+
+# ---------------------------------------------------------------------------
+# step 1: gather
+# ---------------------------------------------------------------------------
+
+def _embed_case(dtype, V, H, ids, scale, seed=0):
+    T = wl.make_table(dtype, V, H, 0.02, cid=100 + seed, threads=4)
+    tab = upload_table(T, dtype, V, H)
+    ids_d = to_dev(np.asarray(ids, np.int32))
+    raw, out, pad = guarded((len(ids), H), torch.float32)
+    _, err = lhs.lhs_embed(tab, ids_d, scale, out=out)
+    ref, ref_err = orc.embed(T, dtype, V, H, ids, scale)
+    got = out.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    assert int(err.item()) == ref_err
+    assert canaries_intact(raw, pad)
+
+
+@pytest.mark.parametrize("dtype,H", [(orc.F32, 256), (orc.F32, 36), (orc.F32, 7),
+                                     (orc.F16, 256), (orc.F16, 72), (orc.F16, 13),
+                                     (orc.BF16, 896), (orc.BF16, 100),
+                                     (orc.Q8_0, 768), (orc.Q8_0, 96), (orc.Q8_0, 32)])
+@pytest.mark.parametrize("scaled", [False, True])
+def test_embed_parity(dtype, H, scaled):
+    V = 1031
+    g = np.random.default_rng(H)
+    ids = np.concatenate([[0, V - 1, 5, 5], g.integers(0, V, 200), [-1, V, 2 ** 31 - 1, 7]])
+    s = np.float32(math.sqrt(H)) if scaled else np.float32(1.0)
+    _embed_case(dtype, V, H, ids.astype(np.int32), s, seed=dtype)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen05b", "gemma_q8"])
+def test_embed_workloads_full_size(name):
+    w = wl.WORKLOADS[name]
+    T = wl.table_for(w)
+    tab = upload_table(T, w.dtype, w.vocab, w.hidden)
+    ids = wl.ids_for(w)
+    for s in ([w.embed_scale, np.float32(1.0)] if name == "qwen05b" else [w.embed_scale]):
+        out, err = lhs.lhs_embed(tab, to_dev(ids), s)
+        ref, ref_err = orc.embed(T, w.dtype, w.vocab, w.hidden, ids, s)
+        assert int(err.item()) == ref_err == 0
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_embed_empty_and_q8_closed_form():
+    V, H = 64, 768
+    T = wl.make_table(orc.Q8_0, V, H, cid=7, threads=1)
+    tab = upload_table(T, orc.Q8_0, V, H)
+    out, err = lhs.lhs_embed(tab, torch.empty(0, dtype=torch.int32, device="cuda"), 1.0)
+    assert out.numel() == 0 and int(err.item()) == 0
+    # Port Spec forward graph: x = token_embd[ids] * sqrt(768), from the blocks
+    ids = np.arange(V, dtype=np.int32)
+    s = np.float32(math.sqrt(768.0))
+    out, err = lhs.lhs_embed(tab, to_dev(ids), s)
+    blk = T.reshape(V, 24, 34)
+    d = blk[:, :, 0:2].copy().view(np.float16).astype(np.float64)   # [V,24,1]
+    q = blk[:, :, 2:].view(np.int8).astype(np.float64)               # [V,24,32]
+    expect = (d * q).reshape(V, H).astype(np.float32) * s
+    assert np.array_equal(out.cpu().numpy(), expect)
+
+
+# ---------------------------------------------------------------------------
+# step 4: wire codecs
+# ---------------------------------------------------------------------------
+
+def _special(x):
+    x = x.copy()
+    flat = x.reshape(-1)
+    vals = [np.nan, np.inf, -np.inf, 1e6, -65519.99, 65520.0, 65504.0, 3e-8, -0.0, 0.0,
+            6.1e-5, 2 ** -25, 1 + 2 ** -11]
+    for i, v in enumerate(vals):
+        if i * 7 < flat.size:
+            flat[i * 7] = v
+    return x
+
+
+@pytest.mark.parametrize("shape", [(4, 256), (1, 896), (8, 5376), (3, 100), (2, 9), (0, 64)])
+@pytest.mark.parametrize("xdt", [orc.F32, orc.BF16])
+@pytest.mark.parametrize("fmt", [orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8])
+def test_wire_parity(shape, xdt, fmt):
+    s, h = shape
+    g = np.random.default_rng(s * 1000 + h)
+    x = (g.standard_normal(shape).astype(np.float32) *
+         g.uniform(0.5, 8, (s, 1)).astype(np.float32))
+    if fmt != orc.WIRE_I8:
+        x = _special(x)
+    elif s >= 3:
+        x[1] = 0.0                     # all-zero position
+        x[2, min(3, h - 1)] = np.inf   # non-finite position
+    if xdt == orc.BF16:
+        xs = wl.f32_to_bf16_bits(np.nan_to_num(x, nan=0.0, posinf=3e38, neginf=-3e38))
+        xv = orc.bf16_to_f32(xs).reshape(shape)
+        xd = to_dev(xs).view(torch.bfloat16).reshape(shape)
+    else:
+        xv = x
+        xd = to_dev(x)
+    ref_buf, ref_err = orc.wire_encode(fmt, xv, layer=9, flags=3, top_k=5)
+    raw, buf, pad = guarded((ref_buf.size,), torch.uint8)
+    _, err = lhs.lhs_wire_encode(fmt, xd, 9, 3, 5, buf=buf)
+    got = buf.cpu().numpy()
+    assert np.array_equal(got, ref_buf)
+    assert int(err.item()) == ref_err
+    assert canaries_intact(raw, pad)
+    # decode what the GPU encoded
+    ref_x, ref_derr = orc.wire_decode(fmt, ref_buf, s, h)
+    y, derr = lhs.lhs_wire_decode(fmt, buf, s, h)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), ref_x.view(np.uint32))
+    assert int(derr.item()) == ref_derr == 0
+
+
+def test_wire_decode_malformed():
+    x = np.ones((3, 64), np.float32)
+    for fmt in (orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8):
+        buf, _ = lhs.lhs_wire_encode(fmt, to_dev(x))
+        out = torch.full((2, 64), 7.0, device="cuda")
+        _, err = lhs.lhs_wire_decode(fmt, buf, 2, 64, out=out)   # header says 3
+        assert int(err.item()) == lhs.LHS_ERRBIT_MALFORMED
+        assert torch.all(out == 7.0)
+    buf, _ = lhs.lhs_wire_encode(orc.WIRE_I8, to_dev(x))
+    bad = buf.cpu().numpy().copy()
+    bad[16 + 72 + 4:16 + 72 + 8] = np.frombuffer(np.float32(0.5).tobytes(), np.uint8)
+    out = torch.full((3, 64), 7.0, device="cuda")
+    _, err = lhs.lhs_wire_decode(orc.WIRE_I8, to_dev(bad), 3, 64, out=out)
+    ref, ref_err = orc.wire_decode(orc.WIRE_I8, bad, 3, 64, out=np.full((3, 64), 7.0, np.float32))
+    assert int(err.item()) == ref_err == lhs.LHS_ERRBIT_MALFORMED
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+# ---------------------------------------------------------------------------
+# steps 2+3: lm_head + top-k
+# ---------------------------------------------------------------------------
+
+LM_CASES = [
+    # dtype, V, H, B, k, resid dtype        (tensor-core path unless noted)
+    (orc.F16, 1000, 256, 3, 5, orc.F32),
+    (orc.BF16, 8191, 96, 8, 40, orc.F32),     # ragged vocab, hidden % 64 != 0
+    (orc.BF16, 1500, 64, 11, 7, orc.BF16),    # two batch passes, bf16 residuals
+    (orc.F16, 300, 128, 1, 128, orc.F32),     # k = kMax
+    (orc.BF16, 128, 64, 2, 1, orc.F32),       # one block, k = 1
+    (orc.F32, 1000, 256, 4, 5, orc.F32),      # CUDA-core path
+    (orc.Q8_0, 700, 128, 2, 10, orc.F32),     # CUDA-core path
+    (orc.F16, 1000, 72, 2, 6, orc.F32),       # hidden % 64 != 0, tensor-core path
+    (orc.F16, 1000, 68, 2, 6, orc.F32),       # hidden % 8 != 0 -> CUDA-core path
+    (orc.BF16, 100, 64, 3, 100, orc.F32),     # vocab < 128 -> CUDA-core path, k = V
+]
+
+
+def _lm_inputs(dtype, V, H, B, rdt, seed):
+    T = wl.make_table(dtype, V, H, 0.02, cid=200 + seed, threads=4)
+    R = wl.residuals(300 + seed, B, H, (0.5, 8.0), rdt)
+    return T, R
+
+
+def _resid_dev(R, rdt):
+    d = to_dev(R)
+    return d.view(torch.bfloat16) if rdt == orc.BF16 else d
+
+
+@pytest.mark.parametrize("case", LM_CASES,
+                         ids=[f"{wl.DTYPE_NAMES[c[0]]}-V{c[1]}-H{c[2]}-B{c[3]}-k{c[4]}"
+                              for c in LM_CASES])
+def test_lm_head_parity(case):
+    dtype, V, H, B, k, rdt = case
+    T, R = _lm_inputs(dtype, V, H, B, rdt, seed=LM_CASES.index(case))
+    tab = upload_table(T, dtype, V, H)
+    rd = _resid_dev(R, rdt)
+    xv = resid_values(R, rdt)
+    L64, S64 = orc.logits(T, dtype, V, H, xv, threads=8, with_sumabs=True)
+    rtol = RTOL[dtype]
+    # raw logits: within the dot-product tolerance of binary64
+    raw, err = lhs.lhs_logits(tab, rd)
+    assert int(err.item()) == 0
+    Lg = raw.cpu().numpy()
+    assert np.all(np.abs(Lg.astype(np.float64) - L64) <= rtol * S64 + 1e-30)
+    # fused top-k: bit-exact against the oracle's top-k of the GPU's own logits
+    raw_ids, out_ids, pad_i = guarded((B, k), torch.int32)
+    raw_v, out_v, pad_v = guarded((B, k), torch.float32)
+    ids, vals, probs, err = lhs.lhs_logits_topk(tab, rd, k, temperature=0.7, ids=out_ids,
+                                                logits=out_v)
+    assert int(err.item()) == 0
+    assert canaries_intact(raw_ids, pad_i) and canaries_intact(raw_v, pad_v)
+    ids, vals, probs = ids.cpu().numpy(), vals.cpu().numpy(), probs.cpu().numpy()
+    for b in range(B):
+        rid, rv = orc.topk_f32(Lg[b], k)
+        assert np.array_equal(ids[b], rid), b
+        assert np.array_equal(vals[b].view(np.uint32), rv.view(np.uint32)), b
+        rp = orc.softmax_probs(Lg[b], 0.7, rid)
+        assert np.all(np.abs(probs[b] - rp) <= PROB_RTOL * rp), b
+        check_topk_against_fp64(ids[b], vals[b], L64[b], S64[b], k, rtol)
+
+
+@pytest.mark.parametrize("dtype", [orc.F16, orc.BF16, orc.F32])
+def test_lm_head_one_hot_and_integer_tables_exact(dtype):
+    V, H = 777, 128
+    T = wl.make_table(dtype, V, H, 0.02, cid=55, threads=2)
+    tab = upload_table(T, dtype, V, H)
+    cols = orc.decode_rows(T, dtype, H, 0, V)
+    X = np.zeros((3, H), np.float32)
+    X[0, 0] = 1.0
+    X[1, 77] = 1.0
+    X[2, H - 1] = 1.0
+    raw, _ = lhs.lhs_logits(tab, to_dev(X))
+    got = raw.cpu().numpy()
+    for b, j in enumerate((0, 77, H - 1)):
+        assert np.array_equal(got[b], cols[:, j])
+    # integer-valued table and residuals: every partial sum is exact
+    g = np.random.default_rng(1)
+    Ti = g.integers(-2, 3, (V, H))
+    Xi = g.integers(-8, 9, (5, H)).astype(np.float32)
+    if dtype == orc.F32:
+        Ts = Ti.astype(np.float32)
+    elif dtype == orc.F16:
+        Ts = Ti.astype(np.float16).view(np.uint16)
+    else:
+        Ts = wl.f32_to_bf16_bits(Ti.astype(np.float32))
+    tab = upload_table(Ts, dtype, V, H)
+    raw, _ = lhs.lhs_logits(tab, to_dev(Xi))
+    assert np.array_equal(raw.cpu().numpy(), (Xi.astype(np.int64) @ Ti.T).astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", [orc.BF16, orc.F32])
+def test_topk_planted_ties_break_by_id(dtype):
+    V, H, k = 2000, 64, 20
+    base = wl.make_table(dtype, 40, H, 0.02, cid=9, threads=1)
+    T = base[np.arange(V) % 40]          # every row repeated 50 times
+    tab = upload_table(T, dtype, V, H)
+    X = wl.residuals(9, 2, H)
+    ids, vals, _, _ = lhs.lhs_logits_topk(tab, to_dev(X), k)
+    raw, _ = lhs.lhs_logits(tab, to_dev(X))
+    Lg = raw.cpu().numpy()
+    for b in range(2):
+        rid, rv = orc.topk_f32(Lg[b], k)
+        assert np.array_equal(ids.cpu().numpy()[b], rid)
+        # the winners are one row repeated: ids ascend within the tie
+        top = ids.cpu().numpy()[b]
+        same = Lg[b][top] == Lg[b][top[0]]
+        assert np.all(np.diff(top[same]) > 0)
+
+
+def test_f16_table_residual_out_of_range_flags_nonfinite():
+    V, H = 256, 64
+    T = wl.make_table(orc.F16, V, H, cid=3, threads=1)
+    tab = upload_table(T, orc.F16, V, H)
+    X = np.zeros((1, H), np.float32)
+    X[0, 5] = 70000.0
+    _, _, _, err = lhs.lhs_logits_topk(tab, to_dev(X), 3)
+    assert int(err.item()) & lhs.LHS_ERRBIT_NONFINITE
+
+
+@functools.lru_cache(maxsize=1)
+def _workload_table(name):
+    w = wl.WORKLOADS[name]
+    T = wl.table_for(w)
+    return T, upload_table(T, w.dtype, w.vocab, w.hidden)
+
+
+@pytest.mark.parametrize("name,batch", [("tiny", 4), ("qwen05b", 1), ("gemma31b", 1),
+                                        ("gemma31b", 8), ("batched", 256)])
+def test_lm_head_workloads_full_size(name, batch):
+    w = wl.WORKLOADS[name]
+    T, tab = _workload_table(name)
+    R = wl.residuals_for(w, batch)
+    rd = _resid_dev(R, w.resid_dtype)
+    xv = resid_values(R, w.resid_dtype)
+    ids, vals, probs, err = lhs.lhs_logits_topk(tab, rd, w.k)
+    raw, rerr = lhs.lhs_logits(tab, rd)
+    assert int(err.item()) == 0 and int(rerr.item()) == 0
+    ids, vals, probs = ids.cpu().numpy(), vals.cpu().numpy(), probs.cpu().numpy()
+    # sampled residuals: the oracle computes their full logit rows one by one
+    sample = list(range(batch)) if batch <= 8 else [0, 1, 77, 128, 200, 255]
+    for b in sample:
+        Lg = raw[b].cpu().numpy()
+        rid, rv = orc.topk_f32(Lg, w.k)
+        assert np.array_equal(ids[b], rid), b
+        assert np.array_equal(vals[b].view(np.uint32), rv.view(np.uint32)), b
+        rp = orc.softmax_probs(Lg, 1.0, rid)
+        assert np.all(np.abs(probs[b] - rp) <= PROB_RTOL * rp), b
+    for b in sample[:4]:
+        L64, S64 = orc.logits(T, w.dtype, w.vocab, w.hidden, xv[b:b + 1], threads=16,
+                              with_sumabs=True)
+        Lg = raw[b].cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(Lg - L64[0]) <= RTOL[w.dtype] * S64[0] + 1e-30), b
+        check_topk_against_fp64(ids[b], vals[b], L64[0], S64[0], w.k, RTOL[w.dtype])
+
+
+# ---------------------------------------------------------------------------
+# bounded waits
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_gives_up_and_context_survives():
+    err = lhs.lhs_selftest_bounded_wait(50_000_000)
+    torch.cuda.synchronize()
+    assert int(err.item()) == lhs.LHS_ERRBIT_TIMEOUT
+    # the context is still usable
+    V, H = 256, 64
+    T = wl.make_table(orc.F16, V, H, cid=1, threads=1)
+    tab = upload_table(T, orc.F16, V, H)
+    out, e2 = lhs.lhs_embed(tab, to_dev(np.array([3, 4], np.int32)), 1.0)
+    ref, _ = orc.embed(T, orc.F16, V, H, np.array([3, 4], np.int32), 1.0)
+    assert int(e2.item()) == 0 and np.array_equal(out.cpu().numpy(), ref)
