@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     embed_kernel(const uint8_t *__restrict__ table, int64_t vocab, int hidden, int64_t row_bytes,
                  const int32_t *__restrict__ ids, int64_t n, float scale, float *__restrict__ out,
                  int32_t *err) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(kWarps * 32)
             }
         }
     }
+    pdl_trigger();
 }
 
 template <int DT>
@@ -134,13 +136,9 @@ cudaError_t launch_dt(const lhs_table &t, const int32_t *ids, int64_t n, float s
     const int64_t cap = static_cast<int64_t>(num_sms) * 32;
     const int grid = static_cast<int>(blocks_needed < cap ? blocks_needed : cap);
     const uint8_t *tb = static_cast<const uint8_t *>(t.data);
-    if (vec)
-        embed_kernel<DT, true><<<grid, kWarps * 32, 0, stream>>>(tb, t.vocab, t.hidden, t.row_bytes,
-                                                                 ids, n, scale, out, err);
-    else
-        embed_kernel<DT, false><<<grid, kWarps * 32, 0, stream>>>(tb, t.vocab, t.hidden, t.row_bytes,
-                                                                  ids, n, scale, out, err);
-    return cudaGetLastError();
+    return launch_pdl(vec ? embed_kernel<DT, true> : embed_kernel<DT, false>, dim3(grid),
+                      dim3(kWarps * 32), 0, stream, tb, t.vocab, t.hidden, t.row_bytes, ids, n,
+                      scale, out, err);
 }
 
 }  // namespace

@@ -106,6 +106,18 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// Programmatic dependent launch.  pdl_wait(): block until the preceding
+// kernel in the stream has completed and its memory is visible (a no-op when
+// this kernel was not launched as a dependent).  pdl_trigger(): allow the
+// next kernel in the stream to start its prologue now.  Every kernel here
+// calls pdl_wait() before it reads anything an earlier kernel may write and
+// before it writes anything an earlier kernel may read, and only then
+// pdl_trigger().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier among `nthreads` threads (multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -159,5 +171,23 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
                            void *ws, int32_t *err, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int32_t *err, int64_t timeout_ns, cudaStream_t stream);
+
+// Launch `kernel` as a programmatic dependent of the previous work in
+// `stream` (its prologue may overlap the tail of the preceding kernel).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace lhs

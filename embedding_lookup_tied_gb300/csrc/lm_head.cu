@@ -107,9 +107,18 @@ __device__ void group_radix_select(const uint64_t *keys, int cnt, int kk, unsign
     for (int shift = 56; shift >= 0; shift -= 8) {
         for (int i = g.gtid; i < 256; i += g.T) hist[i] = 0;
         group_sync(g);
-        for (int i = g.gtid; i < cnt; i += g.T) {
-            const uint64_t key = keys[i];
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        // histogram of the digit, one atomic per distinct digit per warp
+        // (keys that share a prefix mostly share the next digit too)
+        for (int base = 0; base < cnt; base += g.T) {
+            const int i = base + g.gtid;
+            uint32_t digit = 0xFFFFFFFFu;
+            if (i < cnt) {
+                const uint64_t key = keys[i];
+                if ((key & mask) == prefix) digit = static_cast<uint32_t>(key >> shift) & 255u;
+            }
+            const unsigned peers = __match_any_sync(0xFFFFFFFFu, digit);
+            if (digit != 0xFFFFFFFFu && __ffs(peers) - 1 == lane)
+                atomicAdd(&hist[digit], static_cast<unsigned>(__popc(peers)));
         }
         group_sync(g);
         if (g.gtid < 32) {
@@ -169,15 +178,23 @@ __device__ void group_compact(uint64_t *keys, int *cnt, uint64_t *tau, int kk, T
         sm.tmin[g.col] = ~0ull;
     }
     group_sync(g);
+    uint64_t kmin = ~0ull;
     for (int i = g.gtid; i < n; i += g.T) {
         const uint64_t key = keys[i];
         if ((key & mask) >= prefix) {
             const int pos = atomicAdd(&sm.nsel[g.col], 1);
             sm.scratch[g.col][pos] = key;
-            atomicMin(reinterpret_cast<unsigned long long *>(&sm.tmin[g.col]),
-                      static_cast<unsigned long long>(key));
+            kmin = key < kmin ? key : kmin;
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, kmin, o);
+        kmin = other < kmin ? other : kmin;
+    }
+    if ((g.gtid & 31) == 0 && kmin != ~0ull)
+        atomicMin(reinterpret_cast<unsigned long long *>(&sm.tmin[g.col]),
+                  static_cast<unsigned long long>(kmin));
     group_sync(g);
     for (int i = g.gtid; i < kk; i += g.T) keys[i] = sm.scratch[g.col][i];
     if (g.gtid == 0) {
@@ -220,13 +237,17 @@ __device__ __forceinline__ void topk_offer(TopkShared &sm, int col, int cap, flo
 }
 
 // After a round that could add up to `round_max` candidates per column:
-// cut lists that could overflow before the next round.  All consumers call.
+// cut lists back to k once they hold 2k+64 entries (so the threshold rises
+// early and later rounds offer few candidates), and always before they could
+// overflow.  The cut runs while the producer keeps the TMA ring full, so it
+// costs no HBM time while it is shorter than the ring.  All consumers call.
 __device__ void topk_round_end(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
                                int round_max) {
     named_bar_sync(kBarAll, nthreads);
     if (tid == 0) {
+        const int limit = min(cap - round_max, 2 * k + 64);
         int need = 0;
-        for (int b = 0; b < ncols; ++b) need |= (sm.cnt[b] > cap - round_max);
+        for (int b = 0; b < ncols; ++b) need |= (sm.cnt[b] > limit);
         sm.need_compact = need;
     }
     named_bar_sync(kBarAll, nthreads);
@@ -276,6 +297,8 @@ template <bool BF16T, int XDT>
 __global__ void __launch_bounds__(256)
     prep_kernel(const void *__restrict__ resid, int Bc, int K, int Kp, uint16_t *__restrict__ xs,
                 int32_t *err) {
+    pdl_wait();     // x may come from the previous kernel; xs may still be read by it
+    pdl_trigger();  // the projection may start streaming the table now
     const int64_t total = static_cast<int64_t>(8) * Kp;
     int bad = 0;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -381,6 +404,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (tid < kConsumers) topk_init(sm.tk, tid, kConsumers);
     __syncthreads();
+    pdl_trigger();  // one wave: the merge may take its place now and wait
 
     if (warp == kConsumerWarps) {
         // ---------------- producer ----------------
@@ -388,37 +412,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_prefetch_map(&tm_a);
             tma_prefetch_map(&tm_a16);
             tma_prefetch_map(&tm_x);
-            uint32_t it = 0;
-            bool ok = true;
-            for (int blk = 0; blk < nblk && ok; ++blk) {
+            const uint32_t total = static_cast<uint32_t>(nblk) * p.nk;
+            auto block_rows = [&](int blk) {
                 const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
-                const int rows = static_cast<int>((r1 - row0) < BM ? (r1 - row0) : BM);
-                const int n16 = (rows + kBoxRowsSmall - 1) / kBoxRowsSmall;
-                const uint32_t abytes = rows == BM ? kAStageBytes : n16 * kBoxRowsSmall * BK * 2;
-                for (int kc = 0; kc < p.nk; ++kc, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
-                    if (!mbar_wait(&sm.empty[s], ph ^ 1, kWaitTimeoutNs)) {
-                        // consumers stopped releasing slots; they record
-                        // their own timeout and leave together
-                        set_err(p.err, LHS_ERRBIT_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    if (ld_volatile(&sm.tk.abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&sm.full[s], abytes + kXStageBytes);
-                    if (rows == BM) {
-                        tma_load_2d(sm.a[s], &tm_a, &sm.full[s], kc * BK, static_cast<int32_t>(row0));
-                    } else {
-                        for (int u = 0; u < n16; ++u)
-                            tma_load_2d(sm.a[s] + u * kBoxRowsSmall * BK * 2, &tm_a16, &sm.full[s],
-                                        kc * BK, static_cast<int32_t>(row0 + u * kBoxRowsSmall));
-                    }
-                    tma_load_2d(sm.x[s], &tm_x, &sm.full[s], kc * BK, 0);
+                return static_cast<int>((r1 - row0) < BM ? (r1 - row0) : BM);
+            };
+            auto issue_a = [&](uint32_t j) {
+                const int blk = j / p.nk, kc = j % p.nk, s = j % kStages;
+                const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
+                const int rows = block_rows(blk);
+                if (rows == BM) {
+                    tma_load_2d(sm.a[s], &tm_a, &sm.full[s], kc * BK, static_cast<int32_t>(row0));
+                } else {
+                    const int n16 = (rows + kBoxRowsSmall - 1) / kBoxRowsSmall;
+                    for (int u = 0; u < n16; ++u)
+                        tma_load_2d(sm.a[s] + u * kBoxRowsSmall * BK * 2, &tm_a16, &sm.full[s],
+                                    kc * BK, static_cast<int32_t>(row0 + u * kBoxRowsSmall));
                 }
+            };
+            auto stage_bytes = [&](uint32_t j) {
+                const int rows = block_rows(j / p.nk);
+                const int n16 = (rows + kBoxRowsSmall - 1) / kBoxRowsSmall;
+                return static_cast<uint32_t>(rows == BM ? kAStageBytes : n16 * kBoxRowsSmall * BK * 2) +
+                       kXStageBytes;
+            };
+            // The table is never written by an earlier kernel, so the first
+            // ring's worth of table tiles is requested before waiting for the
+            // residual operand the preceding kernel prepares.
+            const uint32_t pre = total < kStages ? total : kStages;
+            for (uint32_t j = 0; j < pre; ++j) {
+                mbar_arrive_expect_tx(&sm.full[j], stage_bytes(j));
+                issue_a(j);
+            }
+            pdl_wait();
+            for (uint32_t j = 0; j < pre; ++j)
+                tma_load_2d(sm.x[j], &tm_x, &sm.full[j], (j % p.nk) * BK, 0);
+            uint32_t it = pre;
+            for (; it < total; ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                if (!mbar_wait(&sm.empty[s], ph ^ 1, kWaitTimeoutNs)) {
+                    // consumers stopped releasing slots; they record their
+                    // own timeout and leave together
+                    set_err(p.err, LHS_ERRBIT_TIMEOUT);
+                    break;
+                }
+                if (ld_volatile(&sm.tk.abort_flag)) break;
+                mbar_arrive_expect_tx(&sm.full[s], stage_bytes(it));
+                issue_a(it);
+                tma_load_2d(sm.x[s], &tm_x, &sm.full[s], (it % p.nk) * BK, 0);
             }
             // drain: every issued stage must land before the CTA exits
             const uint32_t issued = it;
@@ -558,6 +600,8 @@ __global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtPa
     int q = 1;
     while (q < p.Bc) q <<= 1;
     const int cap = kCandTotal / q;
+    pdl_wait();
+    pdl_trigger();
 
     for (int64_t i = tid; i < static_cast<int64_t>(p.Bc) * p.K; i += kSimtThreads) {
         float v;
@@ -633,6 +677,8 @@ __global__ void __launch_bounds__(256)
     uint64_t *keys = reinterpret_cast<uint64_t *>(dyn_smem + ((sizeof(MergeSmemHead) + 15) & ~size_t(15)));
     const int b = blockIdx.x, tid = threadIdx.x;
     const int n = G * k;
+    pdl_wait();
+    pdl_trigger();
     for (int i = tid; i < n; i += 256) {
         const int gi = i / k, j = i % k;
         keys[i] = part_keys[(static_cast<size_t>(gi) * batch_total + b) * k + j];
@@ -805,17 +851,11 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             const int Bc = batch - c0 < plan.batch_chunk ? batch - c0 : plan.batch_chunk;
             const void *rc = static_cast<const uint8_t *>(resid) + static_cast<size_t>(c0) * t.hidden * relt;
             const int pgrid = static_cast<int>((static_cast<int64_t>(8) * plan.kpad + 255) / 256);
-            if (bf16) {
-                if (resid_dtype == LHS_F32)
-                    prep_kernel<true, LHS_F32><<<pgrid, 256, 0, stream>>>(rc, Bc, t.hidden, plan.kpad, xs, err);
-                else
-                    prep_kernel<true, LHS_BF16><<<pgrid, 256, 0, stream>>>(rc, Bc, t.hidden, plan.kpad, xs, err);
-            } else {
-                if (resid_dtype == LHS_F32)
-                    prep_kernel<false, LHS_F32><<<pgrid, 256, 0, stream>>>(rc, Bc, t.hidden, plan.kpad, xs, err);
-                else
-                    prep_kernel<false, LHS_BF16><<<pgrid, 256, 0, stream>>>(rc, Bc, t.hidden, plan.kpad, xs, err);
-            }
+            auto prep = bf16 ? (resid_dtype == LHS_F32 ? prep_kernel<true, LHS_F32> : prep_kernel<true, LHS_BF16>)
+                             : (resid_dtype == LHS_F32 ? prep_kernel<false, LHS_F32> : prep_kernel<false, LHS_BF16>);
+            e = launch_pdl(prep, dim3(pgrid), dim3(256), 0, stream, rc, Bc, static_cast<int>(t.hidden),
+                           plan.kpad, xs, err);
+            if (e != cudaSuccess) return e;
             TcParams p;
             p.V = t.vocab;
             p.K = t.hidden;
@@ -829,8 +869,8 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             p.part_keys = part_keys;
             p.part_ms = part_ms;
             p.err = err;
-            kern<<<plan.grid, kTcThreads, kTcSmemBytes, stream>>>(tm_a, tm_a16, tm_x, p);
-            e = cudaGetLastError();
+            e = launch_pdl(kern, dim3(plan.grid), dim3(kTcThreads), kTcSmemBytes, stream, tm_a, tm_a16,
+                           tm_x, p);
             if (e != cudaSuccess) return e;
         }
     } else {
@@ -862,8 +902,7 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             p.part_keys = part_keys;
             p.part_ms = part_ms;
             p.err = err;
-            kern<<<plan.grid, kSimtThreads, smem, stream>>>(p);
-            e = cudaGetLastError();
+            e = launch_pdl(kern, dim3(plan.grid), dim3(kSimtThreads), smem, stream, p);
             if (e != cudaSuccess) return e;
         }
     }
@@ -880,9 +919,9 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             done[dev.device] = true;
         }
     }
-    merge_kernel<<<batch, 256, msmem, stream>>>(part_keys, part_ms, plan.grid, batch, k, invT, ids,
-                                                 logits_out, probs);
-    return cudaGetLastError();
+    return launch_pdl(merge_kernel, dim3(batch), dim3(256), msmem, stream, part_keys, part_ms,
+                      plan.grid, static_cast<int>(batch), static_cast<int>(k), invT, ids, logits_out,
+                      probs);
 }
 
 // ---------------------------------------------------------------------------

@@ -66,6 +66,7 @@ template <int FMT, int XDT, bool VEC>
 __global__ void __launch_bounds__(kEwThreads)
     encode_ew_kernel(const void *__restrict__ x, int64_t n, uint32_t layer, uint32_t seq_len,
                      uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf) {
+    pdl_wait();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (tid == 0) write_header(buf, layer, seq_len, flags, top_k);
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kEwThreads)
         else
             reinterpret_cast<float *>(pay)[i] = v;
     }
+    pdl_trigger();
 }
 
 // ---- f32 / f16 decode ------------------------------------------------------
@@ -101,6 +103,7 @@ template <int FMT, bool VEC>
 __global__ void __launch_bounds__(kEwThreads)
     decode_ew_kernel(const uint8_t *__restrict__ buf, int64_t n, uint32_t seq_len,
                      float *__restrict__ x, int32_t *err) {
+    pdl_wait();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const uint32_t hdr_seq = __ldg(reinterpret_cast<const uint32_t *>(buf) + 1);
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(kEwThreads)
         else
             x[i] = __ldg(reinterpret_cast<const float *>(pay) + i);
     }
+    pdl_trigger();
 }
 
 // ---- i8 encode -------------------------------------------------------------
@@ -172,6 +176,7 @@ template <int XDT, bool VEC>
 __global__ void __launch_bounds__(kI8Threads)
     encode_i8_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
                      uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    pdl_wait();
     __shared__ float sm_m[kI8Threads / 32];
     __shared__ int sm_f[kI8Threads / 32];
     if (blockIdx.x == 0 && threadIdx.x == 0)
@@ -261,6 +266,7 @@ __global__ void __launch_bounds__(kI8Threads)
                 pos[8 + j] = static_cast<uint8_t>(i8_code(load_x<XDT>(x, xrow + j), scale));
         }
     }
+    pdl_trigger();
 }
 
 // ---- i8 decode -------------------------------------------------------------
@@ -268,6 +274,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kI8Threads)
     decode_i8_kernel(const uint8_t *__restrict__ buf, int32_t seq_len, int32_t hidden,
                      float *__restrict__ x, int32_t *err) {
+    pdl_wait();
     const uint32_t hdr_seq = __ldg(reinterpret_cast<const uint32_t *>(buf) + 1);
     if (hdr_seq != static_cast<uint32_t>(seq_len)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) set_err(err, LHS_ERRBIT_MALFORMED);
@@ -315,6 +322,7 @@ __global__ void __launch_bounds__(kI8Threads)
                 xo[j] = __fmul_rn(static_cast<float>(static_cast<int8_t>(__ldg(pos + 8 + j))), scale);
         }
     }
+    pdl_trigger();
 }
 
 int ew_grid(int64_t work_items, int num_sms) {
@@ -341,35 +349,22 @@ cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
         int grid = static_cast<int>(seq_len < cap ? seq_len : cap);
         if (grid < 1) grid = 1;
-#define LHS_I8_ENC(XDT, V) \
-    encode_i8_kernel<XDT, V><<<grid, kI8Threads, 0, stream>>>(x, seq_len, hidden, layer, flags, top_k, b, err)
-        if (x_dtype == LHS_F32) {
-            if (vec) LHS_I8_ENC(LHS_F32, true); else LHS_I8_ENC(LHS_F32, false);
-        } else {
-            if (vec) LHS_I8_ENC(LHS_BF16, true); else LHS_I8_ENC(LHS_BF16, false);
-        }
-#undef LHS_I8_ENC
-        return cudaGetLastError();
+        auto kern = x_dtype == LHS_F32 ? (vec ? encode_i8_kernel<LHS_F32, true> : encode_i8_kernel<LHS_F32, false>)
+                                       : (vec ? encode_i8_kernel<LHS_BF16, true> : encode_i8_kernel<LHS_BF16, false>);
+        return launch_pdl(kern, dim3(grid), dim3(kI8Threads), 0, stream, x, seq_len, hidden, layer,
+                          flags, top_k, b, err);
     }
     const bool vec = aligned;
     const int grid = ew_grid(vec ? (n + 7) / 8 : n, dev.num_sms);
-#define LHS_EW_ENC(F, XDT, V) \
-    encode_ew_kernel<F, XDT, V><<<grid, kEwThreads, 0, stream>>>(x, n, layer, s, flags, top_k, b)
+void (*kern)(const void *, int64_t, uint32_t, uint32_t, uint32_t, uint32_t, uint8_t *);
     if (fmt == LHS_WIRE_F16) {
-        if (x_dtype == LHS_F32) {
-            if (vec) LHS_EW_ENC(LHS_WIRE_F16, LHS_F32, true); else LHS_EW_ENC(LHS_WIRE_F16, LHS_F32, false);
-        } else {
-            if (vec) LHS_EW_ENC(LHS_WIRE_F16, LHS_BF16, true); else LHS_EW_ENC(LHS_WIRE_F16, LHS_BF16, false);
-        }
+        if (x_dtype == LHS_F32) kern = vec ? encode_ew_kernel<LHS_WIRE_F16, LHS_F32, true> : encode_ew_kernel<LHS_WIRE_F16, LHS_F32, false>;
+        else kern = vec ? encode_ew_kernel<LHS_WIRE_F16, LHS_BF16, true> : encode_ew_kernel<LHS_WIRE_F16, LHS_BF16, false>;
     } else {
-        if (x_dtype == LHS_F32) {
-            if (vec) LHS_EW_ENC(LHS_WIRE_F32, LHS_F32, true); else LHS_EW_ENC(LHS_WIRE_F32, LHS_F32, false);
-        } else {
-            if (vec) LHS_EW_ENC(LHS_WIRE_F32, LHS_BF16, true); else LHS_EW_ENC(LHS_WIRE_F32, LHS_BF16, false);
-        }
+        if (x_dtype == LHS_F32) kern = vec ? encode_ew_kernel<LHS_WIRE_F32, LHS_F32, true> : encode_ew_kernel<LHS_WIRE_F32, LHS_F32, false>;
+        else kern = vec ? encode_ew_kernel<LHS_WIRE_F32, LHS_BF16, true> : encode_ew_kernel<LHS_WIRE_F32, LHS_BF16, false>;
     }
-#undef LHS_EW_ENC
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kEwThreads), 0, stream, x, n, layer, s, flags, top_k, b);
 }
 
 cudaError_t launch_wire_decode(int fmt, const void *buf, int32_t seq_len, int32_t hidden,
@@ -385,22 +380,15 @@ cudaError_t launch_wire_decode(int fmt, const void *buf, int32_t seq_len, int32_
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
         int grid = static_cast<int>(seq_len < cap ? seq_len : cap);
         if (grid < 1) grid = 1;
-        if (vec)
-            decode_i8_kernel<true><<<grid, kI8Threads, 0, stream>>>(b, seq_len, hidden, x, err);
-        else
-            decode_i8_kernel<false><<<grid, kI8Threads, 0, stream>>>(b, seq_len, hidden, x, err);
-        return cudaGetLastError();
+        return launch_pdl(vec ? decode_i8_kernel<true> : decode_i8_kernel<false>, dim3(grid),
+                          dim3(kI8Threads), 0, stream, b, seq_len, hidden, x, err);
     }
     const int grid = ew_grid(aligned ? (n + 7) / 8 : n, dev.num_sms);
     const uint32_t s = static_cast<uint32_t>(seq_len);
-    if (fmt == LHS_WIRE_F16) {
-        if (aligned) decode_ew_kernel<LHS_WIRE_F16, true><<<grid, kEwThreads, 0, stream>>>(b, n, s, x, err);
-        else decode_ew_kernel<LHS_WIRE_F16, false><<<grid, kEwThreads, 0, stream>>>(b, n, s, x, err);
-    } else {
-        if (aligned) decode_ew_kernel<LHS_WIRE_F32, true><<<grid, kEwThreads, 0, stream>>>(b, n, s, x, err);
-        else decode_ew_kernel<LHS_WIRE_F32, false><<<grid, kEwThreads, 0, stream>>>(b, n, s, x, err);
-    }
-    return cudaGetLastError();
+    void (*kern)(const uint8_t *, int64_t, uint32_t, float *, int32_t *);
+    if (fmt == LHS_WIRE_F16) kern = aligned ? decode_ew_kernel<LHS_WIRE_F16, true> : decode_ew_kernel<LHS_WIRE_F16, false>;
+    else kern = aligned ? decode_ew_kernel<LHS_WIRE_F32, true> : decode_ew_kernel<LHS_WIRE_F32, false>;
+    return launch_pdl(kern, dim3(grid), dim3(kEwThreads), 0, stream, b, n, s, x, err);
 }
 
 }  // namespace lhs

@@ -26,6 +26,20 @@ def bits16(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy().view(np.uint16)
 
 
+def same_f32(got: np.ndarray, ref: np.ndarray) -> bool:
+    """Bit-identical binary32 arrays, except that a NaN matches any NaN: the
+    payload a NaN carries through arithmetic or widening differs between the
+    GPU (canonical 0x7FFFFFFF) and the host CPU (quieted input NaN)."""
+    got = np.ascontiguousarray(got, np.float32)
+    ref = np.ascontiguousarray(ref, np.float32)
+    if got.shape != ref.shape:
+        return False
+    gn, rn = np.isnan(got), np.isnan(ref)
+    if not np.array_equal(gn, rn):
+        return False
+    return bool(np.array_equal(got.view(np.uint32)[~gn], ref.view(np.uint32)[~rn]))
+
+
 def upload_table(table_np: np.ndarray, dtype: int, vocab: int, hidden: int):
     t = to_dev(table_np)
     return lhs.lhs_table_init(t, vocab, hidden, dtype)

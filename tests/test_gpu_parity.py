@@ -14,8 +14,8 @@ import torch
 import embedding_lookup_tied_gb300 as lhs
 import oracle as orc
 import workloads as wl
-from gpu_util import (PROB_RTOL, RTOL, bits16, canaries_intact, check_topk_against_fp64,
-                      guarded, resid_values, to_dev, upload_table)
+from gpu_util import (PROB_RTOL, RTOL, canaries_intact, check_topk_against_fp64, guarded,
+                      resid_values, same_f32, to_dev, upload_table)
 
 pytestmark = pytest.mark.gpu
 
@@ -125,7 +125,7 @@ def test_wire_parity(shape, xdt, fmt):
     # decode what the GPU encoded
     ref_x, ref_derr = orc.wire_decode(fmt, ref_buf, s, h)
     y, derr = lhs.lhs_wire_decode(fmt, buf, s, h)
-    assert np.array_equal(y.cpu().numpy().view(np.uint32), ref_x.view(np.uint32))
+    assert same_f32(y.cpu().numpy(), ref_x)
     assert int(derr.item()) == ref_derr == 0
 
 
