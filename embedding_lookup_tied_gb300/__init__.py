@@ -25,13 +25,15 @@ LHS_ERRBIT_NONFINITE = 4
 LHS_ERRBIT_TIMEOUT = 8
 LHS_F32, LHS_F16, LHS_BF16, LHS_Q8_0 = 0, 1, 2, 3
 LHS_WIRE_F32, LHS_WIRE_F16, LHS_WIRE_I8 = 0, 1, 2
+LHS_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 LIB_PATH = _build.LIB
 
 # Exported symbols of the C-ABI, in declaration order.
 ABI_SYMBOLS = (
     "lhs_table_init", "lhs_table_info", "lhs_embed", "lhs_logits_topk_workspace",
-    "lhs_logits_topk", "lhs_logits", "lhs_wire_bytes", "lhs_wire_encode",
+    "lhs_logits_topk", "lhs_logits", "lhs_logits_topk_noalloc", "lhs_wire_bytes",
+    "lhs_wire_encode",
     "lhs_wire_decode", "lhs_selftest_bounded_wait", "lhs_strerror",
     "lhs_last_cuda_error", "lhs_version",
 )
@@ -75,6 +77,8 @@ def lib() -> ctypes.CDLL:
         "lhs_logits_topk": (ctypes.c_int, [T, P, i32, i32, i32, ctypes.c_float, P, P, P,
                                            P, sz, P, P]),
         "lhs_logits": (ctypes.c_int, [T, P, i32, i32, P, P, sz, P, P]),
+        "lhs_logits_topk_noalloc": (ctypes.c_int, [T, P, i32, i32, i32, ctypes.c_float, P,
+                                                   P, P, P, P]),
         "lhs_wire_bytes": (i64, [i32, i32, i32]),
         "lhs_wire_encode": (ctypes.c_int, [i32, P, i32, i32, i32, u32, u32, u32, P, sz,
                                            P, P]),
@@ -231,6 +235,28 @@ def lhs_logits(table: Table, resid: torch.Tensor, ws=None, out=None, err=None, s
                             ws.numel() * ws.element_size(), _dev(err, "err"),
                             _stream(stream)), "lhs_logits")
     return out, err
+
+
+def lhs_logits_topk_noalloc(table: Table, resid: torch.Tensor, k: int,
+                            temperature: float = 1.0, want_probs: bool = True, ids=None,
+                            logits=None, probs=None, err=None, stream=None):
+    """lhs_logits_topk with the library's built-in scratch instead of a
+    workspace, for callers that cannot allocate device memory on the call
+    path.  Returns (ids, logits, probs|None, err word)."""
+    B = resid.shape[0]
+    dev = table.device
+    ids = torch.empty((B, k), dtype=torch.int32, device=dev) if ids is None else ids
+    logits = torch.empty((B, k), dtype=torch.float32, device=dev) if logits is None else logits
+    if want_probs and probs is None:
+        probs = torch.empty((B, k), dtype=torch.float32, device=dev)
+    err = _err_word(err, dev)
+    _check(lib().lhs_logits_topk_noalloc(ctypes.byref(table.c), _dev(resid, "resid"),
+                                         _resid_dtype(resid), B, k, float(temperature),
+                                         _dev(ids, "ids"), _dev(logits, "logits"),
+                                         _dev(probs, "probs") if want_probs else None,
+                                         _dev(err, "err"), _stream(stream)),
+           "lhs_logits_topk_noalloc")
+    return ids, logits, (probs if want_probs else None), err
 
 
 def lhs_wire_bytes(fmt: int, seq_len: int, hidden: int) -> int:

@@ -149,6 +149,32 @@ LHS_API int lhs_logits(const lhs_table *t, const void *d_resid, int32_t resid_dt
                int32_t batch, float *d_logits, void *d_ws, size_t ws_bytes,
                int32_t *d_err, void *stream);
 
+/* Bytes of the fixed scratch array lhs_logits_topk_noalloc uses (4 MiB). */
+#define LHS_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+
+/* lhs_logits_topk for callers that cannot allocate device memory where they
+ * need top-k tokens — a plugin inside an application that owns the whole
+ * device memory budget through its own pool, or a latency-critical loop in
+ * which cudaMalloc/cudaFree (which may synchronise the device) is not
+ * acceptable.  No counterpart in the source pages (the paper): this is an
+ * interface convenience, not part of the method.
+ * Same arguments, results and errors as lhs_logits_topk minus the
+ * workspace: the scratch is an array of LHS_NOALLOC_SCRATCH_BYTES compiled
+ * into the library (each GPU that loads the library holds it until exit).
+ * A request whose lhs_logits_topk_workspace() size exceeds that limit
+ * returns LHS_ERR_BUFFER_TOO_SMALL and enqueues nothing (with 152 SMs, every
+ * batch <= 8 with k <= 128 and hidden <= 65536 fits).  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current): make that first call before any stream
+ * capture.  Allocates nothing.  All calls share the one array and it keeps
+ * the last call's contents (no part of it needs to start at zero); calls
+ * that overlap on the GPU — different streams or unordered host threads —
+ * race on it: serialise them. */
+LHS_API int lhs_logits_topk_noalloc(const lhs_table *t, const void *d_resid,
+                                    int32_t resid_dtype, int32_t batch, int32_t k,
+                                    float temperature, int32_t *d_ids, float *d_logits,
+                                    float *d_probs, int32_t *d_err, void *stream);
+
 /* Step 4 — residual wire codecs (ADR-0009 Wire Layout).
  * Message = 16-byte header [layer u32][seq_len u32][flags u32][top_k u32]
  * (little-endian) followed by the payload:
