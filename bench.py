@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--impl", default="lhs", choices=["lhs", "reference"])
     ap.add_argument("--workload", default="qwen05b", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--batch", type=int, default=None, help="lm_head batch (default: workload's first)")
+    ap.add_argument("--vocab", type=int, default=None,
+                    help="override the workload's vocab rows (small cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
@@ -174,12 +176,16 @@ class Ctx:
     pass
 
 
-def setup(name, batch, device):
+def setup(name, batch, device, vocab=None):
+    import dataclasses
+
     import torch
 
     import embedding_lookup_tied_gb300 as lhs
     c = Ctx()
     c.w = w = wl.WORKLOADS[name]
+    if vocab:
+        c.w = w = dataclasses.replace(w, vocab=vocab)
     c.B = batch or (w.batches[0] if w.batches else 1)
     c.k = w.k or 10
     c.fmt = w.wire[0] if w.wire else wl.WIRE_F16
@@ -238,8 +244,10 @@ def setup(name, batch, device):
     # the tensor-core path or GEMV alone on the CUDA-core path, then 1 merge;
     # wire encode 1; decode 1
     tc = w.dtype in (wl.F16, wl.BF16) and H % 8 == 0 and H >= 64 and w.vocab >= 128
+    gemm = tc and w.dtype == wl.BF16 and w.resid_dtype == wl.BF16 and c.B > 8
     passes = (c.B + 7) // 8
-    c.launches_per_step = 1 + (passes * (2 if tc else 1) + 1) + 1 + 1
+    lm = 2 if gemm else (passes * (2 if tc else 1) + 1)
+    c.launches_per_step = 1 + lm + 1 + 1
     return c
 
 
@@ -450,7 +458,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
-    c = setup(args.workload, args.batch, dev)
+    c = setup(args.workload, args.batch, dev, args.vocab)
     steps = args.steps or default_steps(args.workload)
     ms, lm_ms, clocks = time_device(c, steps, max(3, args.warmup), world)
     ms = max_over_ranks(ms, world, dev)

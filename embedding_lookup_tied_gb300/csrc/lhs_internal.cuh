@@ -153,8 +153,9 @@ cudaError_t launch_wire_decode(int fmt, const void *buf, int32_t seq_len, int32_
 
 // lm_head: plan (workspace layout + kernel choice) and launch
 struct LmHeadPlan {
-    int path;          // 0 = tensor-core streaming GEMV (f16/bf16 table, batch <= 8)
+    int path;          // 0 = tensor-core streaming GEMV (f16/bf16 table, batch <= 8 per pass)
                        // 1 = CUDA-core streaming GEMV (any table dtype)
+                       // 2 = tcgen05 GEMM (bf16 table, bf16 residuals, batch > 8)
     int grid;          // CTAs of the projection kernel (= partial top-k lists)
     int batch_chunk;   // residuals per pass of the projection
     int kpad;          // hidden rounded up for the tensor-core operand
@@ -171,6 +172,18 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
                            void *ws, int32_t *err, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int32_t *err, int64_t timeout_ns, cudaStream_t stream);
+
+// 2-D TMA map over a row-major [rows x cols] 16-bit matrix with the given
+// row pitch; box = box_cols x box_rows, 128-byte swizzle, zero fill outside.
+bool make_tma_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                        uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, bool bf16);
+
+// Batched lm_head on tcgen05 (bf16 table, bf16 residuals): clusters of two
+// CTAs; see gemm_tc.cu.
+int gemm_lm_head_clusters(const DeviceInfo &dev, int k);
+cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch, int k, float invT,
+                                float *raw, uint64_t *part_keys, float2 *part_ms, int32_t *err,
+                                int clusters, const DeviceInfo &dev, cudaStream_t stream);
 
 // Launch `kernel` as a programmatic dependent of the previous work in
 // `stream` (its prologue may overlap the tail of the preceding kernel).

@@ -727,6 +727,8 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // host helpers
 // ---------------------------------------------------------------------------
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -743,7 +745,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D map over a row-major [rows x cols] 16-bit matrix with a given row
 // pitch; box = box_cols x box_rows, 128-byte swizzle, zero fill outside.
-bool make_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+bool make_tma_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
                     uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, bool bf16) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -757,6 +759,8 @@ bool make_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint64_t 
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 constexpr size_t kTcSmemBytes = sizeof(TcSmem) + 1024;
 constexpr size_t kSimtXBytesMax = 96 * 1024;
@@ -774,17 +778,34 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dtype,
                  const DeviceInfo &dev, LmHeadPlan *plan) {
-    (void)resid_dtype;
     LmHeadPlan p{};
     // tensor-core path: 16-bit table, TMA-able rows (16-byte pitch), and at
     // least one full box in each dimension
     const bool tc = (t.dtype == LHS_F16 || t.dtype == LHS_BF16) && (t.hidden % 8 == 0) &&
                     t.hidden >= BK && t.vocab >= BM;
-    p.path = tc ? 0 : 1;
+    // batches beyond one GEMV pass, with operands that are exact in bf16,
+    // are a dense contraction: tcgen05 GEMM
+    bool gemm = tc && t.dtype == LHS_BF16 && resid_dtype == LHS_BF16 && batch > kBatchChunk &&
+                dev.num_sms >= 2;
     const int64_t units = (t.vocab + 15) / 16;
-    p.grid = static_cast<int>(units < dev.num_sms ? units : dev.num_sms);
     p.kpad = static_cast<int>(align_up(t.hidden, BK));
-    if (tc) {
+    int clusters = 0;
+    if (gemm) {
+        clusters = gemm_lm_head_clusters(dev, k);
+        // the epilogue stores vocab rows as 16-bit offsets within a cluster's range
+        const int64_t tiles = (t.vocab + 255) / 256;
+        if ((tiles + clusters - 1) / clusters * 256 > 65535) gemm = false;
+    }
+    p.path = gemm ? 2 : (tc ? 0 : 1);
+    if (gemm) {
+        p.grid = clusters;  // partial lists: one per cluster
+        p.batch_chunk = batch;
+    } else {
+        p.grid = static_cast<int>(units < dev.num_sms ? units : dev.num_sms);
+    }
+    if (gemm) {
+        // nothing else to size: the GEMM reads the residuals in place
+    } else if (tc) {
         p.batch_chunk = kBatchChunk;
         if (kTcSmemBytes > static_cast<size_t>(dev.max_smem_optin)) return LHS_ERR_UNSUPPORTED;
     } else {
@@ -800,7 +821,7 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
         return LHS_ERR_UNSUPPORTED;
     size_t off = 0;
     p.off_x = off;
-    off += tc ? align_up(static_cast<size_t>(16) * p.kpad * 2, 1024) : 0;
+    off += (tc && !gemm) ? align_up(static_cast<size_t>(16) * p.kpad * 2, 1024) : 0;
     p.off_keys = off;
     off += align_up(static_cast<size_t>(p.grid) * batch * kk * 8, 256);
     p.off_ms = off;
@@ -824,13 +845,17 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
     float2 *part_ms = reinterpret_cast<float2 *>(wsb + plan.off_ms);
     const size_t relt = resid_dtype == LHS_F32 ? 4 : 2;
 
-    if (plan.path == 0) {
+    if (plan.path == 2) {
+        e = launch_gemm_lm_head(t, resid, batch, k, invT, raw_logits, part_keys, part_ms, err,
+                                plan.grid, dev, stream);
+        if (e != cudaSuccess) return e;
+    } else if (plan.path == 0) {
         const bool bf16 = t.dtype == LHS_BF16;
         uint16_t *xs = reinterpret_cast<uint16_t *>(wsb + plan.off_x);
         CUtensorMap tm_a, tm_a16, tm_x;
-        if (!make_map_16bit(&tm_a, t.data, t.hidden, t.vocab, t.row_bytes, BK, BM, bf16) ||
-            !make_map_16bit(&tm_a16, t.data, t.hidden, t.vocab, t.row_bytes, BK, kBoxRowsSmall, bf16) ||
-            !make_map_16bit(&tm_x, xs, plan.kpad, 16, static_cast<uint64_t>(plan.kpad) * 2, BK, 16, bf16))
+        if (!make_tma_map_16bit(&tm_a, t.data, t.hidden, t.vocab, t.row_bytes, BK, BM, bf16) ||
+            !make_tma_map_16bit(&tm_a16, t.data, t.hidden, t.vocab, t.row_bytes, BK, kBoxRowsSmall, bf16) ||
+            !make_tma_map_16bit(&tm_x, xs, plan.kpad, 16, static_cast<uint64_t>(plan.kpad) * 2, BK, 16, bf16))
             return cudaErrorInvalidValue;
         auto kern = bf16 ? (raw ? gemv_tc_kernel<true, true> : gemv_tc_kernel<true, false>)
                          : (raw ? gemv_tc_kernel<false, true> : gemv_tc_kernel<false, false>);

@@ -210,6 +210,43 @@ def test_lm_head_parity(case):
         check_topk_against_fp64(ids[b], vals[b], L64[b], S64[b], k, rtol)
 
 
+GEMM_CASES = [
+    # bf16 table, bf16 residuals, batch > 8: tcgen05 GEMM path
+    # V, H, B, k
+    (5000, 512, 37, 20),      # ragged last vocab tile; second CTA of each pair idle
+    (1000, 96, 200, 64),      # hidden % 64 != 0; three stages
+    (700, 64, 256, 128),      # k = 128, two stages; both residual halves
+    (3000, 256, 130, 5),      # four stages; one residual in the second half
+]
+
+
+@pytest.mark.parametrize("case", GEMM_CASES, ids=[f"V{c[0]}-H{c[1]}-B{c[2]}-k{c[3]}"
+                                                  for c in GEMM_CASES])
+def test_gemm_lm_head_parity(case):
+    V, H, B, k = case
+    T = wl.make_table(orc.BF16, V, H, 0.02, cid=400 + V, threads=4)
+    R = wl.residuals(500 + B, B, H, (0.5, 8.0), orc.BF16)
+    tab = upload_table(T, orc.BF16, V, H)
+    rd = _resid_dev(R, orc.BF16)
+    xv = resid_values(R, orc.BF16)
+    L64, S64 = orc.logits(T, orc.BF16, V, H, xv, threads=8, with_sumabs=True)
+    raw, err = lhs.lhs_logits(tab, rd)
+    assert int(err.item()) == 0
+    Lg = raw.cpu().numpy()
+    assert np.all(np.abs(Lg.astype(np.float64) - L64) <= RTOL[orc.BF16] * S64 + 1e-30)
+    ids, vals, probs, err = lhs.lhs_logits_topk(tab, rd, k, temperature=1.3)
+    assert int(err.item()) == 0
+    ids, vals, probs = ids.cpu().numpy(), vals.cpu().numpy(), probs.cpu().numpy()
+    for b in range(B):
+        rid, rv = orc.topk_f32(Lg[b], k)
+        assert np.array_equal(ids[b], rid), b
+        assert np.array_equal(vals[b].view(np.uint32), rv.view(np.uint32)), b
+        rp = orc.softmax_probs(Lg[b], 1.3, rid)
+        assert np.all(np.abs(probs[b] - rp) <= PROB_RTOL * rp), b
+    for b in (0, B // 2, B - 1):
+        check_topk_against_fp64(ids[b], vals[b], L64[b], S64[b], k, RTOL[orc.BF16])
+
+
 @pytest.mark.parametrize("dtype", [orc.F16, orc.BF16, orc.F32])
 def test_lm_head_one_hot_and_integer_tables_exact(dtype):
     V, H = 777, 128
