@@ -12,13 +12,25 @@
 // operands K-major bf16 staged by TMA with 128-byte swizzle, the f32
 // accumulator lives in TMEM (2 x 256 columns, double-buffered so the MMAs
 // of the next tile overlap the epilogue of this one).  An epilogue thread
-// therefore owns one residual: it keeps its own running (max, sum exp) and
-// its own sorted top-k list in shared memory, with no cross-thread
-// reduction.
+// therefore owns one residual: its running (max, sum exp) and its top-k
+// candidates need no reduction across threads.
 //
 // CTAs run in clusters of two, one per half of the residuals.  Both need the
 // same 256-row table tile per stage: each CTA loads 128 rows and multicasts
 // them to both, so HBM reads every table row once per call.
+//
+// Top-k in two passes, so that the main pass keeps almost nothing:
+//  * sample pass: every cluster computes ONE tile (a stratified sample of
+//    clusters x 256 vocab rows); each epilogue thread keeps, for each of 32
+//    column groups of the tile, the largest logit, and a merge takes the
+//    exact top-k of all clusters' group maxima.  The k-th of those is a
+//    lower bound of the final k-th logit (the k-th largest of any subset of
+//    the logits never exceeds the k-th largest of all of them), and close
+//    to it: the sample's best logits almost never share a group.
+//  * main pass: every logit below that bound is dropped at once; the few
+//    others go to a per-(cluster, residual) candidate buffer in global
+//    memory, cut back to k by a warp-cooperative bitonic sort if it would
+//    overflow.  The merge selects the final top-k from the buffers.
 //
 // Roles (192 threads): warp 0 — TMA producer; warp 1 — TMEM allocation and
 // the single MMA-issuing thread; warps 2..5 — epilogue (TMEM lane quarter =
@@ -37,6 +49,7 @@ namespace {
 constexpr int GM = 128;                      // residuals per CTA (TMEM lanes)
 constexpr int GN = 256;                      // vocab rows per tile
 constexpr int GK = 64;                       // k per stage: 128 bytes of bf16
+constexpr int kStagesG = 4;
 constexpr int kGemmThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kAccCols = 256;                // f32 columns per accumulator buffer
@@ -45,32 +58,36 @@ constexpr int kAStageBytes = GM * GK * 2;    // 16 KB: this CTA's residuals
 constexpr int kBStageBytes = GN * GK * 2;    // 32 KB: the whole table tile
 constexpr int kBHalfBytes = kBStageBytes / 2;
 
+enum { kModeRaw = 0, kModeSample = 1, kModeMain = 2 };
+constexpr int kSampleLen = 32;               // sample keys per (cluster, residual)
+
 struct GemmParams {
     int64_t V;
     int K;
-    int B;            // residuals in the call
-    int k;            // top-k (0 = raw mode)
+    int B;                       // residuals in the call
+    int k;                       // top-k (sample / main)
     float invT;
-    int tiles;        // ceil(V / GN)
-    int clusters;     // clusters in the grid
-    float *raw;       // raw mode: [B x V]
-    uint64_t *part_keys;
-    float2 *part_ms;
+    int tiles;                   // ceil(V / GN)
+    int clusters;                // clusters in the grid
+    float *raw;                  // raw: [B x V]
+    uint64_t *keys;              // sample: [clusters][B][32]; main: [clusters][B][cap]
+    float2 *ms;                  // [clusters][B]
+    const float *sample_logits;  // main: [B][k] top-k logits of the sample, or null
+    int cap;                     // main: candidate buffer entries per (cluster, residual)
     int32_t *err;
 };
 
-template <int S>
 struct GemmSmem {
-    uint8_t a[S][kAStageBytes];
-    uint8_t b[S][kBStageBytes];
-    uint64_t full[S];
-    uint64_t empty[S];
+    uint8_t a[kStagesG][kAStageBytes];
+    uint8_t b[kStagesG][kBStageBytes];
+    uint64_t full[kStagesG];
+    uint64_t empty[kStagesG];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
     int abort_flag;
-    // followed by the top-k lists: list[i * GM + row], i < k
 };
+constexpr size_t kGemmSmemBytes = 1024 + sizeof(GemmSmem);
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -161,6 +178,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 __device__ __forceinline__ int ld_vol(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
 
+// bounded wait that gives up at once when the CTA has already aborted
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *abort_flag,
+                                              int32_t *err) {
+    if (ld_vol(abort_flag)) return false;
+    if (mbar_wait(bar, parity, kWaitTimeoutNs)) return true;
+    set_err(err, LHS_ERRBIT_TIMEOUT);
+    *reinterpret_cast<volatile int *>(abort_flag) = 1;
+    return false;
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22), enough for
+// the softmax normaliser (probabilities are checked to 1e-5).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // The bits of `mask` whose (logit, vocab row) key beats `tau` exactly.
 // Static indices only, so vals[] stays in registers.
 __device__ __forceinline__ uint32_t exact_mask(const float (&vals)[32], uint32_t mask, int64_t vc,
@@ -172,43 +207,6 @@ __device__ __forceinline__ uint32_t exact_mask(const float (&vals)[32], uint32_t
             if (topk_key(vals[j], static_cast<int32_t>(vc + j)) > tau) exact |= 1u << j;
     return exact;
 }
-
-// 2^x with the hardware approximation (relative error ~2^-22), enough for
-// the softmax normaliser (probabilities are checked to 1e-5).
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// bounded wait that gives up at once when the CTA has already aborted
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *abort_flag,
-                                              int32_t *err) {
-    if (ld_vol(abort_flag)) return false;
-    if (mbar_wait(bar, parity, kWaitTimeoutNs)) return true;
-    set_err(err, LHS_ERRBIT_TIMEOUT);
-    *reinterpret_cast<volatile int *>(abort_flag) = 1;
-    return false;
-}
-
-// Candidate buffers of the top-k epilogue.  Residual `row` of the CTA owns
-// entries [0, cnt) of keys32[i * GM + row] (order key of the logit) and
-// offs[i * GM + row] (vocab row - first row of the cluster's range), 6 bytes
-// per entry.  Each epilogue thread appends its own residual's candidates;
-// when a buffer could overflow, the warp cuts it back to the k best with a
-// bitonic sort in registers (E entries per lane).
-template <int S>
-struct TopkCap {
-    // entries per residual that fit beside S stages in 227 KB
-    static constexpr int value = S >= 4 ? 44 : (S == 3 ? 108 : 172);
-    static constexpr int sortn = value <= 64 ? 64 : (value <= 128 ? 128 : 256);
-};
-
-constexpr size_t kSmemOptin = 232448;  // 227 KB per CTA on sm_103a
-static_assert(1024 + sizeof(GemmSmem<4>) + 16 + TopkCap<4>::value * GM * 6 <= kSmemOptin, "S=4");
-static_assert(1024 + sizeof(GemmSmem<3>) + 16 + TopkCap<3>::value * GM * 6 <= kSmemOptin, "S=3");
-static_assert(1024 + sizeof(GemmSmem<2>) + 16 + TopkCap<2>::value * GM * 6 <= kSmemOptin, "S=2");
-static_assert(kMaxK + 32 <= TopkCap<2>::value, "largest k fits the two-stage buffers");
 
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
     const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), m);
@@ -254,61 +252,55 @@ struct BitonicStage {
     }
 };
 
-// Warp-collective: sort the n entries of residual `row` (full 64-bit keys,
-// id = id_base + off) descending and keep the first kk in the buffer.
-// Returns the kk-th key (0 when n < kk) in every lane.
+// Warp-collective: sort the n keys of one candidate buffer (global memory)
+// descending and keep the first kk.  Returns the kk-th key (0 when n < kk).
 template <int N>
-__device__ __forceinline__ uint64_t warp_cut(uint32_t *keys32, uint16_t *offs, int row, int n, int kk,
-                             uint32_t id_base, int lane) {
+__device__ __forceinline__ uint64_t warp_cut(uint64_t *buf, int n, int kk, int lane) {
     constexpr int E = N / 32;
     uint64_t v[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const int i = lane * E + e;
-        v[e] = i < n ? (static_cast<uint64_t>(keys32[i * GM + row]) << 32) |
-                           (0xFFFFFFFFu - (id_base + offs[i * GM + row]))
-                     : 0ull;
+        v[e] = i < n ? buf[i] : 0ull;
     }
-    BitonicStage<N, 1, 0>::run(v, lane);  // descending
+    BitonicStage<N, 1, 0>::run(v, lane);
     __syncwarp();  // every lane has read the buffer before it is rewritten
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const int i = lane * E + e;
-        if (i < kk && i < n) {
-            keys32[i * GM + row] = static_cast<uint32_t>(v[e] >> 32);
-            offs[i * GM + row] =
-                static_cast<uint16_t>((0xFFFFFFFFu - static_cast<uint32_t>(v[e])) - id_base);
-        }
+        if (i < kk && i < n) buf[i] = v[e];
     }
     __syncwarp();
     if (n < kk) return 0ull;
     const int idx = kk - 1;
-    // fetch element idx from its lane without indexing v[] at run time
     uint64_t sel = 0ull;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
+    for (int e = 0; e < E; ++e) {  // element idx from its lane, no run-time index into v[]
         const uint64_t t = shfl_u64(v[e], idx / E);
         if (e == idx % E) sel = t;
     }
     return sel;
 }
 
-template <int S, bool RAW>
+template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_t,
                    const GemmParams p) {
+    constexpr int S = kStagesG;
     extern __shared__ uint8_t dyn_smem[];
-    GemmSmem<S> &sm = *reinterpret_cast<GemmSmem<S> *>(
+    GemmSmem &sm = *reinterpret_cast<GemmSmem *>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
-    constexpr int CAP = TopkCap<S>::value;
-    uint32_t *keys32 = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(&sm) +
-                                                    ((sizeof(GemmSmem<S>) + 15) & ~size_t(15)));
-    uint16_t *offs = reinterpret_cast<uint16_t *>(keys32 + CAP * GM);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();          // residual half
     const int cl = blockIdx.x >> 1;                   // cluster index
-    const int t0 = static_cast<int>((static_cast<int64_t>(p.tiles) * cl) / p.clusters);
-    const int t1 = static_cast<int>((static_cast<int64_t>(p.tiles) * (cl + 1)) / p.clusters);
+    int t0, t1;
+    if (MODE == kModeSample) {  // one tile per cluster, spread over the vocab
+        t0 = static_cast<int>((static_cast<int64_t>(p.tiles) * cl) / p.clusters);
+        t1 = t0 + 1;
+    } else {
+        t0 = static_cast<int>((static_cast<int64_t>(p.tiles) * cl) / p.clusters);
+        t1 = static_cast<int>((static_cast<int64_t>(p.tiles) * (cl + 1)) / p.clusters);
+    }
     const int nk = (p.K + GK - 1) / GK;
     const uint32_t total = static_cast<uint32_t>(t1 - t0) * nk;
 
@@ -405,109 +397,156 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------- epilogue ----------------
-        pdl_wait();  // partial lists may still be read by the previous merge
+        pdl_wait();  // outputs may still be read, and the sample bound written, by earlier kernels
         const int q = warp & 3;                       // TMEM lane quarter
         const int row = q * 32 + lane;                // this thread's residual in the CTA
         const int b = static_cast<int>(rank) * GM + row;
         const bool valid = b < p.B;
-        float m_run = -INFINITY, s_run = 0.0f;
-        int cnt = 0;          // entries in this residual's buffer
-        uint64_t tau = 0ull;  // a key every kept entry beats (the k-th best after a cut)
-        float tau_val = -INFINITY;  // the logit of tau
-        const float l2e_invT = 1.4426950408889634f * p.invT;
-        const uint32_t id_base = static_cast<uint32_t>(t0) * GN;
-        for (int tile = t0, ti = 0; tile < t1; ++tile, ++ti) {
-            const int buf = ti & 1;
-            // the decision must be warp-uniform: tcgen05.ld is warp-collective
-            const bool ok = wait_or_abort(&sm.tmem_full[buf], (ti >> 1) & 1, &sm.abort_flag, p.err);
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            tc_fence_after();
-            const int64_t v0 = static_cast<int64_t>(tile) * GN;
-            for (int c = 0; c < kAccCols / 32; ++c) {
-                float vals[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols + c * 32, vals);
-                const int64_t vc = v0 + c * 32;
-                if (RAW) {
-                    if (valid)
-                        for (int j = 0; j < 32; ++j)
-                            if (vc + j < p.V) p.raw[static_cast<int64_t>(b) * p.V + vc + j] = vals[j];
-                    continue;
-                }
-                const int nvalid = valid ? static_cast<int>(p.V - vc < 32 ? (p.V - vc) : 32) : 0;
-                const uint32_t vmask = nvalid >= 32 ? 0xFFFFFFFFu : ((1u << nvalid) - 1u);
-                if (nvalid > 0) {
-                    float cmax = -INFINITY;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+
+        if (MODE == kModeRaw) {
+            for (int tile = t0, ti = 0; tile < t1; ++tile, ++ti) {
+                const int buf = ti & 1;
+                const bool ok = wait_or_abort(&sm.tmem_full[buf], (ti >> 1) & 1, &sm.abort_flag, p.err);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;  // tcgen05.ld is warp-collective
+                tc_fence_after();
+                const int64_t v0 = static_cast<int64_t>(tile) * GN;
+                for (int c = 0; c < kAccCols / 32; ++c) {
+                    float vals[32];
+                    tmem_ld32(tmem + lane_base + buf * kAccCols + c * 32, vals);
+                    const int64_t vc = v0 + c * 32;
+                    if (!valid) continue;
+                    float *dst = p.raw + static_cast<int64_t>(b) * p.V + vc;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if ((vmask >> j) & 1u) cmax = fmaxf(cmax, vals[j]);
-                    const float mn = fmaxf(m_run, cmax);
-                    if (mn != -INFINITY) {
-                        // exp((v - mn) / T) = 2^((v - mn) * log2(e) / T)
-                        float acc = s_run * ex2_approx((m_run - mn) * l2e_invT);
+                        if (vc + j < p.V) dst[j] = vals[j];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+            }
+        } else if (MODE == kModeSample) {
+            // the single tile's logits -> for each of the 32 column groups
+            // {j, j+32, ..., j+224} the largest (logit, row) key.  Any set of
+            // real logits gives a lower bound on the k-th largest; the
+            // group maxima hold nearly all of the tile's top logits.
+            const bool ok = t0 < t1 && wait_or_abort(&sm.tmem_full[0], 0, &sm.abort_flag, p.err);
+            if (__all_sync(0xFFFFFFFFu, ok)) {
+                tc_fence_after();
+                const int64_t v0 = static_cast<int64_t>(t0) * GN;
+                uint64_t best[kSampleLen];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if ((vmask >> j) & 1u) acc += ex2_approx((vals[j] - mn) * l2e_invT);
-                        s_run = acc;
-                        m_run = mn;
+                for (int j = 0; j < kSampleLen; ++j) best[j] = 0ull;
+                for (int c = 0; c < kAccCols / 32; ++c) {
+                    float vals[32];
+                    tmem_ld32(tmem + lane_base + c * 32, vals);
+                    const int64_t vc = v0 + c * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const uint64_t key = topk_key(vals[j], static_cast<int32_t>(vc + j));
+                        if (vc + j < p.V && key > best[j]) best[j] = key;
                     }
                 }
-                const uint32_t off0 = static_cast<uint32_t>(vc) - id_base;
-                // candidates: logits not below the threshold's value (NaN
-                // passes), then the exact (value, id) order for those only
-                uint32_t mask = 0;
+                if (valid) {
+                    uint64_t *dst = p.keys + (static_cast<size_t>(cl) * p.B + b) * kSampleLen;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (!(vals[j] < tau_val)) mask |= 1u << j;
-                mask &= vmask;
-                if (mask) mask = exact_mask(vals, mask, vc, tau);
-                // cut every buffer of the warp that this chunk could overflow
-                unsigned need = __ballot_sync(0xFFFFFFFFu, cnt + __popc(mask) > CAP);
+                    for (int j = 0; j < kSampleLen; ++j) dst[j] = best[j];
+                    p.ms[static_cast<size_t>(cl) * p.B + b] = make_float2(-INFINITY, 0.0f);
+                }
+            }
+        } else {
+            // main pass: running softmax; candidates above the sample's k-th
+            // logit into this residual's buffer in global memory
+            float m_run = -INFINITY, s_run = 0.0f;
+            int cnt = 0;
+            uint64_t tau = 0ull;       // exact key every kept entry beats (after a cut)
+            float tau_val = -INFINITY; // the logit below which nothing can be kept
+            if (valid && p.sample_logits) tau_val = p.sample_logits[static_cast<size_t>(b) * p.k + p.k - 1];
+            const float l2e_invT = 1.4426950408889634f * p.invT;
+            uint64_t *cand = p.keys + (static_cast<size_t>(cl) * p.B + (valid ? b : 0)) * p.cap;
+            uint64_t *cand_lane0 =
+                p.keys + (static_cast<size_t>(cl) * p.B + static_cast<int>(rank) * GM + q * 32) * p.cap;
+            for (int tile = t0, ti = 0; tile < t1; ++tile, ++ti) {
+                const int buf = ti & 1;
+                const bool ok = wait_or_abort(&sm.tmem_full[buf], (ti >> 1) & 1, &sm.abort_flag, p.err);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;  // tcgen05.ld is warp-collective
+                tc_fence_after();
+                const int64_t v0 = static_cast<int64_t>(tile) * GN;
+                for (int c = 0; c < kAccCols / 32; ++c) {
+                    float vals[32];
+                    tmem_ld32(tmem + lane_base + buf * kAccCols + c * 32, vals);
+                    const int64_t vc = v0 + c * 32;
+                    const int nvalid = valid ? static_cast<int>(p.V - vc < 32 ? (p.V - vc) : 32) : 0;
+                    const uint32_t vmask = nvalid >= 32 ? 0xFFFFFFFFu
+                                                        : (nvalid > 0 ? ((1u << nvalid) - 1u) : 0u);
+                    if (nvalid > 0) {
+                        float cmax = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if ((vmask >> j) & 1u) cmax = fmaxf(cmax, vals[j]);
+                        const float mn = fmaxf(m_run, cmax);
+                        if (mn != -INFINITY) {
+                            // exp((v - mn) / T) = 2^((v - mn) * log2(e) / T)
+                            float acc = s_run * ex2_approx((m_run - mn) * l2e_invT);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if ((vmask >> j) & 1u) acc += ex2_approx((vals[j] - mn) * l2e_invT);
+                            s_run = acc;
+                            m_run = mn;
+                        }
+                    }
+                    // candidates: not below the bound's value (NaN passes),
+                    // then the exact (value, id) order for those only
+                    uint32_t mask = 0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (!(vals[j] < tau_val)) mask |= 1u << j;
+                    mask &= vmask;
+                    if (mask) mask = exact_mask(vals, mask, vc, tau);
+                    // cut every buffer of the warp this chunk could overflow
+                    unsigned need = __ballot_sync(0xFFFFFFFFu, cnt + __popc(mask) > p.cap);
+                    while (need) {
+                        const int L = __ffs(need) - 1;
+                        need &= need - 1;
+                        const int nL = __shfl_sync(0xFFFFFFFFu, cnt, L);
+                        uint64_t *bufL = cand_lane0 + static_cast<size_t>(L) * p.cap;
+                        const uint64_t kth = p.cap <= 128 ? warp_cut<128>(bufL, nL, p.k, lane)
+                                                          : warp_cut<256>(bufL, nL, p.k, lane);
+                        if (lane == L) {
+                            cnt = nL < p.k ? nL : p.k;
+                            if (kth) {
+                                tau = kth;
+                                tau_val = fmaxf(tau_val, key_value(kth));
+                            }
+                            if (mask) mask = exact_mask(vals, mask, vc, tau);
+                        }
+                    }
+                    if (mask) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if ((mask >> j) & 1u) cand[cnt++] = topk_key(vals[j], static_cast<int32_t>(vc + j));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+            }
+            if (!ld_vol(&sm.abort_flag)) {
+                // cut buffers holding more than k, then pad to k
+                unsigned need = __ballot_sync(0xFFFFFFFFu, cnt > p.k);
                 while (need) {
                     const int L = __ffs(need) - 1;
                     need &= need - 1;
                     const int nL = __shfl_sync(0xFFFFFFFFu, cnt, L);
-                    const uint64_t kth = warp_cut<TopkCap<S>::sortn>(keys32, offs, q * 32 + L, nL,
-                                                                     p.k, id_base, lane);
-                    if (lane == L) {
-                        cnt = nL < p.k ? nL : p.k;
-                        tau = kth;
-                        tau_val = kth ? key_value(kth) : -INFINITY;
-                        // keep only what still beats the new k-th best
-                        if (mask) mask = exact_mask(vals, mask, vc, tau);
-                    }
+                    uint64_t *bufL = cand_lane0 + static_cast<size_t>(L) * p.cap;
+                    if (p.cap <= 128) warp_cut<128>(bufL, nL, p.k, lane);
+                    else warp_cut<256>(bufL, nL, p.k, lane);
+                    if (lane == L) cnt = p.k;
                 }
-                if (mask) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if ((mask >> j) & 1u) {
-                            keys32[cnt * GM + row] = order_key32(vals[j]);
-                            offs[cnt * GM + row] = static_cast<uint16_t>(off0 + j);
-                            ++cnt;
-                        }
-                    }
+                if (valid) {
+                    for (int i = cnt; i < p.k; ++i) cand[i] = 0ull;
+                    p.ms[static_cast<size_t>(cl) * p.B + b] = make_float2(m_run, s_run);
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
-        }
-        if (!RAW && !ld_vol(&sm.abort_flag)) {
-            // final cut of every buffer in the warp, then the partial list
-            unsigned need = __ballot_sync(0xFFFFFFFFu, cnt > p.k);
-            while (need) {
-                const int L = __ffs(need) - 1;
-                need &= need - 1;
-                const int nL = __shfl_sync(0xFFFFFFFFu, cnt, L);
-                warp_cut<TopkCap<S>::sortn>(keys32, offs, q * 32 + L, nL, p.k, id_base, lane);
-                if (lane == L) cnt = nL < p.k ? nL : p.k;
-            }
-            if (valid) {
-                uint64_t *dst = p.part_keys + (static_cast<size_t>(cl) * p.B + b) * p.k;
-                for (int i = 0; i < p.k; ++i)
-                    dst[i] = i < cnt ? (static_cast<uint64_t>(keys32[i * GM + row]) << 32) |
-                                           (0xFFFFFFFFu - (id_base + offs[i * GM + row]))
-                                     : 0ull;
-                p.part_ms[static_cast<size_t>(cl) * p.B + b] = make_float2(m_run, s_run);
             }
         }
     }
@@ -521,50 +560,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     cluster_sync_all();  // neither CTA leaves while its peer may still address it
 }
 
-template <int S>
-size_t gemm_smem_bytes(bool raw) {
-    return 1024 + ((sizeof(GemmSmem<S>) + 15) & ~size_t(15)) +
-           (raw ? 0 : static_cast<size_t>(TopkCap<S>::value) * GM * 6);
-}
-
-template <int S, bool RAW>
-cudaError_t launch_s(const lhs_table &t, const void *resid, int batch, int k, float invT, float *raw,
-                     uint64_t *part_keys, float2 *part_ms, int32_t *err, int clusters,
-                     const DeviceInfo &dev, cudaStream_t stream) {
-    CUtensorMap tm_x, tm_t;
-    if (!make_tma_map_16bit(&tm_x, resid, t.hidden, batch, static_cast<uint64_t>(t.hidden) * 2, GK, GM,
-                            true) ||
-        !make_tma_map_16bit(&tm_t, t.data, t.hidden, t.vocab, t.row_bytes, GK, GN / 2, true))
-        return cudaErrorInvalidValue;
-    const size_t smem = gemm_smem_bytes<S>(RAW);
-    auto kern = gemm_tc_kernel<S, RAW>;
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_t, const GemmParams &p,
+                        const DeviceInfo &dev, cudaStream_t stream) {
+    auto kern = gemm_tc_kernel<MODE>;
     {
         static std::mutex mu;
         static bool done[64] = {};
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev.device]) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 dev.max_smem_optin);
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(kGemmSmemBytes));
             if (e != cudaSuccess) return e;
             done[dev.device] = true;
         }
     }
-    GemmParams p;
-    p.V = t.vocab;
-    p.K = t.hidden;
-    p.B = batch;
-    p.k = k;
-    p.invT = invT;
-    p.tiles = static_cast<int>((t.vocab + GN - 1) / GN);
-    p.clusters = clusters;
-    p.raw = raw;
-    p.part_keys = part_keys;
-    p.part_ms = part_ms;
-    p.err = err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters);
+    cfg.gridDim = dim3(2 * p.clusters);
     cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -580,36 +594,24 @@ cudaError_t launch_s(const lhs_table &t, const void *resid, int batch, int k, fl
 
 }  // namespace
 
-// Stage count: as many as leave each residual's buffer room for k entries
-// plus one full 32-column chunk.
-static int gemm_stages(int k) {
-    if (k + 32 <= TopkCap<4>::value) return 4;
-    if (k + 32 <= TopkCap<3>::value) return 3;
-    return 2;
-}
+size_t gemm_lm_head_smem() { return kGemmSmemBytes; }
 
-size_t gemm_lm_head_smem(int k) {
-    switch (gemm_stages(k)) {
-    case 4: return gemm_smem_bytes<4>(false);
-    case 3: return gemm_smem_bytes<3>(false);
-    default: return gemm_smem_bytes<2>(false);
-    }
-}
+// Candidate buffer entries per (cluster, residual) in the main pass: room
+// for k plus at least one full chunk of 32 after a cut.
+int gemm_lm_head_cap(int k) { return k + 32 <= 128 ? 128 : 256; }
 
 // Clusters of two that can be resident at once (one CTA per SM), so the
 // grid is one wave.  Cached per device.
-int gemm_lm_head_clusters(const DeviceInfo &dev, int k) {
+int gemm_lm_head_clusters(const DeviceInfo &dev) {
     static std::mutex mu;
-    static int cache[64][3] = {};
-    const int kk = k < 1 ? 1 : k;
-    const int si = gemm_stages(kk) == 4 ? 0 : (gemm_stages(kk) == 3 ? 1 : 2);
+    static int cache[64] = {};
     std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev.device][si]) return cache[dev.device][si];
+    if (cache[dev.device]) return cache[dev.device];
     int n = dev.num_sms / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * n);
     cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = gemm_lm_head_smem(kk);
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -618,32 +620,58 @@ int gemm_lm_head_clusters(const DeviceInfo &dev, int k) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int active = 0;
-    const void *fn = si == 0 ? reinterpret_cast<const void *>(gemm_tc_kernel<4, false>)
-                   : si == 1 ? reinterpret_cast<const void *>(gemm_tc_kernel<3, false>)
-                             : reinterpret_cast<const void *>(gemm_tc_kernel<2, false>);
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
+    const void *fn = reinterpret_cast<const void *>(gemm_tc_kernel<kModeMain>);
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGemmSmemBytes));
     if (cudaOccupancyMaxActiveClusters(&active, fn, &cfg) == cudaSuccess && active > 0 && active < n)
         n = active;
     (void)cudaGetLastError();
     if (n < 1) n = 1;
-    cache[dev.device][si] = n;
+    cache[dev.device] = n;
     return n;
 }
 
+int gemm_lm_head_sample_len() { return kSampleLen; }
+
 cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch, int k, float invT,
-                                float *raw, uint64_t *part_keys, float2 *part_ms, int32_t *err,
-                                int clusters, const DeviceInfo &dev, cudaStream_t stream) {
-    const bool is_raw = raw != nullptr;
-    const int kk = is_raw ? 1 : k;
-    switch (gemm_stages(kk)) {
-    case 4:
-        return is_raw ? launch_s<4, true>(t, resid, batch, kk, invT, raw, part_keys, part_ms, err, clusters, dev, stream)
-                      : launch_s<4, false>(t, resid, batch, kk, invT, raw, part_keys, part_ms, err, clusters, dev, stream);
-    case 3:
-        return launch_s<3, false>(t, resid, batch, kk, invT, raw, part_keys, part_ms, err, clusters, dev, stream);
-    default:
-        return launch_s<2, false>(t, resid, batch, kk, invT, raw, part_keys, part_ms, err, clusters, dev, stream);
+                                float *raw, const GemmBuffers &bufs, int32_t *err, int clusters,
+                                const DeviceInfo &dev, cudaStream_t stream) {
+    CUtensorMap tm_x, tm_t;
+    if (!make_tma_map_16bit(&tm_x, resid, t.hidden, batch, static_cast<uint64_t>(t.hidden) * 2, GK, GM,
+                            true) ||
+        !make_tma_map_16bit(&tm_t, t.data, t.hidden, t.vocab, t.row_bytes, GK, GN / 2, true))
+        return cudaErrorInvalidValue;
+    GemmParams p = {};
+    p.V = t.vocab;
+    p.K = t.hidden;
+    p.B = batch;
+    p.k = k;
+    p.invT = invT;
+    p.tiles = static_cast<int>((t.vocab + GN - 1) / GN);
+    p.clusters = clusters;
+    p.err = err;
+    if (raw) {
+        p.raw = raw;
+        return launch_mode<kModeRaw>(tm_x, tm_t, p, dev, stream);
     }
+    cudaError_t e;
+    const float *bound = nullptr;
+    if (bufs.sample_keys) {
+        // sample pass and its merge: the exact top-k of one tile per cluster
+        GemmParams ps = p;
+        ps.keys = bufs.sample_keys;
+        ps.ms = bufs.sample_ms;
+        e = launch_mode<kModeSample>(tm_x, tm_t, ps, dev, stream);
+        if (e != cudaSuccess) return e;
+        e = launch_merge(bufs.sample_keys, bufs.sample_ms, clusters, kSampleLen, kSampleLen, batch, k,
+                         invT, bufs.sample_ids, bufs.sample_logits, nullptr, dev, stream);
+        if (e != cudaSuccess) return e;
+        bound = bufs.sample_logits;
+    }
+    p.keys = bufs.cand;
+    p.ms = bufs.ms;
+    p.cap = bufs.cap;
+    p.sample_logits = bound;
+    return launch_mode<kModeMain>(tm_x, tm_t, p, dev, stream);
 }
 
 }  // namespace lhs

@@ -160,8 +160,11 @@ struct LmHeadPlan {
     int batch_chunk;   // residuals per pass of the projection
     int kpad;          // hidden rounded up for the tensor-core operand
     size_t off_x;      // workspace offsets (bytes)
-    size_t off_keys;
+    size_t off_keys;   // partial lists (GEMM: candidate buffers)
     size_t off_ms;
+    size_t off_sample_keys, off_sample_ms, off_sample_ids, off_sample_logits;  // GEMM sample pass
+    int key_stride;    // entries between consecutive partial lists
+    bool sample;       // GEMM: run the sample pass
     size_t bytes;      // total workspace
 };
 int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dtype,
@@ -178,12 +181,31 @@ cudaError_t launch_selftest_wait(int32_t *err, int64_t timeout_ns, cudaStream_t 
 bool make_tma_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
                         uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, bool bf16);
 
+// Merge of per-CTA partial lists (stride entries apart, the first len of
+// each used) into the sorted top-k per residual, with probabilities when
+// `probs` is not null.
+cudaError_t launch_merge(const uint64_t *part_keys, const float2 *part_ms, int G, int stride,
+                         int len, int batch, int k, float invT, int32_t *ids, float *logits,
+                         float *probs, const DeviceInfo &dev, cudaStream_t stream);
+
 // Batched lm_head on tcgen05 (bf16 table, bf16 residuals): clusters of two
 // CTAs; see gemm_tc.cu.
-int gemm_lm_head_clusters(const DeviceInfo &dev, int k);
+struct GemmBuffers {
+    uint64_t *sample_keys;   // [clusters][batch][32], null: no sample pass
+    float2 *sample_ms;       // [clusters][batch]
+    int32_t *sample_ids;     // [batch][k]
+    float *sample_logits;    // [batch][k]
+    uint64_t *cand;          // [clusters][batch][cap]
+    float2 *ms;              // [clusters][batch]
+    int cap;
+};
+size_t gemm_lm_head_smem();
+int gemm_lm_head_cap(int k);
+int gemm_lm_head_sample_len();
+int gemm_lm_head_clusters(const DeviceInfo &dev);
 cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch, int k, float invT,
-                                float *raw, uint64_t *part_keys, float2 *part_ms, int32_t *err,
-                                int clusters, const DeviceInfo &dev, cudaStream_t stream);
+                                float *raw, const GemmBuffers &bufs, int32_t *err, int clusters,
+                                const DeviceInfo &dev, cudaStream_t stream);
 
 // Launch `kernel` as a programmatic dependent of the previous work in
 // `stream` (its prologue may overlap the tail of the preceding kernel).

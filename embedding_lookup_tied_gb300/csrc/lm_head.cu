@@ -670,18 +670,18 @@ struct MergeSmemHead {
 
 __global__ void __launch_bounds__(256)
     merge_kernel(const uint64_t *__restrict__ part_keys, const float2 *__restrict__ part_ms, int G,
-                 int batch_total, int k, float invT, int32_t *__restrict__ out_ids,
+                 int stride, int len, int batch_total, int k, float invT, int32_t *__restrict__ out_ids,
                  float *__restrict__ out_logits, float *__restrict__ out_probs) {
     extern __shared__ uint8_t dyn_smem[];
     MergeSmemHead &h = *reinterpret_cast<MergeSmemHead *>(dyn_smem);
     uint64_t *keys = reinterpret_cast<uint64_t *>(dyn_smem + ((sizeof(MergeSmemHead) + 15) & ~size_t(15)));
     const int b = blockIdx.x, tid = threadIdx.x;
-    const int n = G * k;
+    const int n = G * len;
     pdl_wait();
     pdl_trigger();
     for (int i = tid; i < n; i += 256) {
-        const int gi = i / k, j = i % k;
-        keys[i] = part_keys[(static_cast<size_t>(gi) * batch_total + b) * k + j];
+        const int gi = i / len, j = i % len;
+        keys[i] = part_keys[(static_cast<size_t>(gi) * batch_total + b) * stride + j];
     }
     if (tid < 32) {
         float2 acc = make_float2(-INFINITY, 0.0f);
@@ -791,7 +791,7 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
     p.kpad = static_cast<int>(align_up(t.hidden, BK));
     int clusters = 0;
     if (gemm) {
-        clusters = gemm_lm_head_clusters(dev, k);
+        clusters = gemm_lm_head_clusters(dev);
         // the epilogue stores vocab rows as 16-bit offsets within a cluster's range
         const int64_t tiles = (t.vocab + 255) / 256;
         if ((tiles + clusters - 1) / clusters * 256 > 65535) gemm = false;
@@ -817,15 +817,30 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
             return LHS_ERR_UNSUPPORTED;
     }
     const int kk = k > 0 ? k : 1;
-    if (k > 0 && merge_smem_bytes(p.grid, k) > static_cast<size_t>(dev.max_smem_optin))
+    if (k > 0 && merge_smem_bytes(p.grid, k > 32 ? k : 32) > static_cast<size_t>(dev.max_smem_optin))
         return LHS_ERR_UNSUPPORTED;
     size_t off = 0;
     p.off_x = off;
     off += (tc && !gemm) ? align_up(static_cast<size_t>(16) * p.kpad * 2, 1024) : 0;
+    p.key_stride = gemm ? gemm_lm_head_cap(kk) : kk;
     p.off_keys = off;
-    off += align_up(static_cast<size_t>(p.grid) * batch * kk * 8, 256);
+    off += align_up(static_cast<size_t>(p.grid) * batch * p.key_stride * 8, 256);
     p.off_ms = off;
     off += align_up(static_cast<size_t>(p.grid) * batch * 8, 256);
+    // GEMM sample pass: one tile per cluster, worth it when each cluster
+    // owns at least two tiles
+    p.sample = gemm && k > 0 && (t.vocab + 255) / 256 >= 2 * static_cast<int64_t>(p.grid);
+    p.off_sample_keys = p.off_sample_ms = p.off_sample_ids = p.off_sample_logits = off;
+    if (p.sample) {
+        p.off_sample_keys = off;
+        off += align_up(static_cast<size_t>(p.grid) * batch * gemm_lm_head_sample_len() * 8, 256);
+        p.off_sample_ms = off;
+        off += align_up(static_cast<size_t>(p.grid) * batch * 8, 256);
+        p.off_sample_ids = off;
+        off += align_up(static_cast<size_t>(batch) * k * 4, 256);
+        p.off_sample_logits = off;
+        off += align_up(static_cast<size_t>(batch) * k * 4, 256);
+    }
     p.bytes = off;
     *plan = p;
     return LHS_OK;
@@ -846,8 +861,15 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
     const size_t relt = resid_dtype == LHS_F32 ? 4 : 2;
 
     if (plan.path == 2) {
-        e = launch_gemm_lm_head(t, resid, batch, k, invT, raw_logits, part_keys, part_ms, err,
-                                plan.grid, dev, stream);
+        GemmBuffers gb;
+        gb.sample_keys = plan.sample ? reinterpret_cast<uint64_t *>(wsb + plan.off_sample_keys) : nullptr;
+        gb.sample_ms = reinterpret_cast<float2 *>(wsb + plan.off_sample_ms);
+        gb.sample_ids = reinterpret_cast<int32_t *>(wsb + plan.off_sample_ids);
+        gb.sample_logits = reinterpret_cast<float *>(wsb + plan.off_sample_logits);
+        gb.cand = part_keys;
+        gb.ms = part_ms;
+        gb.cap = plan.key_stride;
+        e = launch_gemm_lm_head(t, resid, batch, k, invT, raw_logits, gb, err, plan.grid, dev, stream);
         if (e != cudaSuccess) return e;
     } else if (plan.path == 0) {
         const bool bf16 = t.dtype == LHS_BF16;
@@ -932,21 +954,27 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
         }
     }
     if (raw) return cudaSuccess;
-    const size_t msmem = merge_smem_bytes(plan.grid, k);
+    return launch_merge(part_keys, part_ms, plan.grid, plan.key_stride, k, batch, k, invT, ids,
+                        logits_out, probs, dev, stream);
+}
+
+cudaError_t launch_merge(const uint64_t *part_keys, const float2 *part_ms, int G, int stride,
+                         int len, int batch, int k, float invT, int32_t *ids, float *logits,
+                         float *probs, const DeviceInfo &dev, cudaStream_t stream) {
+    const size_t msmem = merge_smem_bytes(G, len);
     {
         static std::mutex mu;
         static bool done[64] = {};
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev.device]) {
-            e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     dev.max_smem_optin);
+            const cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       dev.max_smem_optin);
             if (e != cudaSuccess) return e;
             done[dev.device] = true;
         }
     }
-    return launch_pdl(merge_kernel, dim3(batch), dim3(256), msmem, stream, part_keys, part_ms,
-                      plan.grid, static_cast<int>(batch), static_cast<int>(k), invT, ids, logits_out,
-                      probs);
+    return launch_pdl(merge_kernel, dim3(batch), dim3(256), msmem, stream, part_keys, part_ms, G,
+                      stride, len, batch, k, invT, ids, logits, probs);
 }
 
 // ---------------------------------------------------------------------------

@@ -216,7 +216,9 @@ GEMM_CASES = [
     (5000, 512, 37, 20),      # ragged last vocab tile; second CTA of each pair idle
     (1000, 96, 200, 64),      # hidden % 64 != 0; three stages
     (700, 64, 256, 128),      # k = 128, two stages; both residual halves
-    (3000, 256, 130, 5),      # four stages; one residual in the second half
+    (3000, 256, 130, 5),      # one residual in the second half
+    (40000, 128, 150, 20),    # >= 2 tiles per cluster: sample pass + main pass
+    (39000, 64, 256, 128),    # sample pass with k = 128 (256-entry buffers)
 ]
 
 
