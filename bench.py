@@ -240,13 +240,9 @@ def setup(name, batch, device, vocab=None):
                              c.dec.data_ptr(), c.err.data_ptr(), c.sptr)),
     ]
     c.lm_call = c.calls[1]
-    # kernels per step: embed 1; lm_head: per 8-residual pass (prep + GEMV) on
-    # the tensor-core path or GEMV alone on the CUDA-core path, then 1 merge;
-    # wire encode 1; decode 1
-    tc = w.dtype in (wl.F16, wl.BF16) and H % 8 == 0 and H >= 64 and w.vocab >= 128
-    gemm = tc and w.dtype == wl.BF16 and w.resid_dtype == wl.BF16 and c.B > 8
-    passes = (c.B + 7) // 8
-    lm = 2 if gemm else (passes * (2 if tc else 1) + 1)
+    # kernels per step: embed 1, the lm_head call as the library reports it
+    # for this plan, wire encode 1, decode 1
+    lm = lhs.lhs_logits_topk_launches(c.table, c.B, c.k, rd)
     c.launches_per_step = 1 + lm + 1 + 1
     return c
 

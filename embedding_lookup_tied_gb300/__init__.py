@@ -32,7 +32,7 @@ LIB_PATH = _build.LIB
 # Exported symbols of the C-ABI, in declaration order.
 ABI_SYMBOLS = (
     "lhs_table_init", "lhs_table_info", "lhs_embed", "lhs_logits_topk_workspace",
-    "lhs_logits_topk", "lhs_logits", "lhs_logits_topk_noalloc", "lhs_wire_bytes",
+    "lhs_logits_topk_launches", "lhs_logits_topk", "lhs_logits", "lhs_logits_topk_noalloc", "lhs_wire_bytes",
     "lhs_wire_encode",
     "lhs_wire_decode", "lhs_selftest_bounded_wait", "lhs_strerror",
     "lhs_last_cuda_error", "lhs_version",
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         "lhs_table_info": (ctypes.c_int, [T, P, P, P, P]),
         "lhs_embed": (ctypes.c_int, [T, P, i64, ctypes.c_float, P, P, P]),
         "lhs_logits_topk_workspace": (ctypes.c_int, [T, i32, i32, i32, P]),
+        "lhs_logits_topk_launches": (ctypes.c_int, [T, i32, i32, i32, P]),
         "lhs_logits_topk": (ctypes.c_int, [T, P, i32, i32, i32, ctypes.c_float, P, P, P,
                                            P, sz, P, P]),
         "lhs_logits": (ctypes.c_int, [T, P, i32, i32, P, P, sz, P, P]),
@@ -193,6 +194,13 @@ def lhs_logits_topk_workspace(table: Table, batch: int, k: int, resid_dtype: int
     _check(lib().lhs_logits_topk_workspace(ctypes.byref(table.c), batch, k, resid_dtype,
                                            ctypes.byref(b)), "lhs_logits_topk_workspace")
     return b.value
+
+
+def lhs_logits_topk_launches(table: Table, batch: int, k: int, resid_dtype: int) -> int:
+    n = ctypes.c_int32()
+    _check(lib().lhs_logits_topk_launches(ctypes.byref(table.c), batch, k, resid_dtype,
+                                          ctypes.byref(n)), "lhs_logits_topk_launches")
+    return n.value
 
 
 def lhs_logits_topk(table: Table, resid: torch.Tensor, k: int, temperature: float = 1.0,

@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     embed_kernel(const uint8_t *__restrict__ table, int64_t vocab, int hidden, int64_t row_bytes,
                  const int32_t *__restrict__ ids, int64_t n, float scale, float *__restrict__ out,
                  int32_t *err) {
+    pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -121,7 +122,6 @@ __global__ void __launch_bounds__(kWarps * 32)
             }
         }
     }
-    pdl_trigger();
 }
 
 template <int DT>

@@ -130,6 +130,23 @@ int lhs_logits_topk_workspace(const lhs_table *t, int32_t batch, int32_t k, int3
     return LHS_OK;
 }
 
+int lhs_logits_topk_launches(const lhs_table *t, int32_t batch, int32_t k, int32_t resid_dtype,
+                             int32_t *launches) {
+    if (!launches) return LHS_ERR_INVALID_ARG;
+    int rc = check_table(t);
+    if (rc) return rc;
+    if (resid_dtype != LHS_F32 && resid_dtype != LHS_BF16) return LHS_ERR_INVALID_ARG;
+    if (batch < 1 || k < 0 || k > kMaxK || k > t->vocab) return LHS_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    LmHeadPlan plan;
+    rc = plan_lm_head(*t, batch, k, resid_dtype, dev, &plan);
+    if (rc) return rc;
+    *launches = lm_head_launches(plan, batch, k == 0);
+    return LHS_OK;
+}
+
 int lhs_logits_topk(const lhs_table *t, const void *d_resid, int32_t resid_dtype, int32_t batch,
                     int32_t k, float temperature, int32_t *d_ids, float *d_logits, float *d_probs,
                     void *d_ws, size_t ws_bytes, int32_t *d_err, void *stream) {

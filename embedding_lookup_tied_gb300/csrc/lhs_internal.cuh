@@ -109,10 +109,12 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
 // Programmatic dependent launch.  pdl_wait(): block until the preceding
 // kernel in the stream has completed and its memory is visible (a no-op when
 // this kernel was not launched as a dependent).  pdl_trigger(): allow the
-// next kernel in the stream to start its prologue now.  Every kernel here
-// calls pdl_wait() before it reads anything an earlier kernel may write and
-// before it writes anything an earlier kernel may read, and only then
-// pdl_trigger().
+// next kernel in the stream to be scheduled now.  Every kernel here triggers
+// at its start and calls pdl_wait() before it reads anything an earlier
+// kernel may write and before it writes anything an earlier kernel may read.
+// The wait covers the whole earlier kernel's completion, not its trigger, so
+// the early trigger only lets the next kernel become resident and run its
+// prologue (barrier setup, table prefetch) sooner.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -169,6 +171,9 @@ struct LmHeadPlan {
 };
 int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dtype,
                  const DeviceInfo &dev, LmHeadPlan *plan);
+// Kernel launches one lhs_logits_topk (raw = false) or lhs_logits (raw =
+// true) call with this plan enqueues.
+int lm_head_launches(const LmHeadPlan &plan, int32_t batch, bool raw);
 cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const void *resid,
                            int32_t resid_dtype, int32_t batch, int32_t k, float temperature,
                            int32_t *ids, float *logits_out, float *probs, float *raw_logits,

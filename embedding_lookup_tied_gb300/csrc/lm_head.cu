@@ -259,24 +259,217 @@ __device__ void topk_round_end(TopkShared &sm, int tid, int nthreads, int ncols,
 }
 
 // Final cut to k and write the CTA's partial list and (m, s) per column.
+// Each list is written sorted, largest key first, and padded with 0 (below
+// every key).  A candidate's place is the number of larger candidates in its
+// column (keys are unique), so when the lists are short every candidate is
+// ranked directly — one pass, no selection rounds; otherwise a radix select
+// first cuts each column to k.
+constexpr int kRankWork = 512;  // comparisons per thread for the direct ranking
+
 __device__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
                             int b_off, int batch_total, uint64_t *part_keys, float2 *part_ms,
                             float invT) {
     named_bar_sync(kBarAll, nthreads);
-    {
+    int work = 0;
+    for (int b = 0; b < ncols; ++b) work += sm.cnt[b] * sm.cnt[b];
+    if (work > nthreads * kRankWork) {  // uniform: every thread read the same counts
         const Group g = make_group(tid, nthreads, ncols);
         if (g.col < ncols) group_compact(sm.cand + g.col * cap, &sm.cnt[g.col], &sm.tau[g.col], k, sm, g);
+        named_bar_sync(kBarAll, nthreads);
     }
-    named_bar_sync(kBarAll, nthreads);
-    for (int b = 0; b < ncols; ++b) {
-        uint64_t *dst = part_keys + (static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k;
+    int total = 0;
+    for (int b = 0; b < ncols; ++b) total += sm.cnt[b];
+    for (int i = tid; i < total; i += nthreads) {
+        int b = 0, j = i;
+        while (j >= sm.cnt[b]) j -= sm.cnt[b++];
         const int n = sm.cnt[b];
-        for (int i = tid; i < k; i += nthreads) dst[i] = i < n ? sm.cand[b * cap + i] : 0ull;
+        const uint64_t *src = sm.cand + b * cap;
+        const uint64_t key = src[j];
+        int rank = 0;
+        for (int q = 0; q < n; ++q) rank += src[q] > key;
+        if (rank < k)
+            part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + rank] = key;
+    }
+    for (int i = tid; i < ncols * k; i += nthreads) {
+        const int b = i / k, j = i % k;
+        if (j >= sm.cnt[b])
+            part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + j] = 0ull;
     }
     if (tid < ncols) {
         float2 acc = make_float2(-INFINITY, 0.0f);
         for (int w = 0; w < kConsumerWarps; ++w) acc = ms_combine(acc, sm.ms_warp[w][tid], invT);
         part_ms[static_cast<size_t>(blockIdx.x) * batch_total + b_off + tid] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// merge: global top-k of one residual from G partial lists, sorted, + probs.
+// Executed by 256 threads synchronised with named barrier `bar_id`.
+// ---------------------------------------------------------------------------
+struct MergeSmemHead {
+    uint64_t sel[kMaxK];
+    uint64_t tmin;
+    unsigned hist[256];
+    float2 ms;
+    int nsel, sel_digit, sel_above;
+};
+
+__device__ void merge_column(const uint64_t *part_keys, const float2 *part_ms, int G, int stride,
+                             int len, int batch_total, int b, int k, float invT, int32_t *out_ids,
+                             float *out_logits, float *out_probs, MergeSmemHead &h, uint64_t *keys,
+                             int tid, int bar_id) {
+    const int n = G * len;
+    // all loads of a batch are issued before the first store
+    constexpr int U = 8;
+    for (int base = 0; base < n; base += U * 256) {
+        uint64_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * 256 + tid;
+            v[u] = i < n ? __ldcg(part_keys + (static_cast<size_t>(i / len) * batch_total + b) * stride + i % len)
+                         : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * 256 + tid;
+            if (i < n) keys[i] = v[u];
+        }
+    }
+    if (tid < 32) {
+        float2 acc = make_float2(-INFINITY, 0.0f);
+        float2 o[4];
+        for (int g0 = 0; g0 < G; g0 += 128) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int gi = g0 + 32 * u + tid;
+                o[u] = gi < G ? __ldcg(part_ms + static_cast<size_t>(gi) * batch_total + b)
+                              : make_float2(-INFINITY, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc = ms_combine(acc, o[u], invT);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float2 other;
+            other.x = __shfl_xor_sync(0xFFFFFFFFu, acc.x, o);
+            other.y = __shfl_xor_sync(0xFFFFFFFFu, acc.y, o);
+            acc = ms_combine(acc, other, invT);
+        }
+        if (tid == 0) h.ms = acc;
+    }
+    named_bar_sync(bar_id, 256);
+    Group g;
+    g.gtid = tid;
+    g.T = 256;
+    g.bar_id = bar_id;
+    g.col = 0;
+    uint64_t prefix, mask;
+    group_radix_select(keys, n, k, h.hist, &h.sel_digit, &h.sel_above, g, prefix, mask);
+    if (tid == 0) h.nsel = 0;
+    named_bar_sync(bar_id, 256);
+    for (int i = tid; i < n; i += 256) {
+        const uint64_t key = keys[i];
+        if ((key & mask) >= prefix) h.sel[atomicAdd(&h.nsel, 1)] = key;
+    }
+    named_bar_sync(bar_id, 256);
+    // rank sort (keys unique): position = number of larger keys
+    if (tid < k) {
+        const uint64_t mine = h.sel[tid];
+        int rank = 0;
+        for (int j = 0; j < k; ++j) rank += h.sel[j] > mine;
+        const size_t o = static_cast<size_t>(b) * k + rank;
+        const float v = key_value(mine);
+        out_ids[o] = key_id(mine);
+        out_logits[o] = v;
+        if (out_probs) out_probs[o] = expf((v - h.ms.x) * invT) / h.ms.y;
+    }
+    named_bar_sync(bar_id, 256);  // h and keys are free for the next column
+}
+
+// ---------------------------------------------------------------------------
+// merge of sorted lists.  The GEMV kernels write each CTA's list sorted,
+// largest key first, padded with 0 (below every key).  One block per
+// residual:
+//  1. thread i < G reads the first R = min(k, kMergeR) entries of list i,
+//     all in one round of L2 reads;
+//  2. a lower bound L of the global k-th key: the k-th largest of the first
+//     m = ceil(k/G) entries of every list (G*m >= k keys, so at least k keys
+//     are >= L);
+//  3. the candidates: the entries >= L of every list (a prefix of each),
+//     gathered in shared memory;
+//  4. a candidate's rank among the candidates is its final position: every
+//     key above a candidate is >= L, hence a candidate itself.
+// A list whose R read entries are all >= L (it may hold more), a bound of 0
+// (fewer than k keys in the sampled prefixes) or more than kMergeCand
+// candidates sends the block to a one-key-at-a-time extraction from the
+// list heads in L2 instead (merge_extract_warp).
+// ---------------------------------------------------------------------------
+constexpr int kMergeThreads = 256;             // >= G
+constexpr int kMergeR = 16;                    // entries read per list
+constexpr int kMergeSet = 2 * kMergeThreads;   // G*m <= G + k - 1 < 512
+constexpr int kMergeCand = 1024;
+
+struct MergeSmem {
+    uint64_t set[kMergeSet];
+    uint64_t cand[kMergeCand];
+    float2 ms[kMergeThreads];
+    int scan[kMergeThreads / 32];
+    uint64_t bound;
+    float2 msf;
+    int fallback;
+};
+
+// Slow path: the top-k taken one key at a time from the list heads, read
+// from L2 by one warp; lane l follows lists l, l+32, ... (G <= 256).
+__device__ void merge_extract_warp(const uint64_t *part_keys, int G, int batch_total, int b, int k,
+                                   float invT, float2 ms, int32_t *out_ids, float *out_logits,
+                                   float *out_probs, int lane) {
+    constexpr int S = kMergeThreads / 32;
+    uint64_t head[S];
+    int pos[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+        const int gi = lane + 32 * j;
+        head[j] = gi < G ? __ldcg(part_keys + (static_cast<size_t>(gi) * batch_total + b) * k) : 0ull;
+        pos[j] = 0;
+    }
+    for (int r = 0; r < k; ++r) {
+        uint64_t best = 0ull;
+        int bj = 0;
+#pragma unroll
+        for (int j = 0; j < S; ++j)
+            if (head[j] > best) {
+                best = head[j];
+                bj = j;
+            }
+        uint64_t wbest = best;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, wbest, o);
+            wbest = other > wbest ? other : wbest;
+        }
+        if (lane == 0) {
+            const size_t o = static_cast<size_t>(b) * k + r;
+            const float v = key_value(wbest);
+            out_ids[o] = key_id(wbest);
+            out_logits[o] = v;
+            if (out_probs) out_probs[o] = expf((v - ms.x) * invT) / ms.y;
+        }
+        if (best == wbest && best != 0ull) {  // the one lane whose list held it
+            int pb = 0;
+#pragma unroll
+            for (int j = 0; j < S; ++j) pb = j == bj ? pos[j] : pb;
+            const int gi = lane + 32 * bj;
+            const int pn = pb + 1;
+            const uint64_t nk =
+                pn < k ? __ldcg(part_keys + (static_cast<size_t>(gi) * batch_total + b) * k + pn) : 0ull;
+#pragma unroll
+            for (int j = 0; j < S; ++j)
+                if (j == bj) {
+                    head[j] = nk;
+                    pos[j] = pn;
+                }
+        }
     }
 }
 
@@ -297,8 +490,8 @@ template <bool BF16T, int XDT>
 __global__ void __launch_bounds__(256)
     prep_kernel(const void *__restrict__ resid, int Bc, int K, int Kp, uint16_t *__restrict__ xs,
                 int32_t *err) {
-    pdl_wait();     // x may come from the previous kernel; xs may still be read by it
     pdl_trigger();  // the projection may start streaming the table now
+    pdl_wait();     // x may come from the previous kernel; xs may still be read by it
     const int64_t total = static_cast<int64_t>(8) * Kp;
     int bad = 0;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -600,8 +793,8 @@ __global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtPa
     int q = 1;
     while (q < p.Bc) q <<= 1;
     const int cap = kCandTotal / q;
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
 
     for (int64_t i = tid; i < static_cast<int64_t>(p.Bc) * p.K; i += kSimtThreads) {
         float v;
@@ -660,13 +853,6 @@ __global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtPa
 // ---------------------------------------------------------------------------
 // merge: global top-k per residual from G partial lists, sorted, + probs
 // ---------------------------------------------------------------------------
-struct MergeSmemHead {
-    uint64_t sel[kMaxK];
-    uint64_t tmin;
-    unsigned hist[256];
-    float2 ms;
-    int nsel, sel_digit, sel_above;
-};
 
 __global__ void __launch_bounds__(256)
     merge_kernel(const uint64_t *__restrict__ part_keys, const float2 *__restrict__ part_ms, int G,
@@ -675,18 +861,43 @@ __global__ void __launch_bounds__(256)
     extern __shared__ uint8_t dyn_smem[];
     MergeSmemHead &h = *reinterpret_cast<MergeSmemHead *>(dyn_smem);
     uint64_t *keys = reinterpret_cast<uint64_t *>(dyn_smem + ((sizeof(MergeSmemHead) + 15) & ~size_t(15)));
-    const int b = blockIdx.x, tid = threadIdx.x;
-    const int n = G * len;
-    pdl_wait();
     pdl_trigger();
-    for (int i = tid; i < n; i += 256) {
-        const int gi = i / len, j = i % len;
-        keys[i] = part_keys[(static_cast<size_t>(gi) * batch_total + b) * stride + j];
+    pdl_wait();
+    merge_column(part_keys, part_ms, G, stride, len, batch_total, blockIdx.x, k, invT, out_ids,
+                 out_logits, out_probs, h, keys, threadIdx.x, 1);
+}
+
+// Merge of the GEMV kernels' sorted lists, one block per residual (steps
+// 1-4 above).  The host guarantees G <= kMergeThreads and ceil(k/G) <= kMergeR.
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_sorted_kernel(const uint64_t *__restrict__ part_keys, const float2 *__restrict__ part_ms,
+                        int G, int batch_total, int k, float invT, int32_t *__restrict__ out_ids,
+                        float *__restrict__ out_logits, float *__restrict__ out_probs) {
+    __shared__ MergeSmem sm;
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = k < kMergeR ? k : kMergeR;
+    const int m = (k + G - 1) / G;
+    // 1. one round of reads: list `tid`'s first R entries and its (max, sum)
+    uint64_t e[kMergeR];
+    const uint64_t *list = part_keys + (static_cast<size_t>(tid) * batch_total + b) * k;
+#pragma unroll
+    for (int j = 0; j < kMergeR; ++j) e[j] = (tid < G && j < R) ? __ldcg(list + j) : 0ull;
+    if (tid < G) sm.ms[tid] = __ldcg(part_ms + static_cast<size_t>(tid) * batch_total + b);
+    if (tid == 0) {
+        sm.bound = 0ull;
+        sm.fallback = 0;
     }
-    if (tid < 32) {
+    if (tid < G) {
+#pragma unroll
+        for (int j = 0; j < kMergeR; ++j)
+            if (j < m) sm.set[tid * m + j] = e[j];
+    }
+    __syncthreads();
+    if (warp == 0) {
         float2 acc = make_float2(-INFINITY, 0.0f);
-        for (int gi = tid; gi < G; gi += 32)
-            acc = ms_combine(acc, part_ms[static_cast<size_t>(gi) * batch_total + b], invT);
+        for (int gi = lane; gi < G; gi += 32) acc = ms_combine(acc, sm.ms[gi], invT);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             float2 other;
@@ -694,33 +905,65 @@ __global__ void __launch_bounds__(256)
             other.y = __shfl_xor_sync(0xFFFFFFFFu, acc.y, o);
             acc = ms_combine(acc, other, invT);
         }
-        if (tid == 0) h.ms = acc;
+        if (lane == 0) sm.msf = acc;
     }
-    __syncthreads();
-    Group g;
-    g.gtid = tid;
-    g.T = 256;
-    g.bar_id = 1;
-    g.col = 0;
-    uint64_t prefix, mask;
-    group_radix_select(keys, n, k, h.hist, &h.sel_digit, &h.sel_above, g, prefix, mask);
-    if (tid == 0) h.nsel = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += 256) {
-        const uint64_t key = keys[i];
-        if ((key & mask) >= prefix) h.sel[atomicAdd(&h.nsel, 1)] = key;
-    }
-    __syncthreads();
-    // rank sort (keys unique): position = number of larger keys
-    if (tid < k) {
-        const uint64_t mine = h.sel[tid];
+    // 2. the bound: the sampled key of rank k-1 (nonzero keys are unique)
+    const int na = G * m;
+    for (int i = tid; i < na; i += kMergeThreads) {
+        const uint64_t x = sm.set[i];
         int rank = 0;
-        for (int j = 0; j < k; ++j) rank += h.sel[j] > mine;
-        const size_t o = static_cast<size_t>(b) * k + rank;
-        const float v = key_value(mine);
-        out_ids[o] = key_id(mine);
-        out_logits[o] = v;
-        if (out_probs) out_probs[o] = expf((v - h.ms.x) * invT) / h.ms.y;
+        for (int q = 0; q < na; ++q) rank += sm.set[q] > x;
+        if (rank == k - 1) sm.bound = x;
+    }
+    __syncthreads();
+    const uint64_t L = sm.bound;
+    // 3. each list's prefix >= L, placed by a block-wide exclusive scan
+    int n = 0;
+    if (tid < G) {
+#pragma unroll
+        for (int j = 0; j < kMergeR; ++j) n += (j < R && e[j] >= L) ? 1 : 0;
+        if (n == R && R < k) sm.fallback = 1;
+    }
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) sm.scan[warp] = incl;
+    __syncthreads();
+    int off = incl - n, total = 0;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) {
+        off += w < warp ? sm.scan[w] : 0;
+        total += sm.scan[w];
+    }
+    const bool slow = L == 0ull || sm.fallback || total > kMergeCand;  // uniform
+    if (!slow && tid < G) {
+#pragma unroll
+        for (int j = 0; j < kMergeR; ++j)
+            if (j < n) sm.cand[off + j] = e[j];
+    }
+    __syncthreads();
+    const float2 ms = sm.msf;
+    if (slow) {
+        if (warp == 0)
+            merge_extract_warp(part_keys, G, batch_total, b, k, invT, ms, out_ids, out_logits, out_probs,
+                               lane);
+        return;
+    }
+    // 4. rank among the candidates = final position
+    for (int i = tid; i < total; i += kMergeThreads) {
+        const uint64_t x = sm.cand[i];
+        int rank = 0;
+        for (int q = 0; q < total; ++q) rank += sm.cand[q] > x;
+        if (rank < k) {
+            const size_t o = static_cast<size_t>(b) * k + rank;
+            const float v = key_value(x);
+            out_ids[o] = key_id(x);
+            out_logits[o] = v;
+            if (out_probs) out_probs[o] = expf((v - ms.x) * invT) / ms.y;
+        }
     }
 }
 
@@ -773,6 +1016,7 @@ size_t merge_smem_bytes(int G, int k) {
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
 
 }  // namespace
 
@@ -844,6 +1088,13 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
     p.bytes = off;
     *plan = p;
     return LHS_OK;
+}
+
+int lm_head_launches(const LmHeadPlan &plan, int32_t batch, bool raw) {
+    if (plan.path == 2) return raw ? 1 : (plan.sample ? 4 : 2);
+    const int chunks = (batch + plan.batch_chunk - 1) / plan.batch_chunk;
+    const int per_chunk = plan.path == 0 ? 2 : 1;  // (prep +) projection
+    return chunks * per_chunk + (raw ? 0 : 1);
 }
 
 cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const void *resid,
@@ -954,6 +1205,11 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
         }
     }
     if (raw) return cudaSuccess;
+    if (plan.path != 2 && plan.grid <= kMergeThreads && (k + plan.grid - 1) / plan.grid <= kMergeR)
+        return launch_pdl(merge_sorted_kernel, dim3(batch), dim3(kMergeThreads), 0, stream,
+                          static_cast<const uint64_t *>(part_keys), static_cast<const float2 *>(part_ms),
+                          plan.grid, static_cast<int>(batch), static_cast<int>(k), invT, ids, logits_out,
+                          probs);
     return launch_merge(part_keys, part_ms, plan.grid, plan.key_stride, k, batch, k, invT, ids,
                         logits_out, probs, dev, stream);
 }

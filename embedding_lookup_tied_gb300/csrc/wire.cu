@@ -66,6 +66,7 @@ template <int FMT, int XDT, bool VEC>
 __global__ void __launch_bounds__(kEwThreads)
     encode_ew_kernel(const void *__restrict__ x, int64_t n, uint32_t layer, uint32_t seq_len,
                      uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf) {
+    pdl_trigger();
     pdl_wait();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -95,7 +96,6 @@ __global__ void __launch_bounds__(kEwThreads)
         else
             reinterpret_cast<float *>(pay)[i] = v;
     }
-    pdl_trigger();
 }
 
 // ---- f32 / f16 decode ------------------------------------------------------
@@ -103,6 +103,7 @@ template <int FMT, bool VEC>
 __global__ void __launch_bounds__(kEwThreads)
     decode_ew_kernel(const uint8_t *__restrict__ buf, int64_t n, uint32_t seq_len,
                      float *__restrict__ x, int32_t *err) {
+    pdl_trigger();
     pdl_wait();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -138,7 +139,6 @@ __global__ void __launch_bounds__(kEwThreads)
         else
             x[i] = __ldg(reinterpret_cast<const float *>(pay) + i);
     }
-    pdl_trigger();
 }
 
 // ---- i8 encode -------------------------------------------------------------
@@ -176,6 +176,7 @@ template <int XDT, bool VEC>
 __global__ void __launch_bounds__(kI8Threads)
     encode_i8_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
                      uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    pdl_trigger();
     pdl_wait();
     __shared__ float sm_m[kI8Threads / 32];
     __shared__ int sm_f[kI8Threads / 32];
@@ -266,7 +267,6 @@ __global__ void __launch_bounds__(kI8Threads)
                 pos[8 + j] = static_cast<uint8_t>(i8_code(load_x<XDT>(x, xrow + j), scale));
         }
     }
-    pdl_trigger();
 }
 
 // ---- i8 decode -------------------------------------------------------------
@@ -274,6 +274,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kI8Threads)
     decode_i8_kernel(const uint8_t *__restrict__ buf, int32_t seq_len, int32_t hidden,
                      float *__restrict__ x, int32_t *err) {
+    pdl_trigger();
     pdl_wait();
     const uint32_t hdr_seq = __ldg(reinterpret_cast<const uint32_t *>(buf) + 1);
     if (hdr_seq != static_cast<uint32_t>(seq_len)) {
@@ -322,7 +323,6 @@ __global__ void __launch_bounds__(kI8Threads)
                 xo[j] = __fmul_rn(static_cast<float>(static_cast<int8_t>(__ldg(pos + 8 + j))), scale);
         }
     }
-    pdl_trigger();
 }
 
 int ew_grid(int64_t work_items, int num_sms) {

@@ -118,6 +118,15 @@ LHS_API int lhs_embed(const lhs_table *t, const int32_t *d_ids, int64_t n, float
 LHS_API int lhs_logits_topk_workspace(const lhs_table *t, int32_t batch, int32_t k,
                               int32_t resid_dtype, size_t *bytes);
 
+/* Kernel launches one lhs_logits_topk call (k >= 1) or lhs_logits call
+ * (k == 0) with these arguments enqueues on the current device: the
+ * projection's passes over the table plus, where it runs as a kernel of its
+ * own, the cross-CTA merge.  For launch accounting and CUDA-graph sizing; no
+ * counterpart in the source pages.  Errors as for
+ * lhs_logits_topk_workspace. */
+LHS_API int lhs_logits_topk_launches(const lhs_table *t, int32_t batch, int32_t k,
+                             int32_t resid_dtype, int32_t *launches);
+
 /* Steps 2+3 — tied lm_head projection with fused top-k (ADR-0008
  * POST /v1/logits: residual @ lm_head.T over every vocab row, top_k entries
  * {token_id, prob}; HELIX §5: the projection needs all vocab rows).

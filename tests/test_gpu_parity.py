@@ -157,6 +157,9 @@ LM_CASES = [
     (orc.BF16, 8191, 96, 8, 40, orc.F32),     # ragged vocab, hidden % 64 != 0
     (orc.BF16, 1500, 64, 11, 7, orc.BF16),    # two batch passes, bf16 residuals
     (orc.F16, 300, 128, 1, 128, orc.F32),     # k = kMax
+    (orc.BF16, 5000, 128, 2, 128, orc.F32),   # k = kMax over every SM: lists deeper than staged
+    (orc.BF16, 20000, 64, 8, 50, orc.F32),    # one full pass, 8 residuals
+    (orc.F16, 20000, 64, 12, 50, orc.F32),    # two passes
     (orc.BF16, 128, 64, 2, 1, orc.F32),       # one block, k = 1
     (orc.F32, 1000, 256, 4, 5, orc.F32),      # CUDA-core path
     (orc.Q8_0, 700, 128, 2, 10, orc.F32),     # CUDA-core path
@@ -208,6 +211,22 @@ def test_lm_head_parity(case):
         rp = orc.softmax_probs(Lg[b], 0.7, rid)
         assert np.all(np.abs(probs[b] - rp) <= PROB_RTOL * rp), b
         check_topk_against_fp64(ids[b], vals[b], L64[b], S64[b], k, rtol)
+
+
+def test_launch_count_follows_the_plan():
+    V = 5000
+    T = wl.make_table(orc.BF16, V, 128, 0.02, cid=250, threads=4)
+    tab = upload_table(T, orc.BF16, V, 128)
+    n = functools.partial(lhs.lhs_logits_topk_launches, tab)
+    assert n(1, 10, lhs.LHS_F32) == 3                      # prep + GEMV + merge
+    assert n(8, 128, lhs.LHS_BF16) == 3
+    assert n(9, 10, lhs.LHS_F32) == 5                      # two passes + merge
+    assert n(3, 0, lhs.LHS_F32) == 2                       # raw logits: no merge
+    assert n(64, 10, lhs.LHS_BF16) in (2, 4)               # GEMM (+ sample pass and its merge)
+    assert n(64, 0, lhs.LHS_BF16) == 1
+    T32 = wl.make_table(orc.F32, 1000, 64, 0.02, cid=251, threads=4)
+    tab32 = upload_table(T32, orc.F32, 1000, 64)
+    assert lhs.lhs_logits_topk_launches(tab32, 4, 5, lhs.LHS_F32) == 2
 
 
 GEMM_CASES = [
@@ -295,6 +314,43 @@ def test_topk_planted_ties_break_by_id(dtype):
         top = ids.cpu().numpy()[b]
         same = Lg[b][top] == Lg[b][top[0]]
         assert np.all(np.diff(top[same]) > 0)
+
+
+def _topk_matches_own_logits(tab, X, k, temperature=1.0):
+    ids, vals, probs, err = lhs.lhs_logits_topk(tab, X, k, temperature=temperature)
+    assert int(err.item()) == 0
+    raw, _ = lhs.lhs_logits(tab, X)
+    Lg = raw.cpu().numpy()
+    ids, vals, probs = ids.cpu().numpy(), vals.cpu().numpy(), probs.cpu().numpy()
+    for b in range(Lg.shape[0]):
+        rid, rv = orc.topk_f32(Lg[b], k)
+        assert np.array_equal(ids[b], rid), b
+        assert np.array_equal(vals[b].view(np.uint32), rv.view(np.uint32)), b
+        rp = orc.softmax_probs(Lg[b], temperature, rid)
+        assert np.all(np.abs(probs[b] - rp) <= PROB_RTOL * rp), b
+
+
+def test_topk_clustered_in_one_cta_range():
+    # the 64 largest logits sit in the first rows, i.e. in one or two CTAs'
+    # row ranges: the merge cannot bound them from a few entries per list
+    V, H, k = 5000, 64, 40
+    T = wl.make_table(orc.BF16, V, H, 0.02, cid=260, threads=4)
+    col0 = (1.0 + np.arange(64, dtype=np.float32) / 128.0)
+    T[:64, 0] = wl.f32_to_bf16_bits(col0)
+    tab = upload_table(T, orc.BF16, V, H)
+    X = wl.residuals(261, 2, H)
+    X[:, 0] = 4.0
+    _topk_matches_own_logits(tab, to_dev(X), k, temperature=0.9)
+
+
+def test_topk_when_some_cta_lists_are_short():
+    # 129 rows over 9 CTAs, the last with a single row: k = 128 needs nearly
+    # every row and the sampled list prefixes hold padding
+    V, H, k = 129, 64, 128
+    T = wl.make_table(orc.BF16, V, H, 0.02, cid=262, threads=1)
+    tab = upload_table(T, orc.BF16, V, H)
+    X = wl.residuals(263, 3, H)
+    _topk_matches_own_logits(tab, to_dev(X), k)
 
 
 def test_f16_table_residual_out_of_range_flags_nonfinite():
