@@ -204,16 +204,25 @@ __device__ void group_compact(uint64_t *keys, int *cnt, uint64_t *tau, int kk, T
     group_sync(g);
 }
 
+// Online softmax state (m, s): s = sum exp((v - m) / T) over the values
+// seen, m their max.  Of the two rescalings exp((m - m') / T) and
+// exp((v - m') / T) one has a zero argument, i.e. is exactly 1, so only the
+// other is evaluated.
 __device__ __forceinline__ void ms_update(float &m, float &s, float v, float invT) {
     const float mn = fmaxf(m, v);
     if (mn == -INFINITY) return;
-    s = s * expf((m - mn) * invT) + expf((v - mn) * invT);
-    m = mn;
+    if (m >= v) {
+        s = s + expf((v - mn) * invT);
+    } else {
+        s = s * expf((m - mn) * invT) + 1.0f;
+        m = mn;
+    }
 }
 __device__ __forceinline__ float2 ms_combine(float2 a, float2 b, float invT) {
     const float mn = fmaxf(a.x, b.x);
     if (mn == -INFINITY) return make_float2(-INFINITY, 0.0f);
-    return make_float2(mn, a.y * expf((a.x - mn) * invT) + b.y * expf((b.x - mn) * invT));
+    if (a.x >= b.x) return make_float2(a.x, a.y + b.y * expf((b.x - a.x) * invT));
+    return make_float2(b.x, b.y + a.y * expf((a.x - b.x) * invT));
 }
 
 __device__ __forceinline__ void topk_init(TopkShared &sm, int tid, int nthreads) {
@@ -388,36 +397,46 @@ __device__ void merge_column(const uint64_t *part_keys, const float2 *part_ms, i
 
 // ---------------------------------------------------------------------------
 // merge of sorted lists.  The GEMV kernels write each CTA's list sorted,
-// largest key first, padded with 0 (below every key).  One block per
-// residual:
-//  1. thread i < G reads the first R = min(k, kMergeR) entries of list i,
-//     all in one round of L2 reads;
-//  2. a lower bound L of the global k-th key: the k-th largest of the first
-//     m = ceil(k/G) entries of every list (G*m >= k keys, so at least k keys
-//     are >= L);
-//  3. the candidates: the entries >= L of every list (a prefix of each),
+// largest key first, padded with 0 (below every key).  Per residual, 256
+// threads (a merge block, or the consumers of the GEMV's last CTA):
+//  1. the first R entries of every list and the lists' (max, sum) pairs are
+//     staged in shared memory, in one round of L2 reads for all residuals;
+//  2. a lower bound L of the global k-th key: from the first m = ceil(k/G)
+//     entries of every list (G*m >= k keys), the k-th largest logit order
+//     key (the upper 32 bits), with the id bits cleared — at least k keys
+//     are >= L;
+//  3. the candidates: the entries >= L of every list, a prefix of each
+//     (lists whose R staged entries are all >= L are read on from L2),
 //     gathered in shared memory;
 //  4. a candidate's rank among the candidates is its final position: every
 //     key above a candidate is >= L, hence a candidate itself.
-// A list whose R read entries are all >= L (it may hold more), a bound of 0
-// (fewer than k keys in the sampled prefixes) or more than kMergeCand
-// candidates sends the block to a one-key-at-a-time extraction from the
-// list heads in L2 instead (merge_extract_warp).
+// A bound of 0 (fewer than k keys in the sampled prefixes: tiny CTAs) or
+// more than kMergeCand candidates (the top keys crowded into few lists)
+// sends the residual to a one-key-at-a-time extraction from the list heads
+// in L2 instead (merge_extract_warp): slower, same result.
 // ---------------------------------------------------------------------------
 constexpr int kMergeThreads = 256;             // >= G
-constexpr int kMergeR = 16;                    // entries read per list
+constexpr int kMergeR = 16;                    // most entries staged per list
 constexpr int kMergeSet = 2 * kMergeThreads;   // G*m <= G + k - 1 < 512
 constexpr int kMergeCand = 1024;
 
-struct MergeSmem {
-    uint64_t set[kMergeSet];
+struct MergeWork {
     uint64_t cand[kMergeCand];
-    float2 ms[kMergeThreads];
-    int scan[kMergeThreads / 32];
-    uint64_t bound;
+    uint32_t set[kMergeSet];
+    uint32_t bound;
+    int total;
     float2 msf;
-    int fallback;
 };
+
+// Entries of every list the merge stages: enough for the bound (m) and for
+// the few entries per list a residual's top-k usually takes (about 2k/G).
+__host__ __device__ __forceinline__ int merge_stage_entries(int G, int k) {
+    const int m = (k + G - 1) / G;
+    int r = 4 + (4 * k + G - 1) / G;
+    if (r < m) r = m;
+    if (r > kMergeR) r = kMergeR > m ? kMergeR : m;
+    return r < k ? r : k;
+}
 
 // Slow path: the top-k taken one key at a time from the list heads, read
 // from L2 by one warp; lane l follows lists l, l+32, ... (G <= 256).
@@ -471,6 +490,157 @@ __device__ void merge_extract_warp(const uint64_t *part_keys, int G, int batch_t
                 }
         }
     }
+}
+
+// Step 1 for residual b: lists[G][R] and sms[G].  All loads of a round are
+// issued before the first store; list and entry indexes advance by adding
+// (no division per load).
+__device__ void stage_sorted_lists(const uint64_t *part_keys, const float2 *part_ms, int G, int k, int R,
+                                   int batch_total, int b, uint64_t *lists, float2 *sms, int tid,
+                                   int nthreads) {
+    constexpr int U = 16;
+    const int n = G * R;
+    float2 mv = tid < G ? __ldcg(part_ms + static_cast<size_t>(tid) * batch_total + b)
+                        : make_float2(-INFINITY, 0.0f);
+    const int dc = nthreads / R, dr = nthreads % R;
+    for (int base = 0; base < n; base += U * nthreads) {
+        int c = (base + tid) / R, j = (base + tid) % R;
+        uint64_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            v[u] = base + u * nthreads + tid < n
+                       ? __ldcg(part_keys + (static_cast<size_t>(c) * batch_total + b) * k + j)
+                       : 0ull;
+            c += dc;
+            j += dr;
+            if (j >= R) {
+                j -= R;
+                ++c;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * nthreads + tid < n) lists[base + u * nthreads + tid] = v[u];
+    }
+    if (tid < G) sms[tid] = mv;
+}
+
+// Steps 2-4 for residual b, by 256 threads synchronised on named barrier
+// `bar_id`.  lists: [G][R] staged entries (R >= ceil(k/G)), sms: [G].  The
+// phases are short dependent chains, so independent work runs side by side:
+// the last warp folds the G (max, sum) pairs while the others rank the
+// sampled keys, and candidates are appended with one shared atomic per warp
+// instead of a block-wide scan.
+__device__ void merge_column_sorted(const uint64_t *lists, int R, const float2 *sms, int G, int k,
+                                    float invT, const uint64_t *part_keys, int batch_total, int b,
+                                    int32_t *out_ids, float *out_logits, float *out_probs, MergeWork &w,
+                                    int tid, int bar_id) {
+    const int lane = tid & 31, warp = tid >> 5;
+    constexpr int kMsWarp = kMergeThreads / 32 - 1;
+    const int m = (k + G - 1) / G;
+    const int na = G * m;
+    const int na4 = (na + 3) & ~3;
+    if (tid == 0) {
+        w.bound = 0u;
+        w.total = 0;
+    }
+    for (int i = tid; i < na4; i += kMergeThreads) {
+        const int gi = m == 1 ? i : i / m;
+        w.set[i] = i < na ? static_cast<uint32_t>(lists[gi * R + (i - gi * m)] >> 32) : 0u;
+    }
+    named_bar_sync(bar_id, kMergeThreads);
+    if (warp == kMsWarp) {
+        // (max, sum) over the lists
+        float2 acc = make_float2(-INFINITY, 0.0f);
+        for (int gi = lane; gi < G; gi += 32) acc = ms_combine(acc, sms[gi], invT);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float2 other;
+            other.x = __shfl_xor_sync(0xFFFFFFFFu, acc.x, o);
+            other.y = __shfl_xor_sync(0xFFFFFFFFu, acc.y, o);
+            acc = ms_combine(acc, other, invT);
+        }
+        if (lane == 0) w.msf = acc;
+    }
+    // 2. the bound: the k-th largest sampled order key (ties allowed); the
+    //    ms warp joins only when the sample needs every thread
+    const uint4 *set4 = reinterpret_cast<const uint4 *>(w.set);
+    const int nw4 = na4 / 4;
+    const int nrank = na < kMsWarp * 32 ? kMsWarp * 32 : kMergeThreads;
+    if (warp != kMsWarp || nrank == kMergeThreads) {
+        for (int i = tid; i < na; i += nrank) {
+            const uint32_t x = w.set[i];
+            int gt = 0, ge = 0;
+#pragma unroll 4
+            for (int q = 0; q < nw4; ++q) {
+                const uint4 y = set4[q];
+                gt += (y.x > x) + (y.y > x) + (y.z > x) + (y.w > x);
+                ge += (y.x >= x) + (y.y >= x) + (y.z >= x) + (y.w >= x);
+            }
+            if (gt < k && ge >= k) w.bound = x;
+        }
+    }
+    named_bar_sync(bar_id, kMergeThreads);
+    const uint64_t L = static_cast<uint64_t>(w.bound) << 32;
+    // 3. each list's prefix >= L (lists that may go on are read on from L2),
+    //    appended at a position taken with one shared atomic per warp
+    int n = 0;
+    const uint64_t *glist = part_keys + (static_cast<size_t>(tid) * batch_total + b) * k;
+    if (tid < G && L != 0ull) {
+        while (n < R && lists[tid * R + n] >= L) ++n;
+        if (n == R) {
+            while (n < k) {
+                uint64_t v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = n + u < k ? __ldcg(glist + n + u) : 0ull;
+                int c = 0;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) c += (c == u && v[u] >= L) ? 1 : 0;
+                n += c;
+                if (c < 8) break;
+            }
+        }
+    }
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int base = 0;
+    if (lane == 31 && incl) base = atomicAdd(&w.total, incl);
+    const int off = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - n;
+    if (L != 0ull) {
+        for (int j = 0; j < n && j < R; ++j)
+            if (off + j < kMergeCand) w.cand[off + j] = lists[tid * R + j];
+        for (int j = R; j < n; ++j)
+            if (off + j < kMergeCand) w.cand[off + j] = __ldcg(glist + j);
+    }
+    named_bar_sync(bar_id, kMergeThreads);
+    const int total = w.total;
+    const bool slow = L == 0ull || total > kMergeCand;  // uniform
+    const float2 ms = w.msf;
+    if (slow) {
+        if (warp == 0)
+            merge_extract_warp(part_keys, G, batch_total, b, k, invT, ms, out_ids, out_logits, out_probs,
+                               lane);
+    } else {
+        // 4. rank among the candidates = final position
+        for (int i = tid; i < total; i += kMergeThreads) {
+            const uint64_t x = w.cand[i];
+            int rank = 0;
+#pragma unroll 4
+            for (int q = 0; q < total; ++q) rank += w.cand[q] > x;
+            if (rank < k) {
+                const size_t o = static_cast<size_t>(b) * k + rank;
+                const float v = key_value(x);
+                out_ids[o] = key_id(x);
+                out_logits[o] = v;
+                if (out_probs) out_probs[o] = expf((v - ms.x) * invT) / ms.y;
+            }
+        }
+    }
+    named_bar_sync(bar_id, kMergeThreads);  // w is free for the next residual
 }
 
 // Row range of CTA c: 16-row units split evenly.
@@ -736,6 +906,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // above, so every consumer reads the same value here
         if (ld_volatile(&sm.tk.abort_flag)) break;
     }
+    // the flag only changes inside the main loop: uniform here
     if (RAW || ld_volatile(&sm.tk.abort_flag)) return;
     // per-warp (m, s) for columns 2t, 2t+1: reduce over g (lanes t, t+4, ...)
 #pragma unroll
@@ -867,104 +1038,22 @@ __global__ void __launch_bounds__(256)
                  out_logits, out_probs, h, keys, threadIdx.x, 1);
 }
 
-// Merge of the GEMV kernels' sorted lists, one block per residual (steps
-// 1-4 above).  The host guarantees G <= kMergeThreads and ceil(k/G) <= kMergeR.
+// Merge of the GEMV kernels' sorted lists, one block per residual.  The
+// host guarantees G <= kMergeThreads and R = merge_stage_entries(G, k).
 __global__ void __launch_bounds__(kMergeThreads)
     merge_sorted_kernel(const uint64_t *__restrict__ part_keys, const float2 *__restrict__ part_ms,
-                        int G, int batch_total, int k, float invT, int32_t *__restrict__ out_ids,
+                        int G, int batch_total, int k, int R, float invT, int32_t *__restrict__ out_ids,
                         float *__restrict__ out_logits, float *__restrict__ out_probs) {
-    __shared__ MergeSmem sm;
+    __shared__ MergeWork w;
+    extern __shared__ uint64_t lists[];  // [G][R], then G float2
+    float2 *sms = reinterpret_cast<float2 *>(lists + G * R);
     pdl_trigger();
     pdl_wait();
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int R = k < kMergeR ? k : kMergeR;
-    const int m = (k + G - 1) / G;
-    // 1. one round of reads: list `tid`'s first R entries and its (max, sum)
-    uint64_t e[kMergeR];
-    const uint64_t *list = part_keys + (static_cast<size_t>(tid) * batch_total + b) * k;
-#pragma unroll
-    for (int j = 0; j < kMergeR; ++j) e[j] = (tid < G && j < R) ? __ldcg(list + j) : 0ull;
-    if (tid < G) sm.ms[tid] = __ldcg(part_ms + static_cast<size_t>(tid) * batch_total + b);
-    if (tid == 0) {
-        sm.bound = 0ull;
-        sm.fallback = 0;
-    }
-    if (tid < G) {
-#pragma unroll
-        for (int j = 0; j < kMergeR; ++j)
-            if (j < m) sm.set[tid * m + j] = e[j];
-    }
+    stage_sorted_lists(part_keys, part_ms, G, k, R, batch_total, blockIdx.x, lists, sms, threadIdx.x,
+                       kMergeThreads);
     __syncthreads();
-    if (warp == 0) {
-        float2 acc = make_float2(-INFINITY, 0.0f);
-        for (int gi = lane; gi < G; gi += 32) acc = ms_combine(acc, sm.ms[gi], invT);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float2 other;
-            other.x = __shfl_xor_sync(0xFFFFFFFFu, acc.x, o);
-            other.y = __shfl_xor_sync(0xFFFFFFFFu, acc.y, o);
-            acc = ms_combine(acc, other, invT);
-        }
-        if (lane == 0) sm.msf = acc;
-    }
-    // 2. the bound: the sampled key of rank k-1 (nonzero keys are unique)
-    const int na = G * m;
-    for (int i = tid; i < na; i += kMergeThreads) {
-        const uint64_t x = sm.set[i];
-        int rank = 0;
-        for (int q = 0; q < na; ++q) rank += sm.set[q] > x;
-        if (rank == k - 1) sm.bound = x;
-    }
-    __syncthreads();
-    const uint64_t L = sm.bound;
-    // 3. each list's prefix >= L, placed by a block-wide exclusive scan
-    int n = 0;
-    if (tid < G) {
-#pragma unroll
-        for (int j = 0; j < kMergeR; ++j) n += (j < R && e[j] >= L) ? 1 : 0;
-        if (n == R && R < k) sm.fallback = 1;
-    }
-    int incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) sm.scan[warp] = incl;
-    __syncthreads();
-    int off = incl - n, total = 0;
-#pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) {
-        off += w < warp ? sm.scan[w] : 0;
-        total += sm.scan[w];
-    }
-    const bool slow = L == 0ull || sm.fallback || total > kMergeCand;  // uniform
-    if (!slow && tid < G) {
-#pragma unroll
-        for (int j = 0; j < kMergeR; ++j)
-            if (j < n) sm.cand[off + j] = e[j];
-    }
-    __syncthreads();
-    const float2 ms = sm.msf;
-    if (slow) {
-        if (warp == 0)
-            merge_extract_warp(part_keys, G, batch_total, b, k, invT, ms, out_ids, out_logits, out_probs,
-                               lane);
-        return;
-    }
-    // 4. rank among the candidates = final position
-    for (int i = tid; i < total; i += kMergeThreads) {
-        const uint64_t x = sm.cand[i];
-        int rank = 0;
-        for (int q = 0; q < total; ++q) rank += sm.cand[q] > x;
-        if (rank < k) {
-            const size_t o = static_cast<size_t>(b) * k + rank;
-            const float v = key_value(x);
-            out_ids[o] = key_id(x);
-            out_logits[o] = v;
-            if (out_probs) out_probs[o] = expf((v - ms.x) * invT) / ms.y;
-        }
-    }
+    merge_column_sorted(lists, R, sms, G, k, invT, part_keys, batch_total, blockIdx.x, out_ids, out_logits,
+                        out_probs, w, threadIdx.x, 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -1205,11 +1294,14 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
         }
     }
     if (raw) return cudaSuccess;
-    if (plan.path != 2 && plan.grid <= kMergeThreads && (k + plan.grid - 1) / plan.grid <= kMergeR)
-        return launch_pdl(merge_sorted_kernel, dim3(batch), dim3(kMergeThreads), 0, stream,
+    if (plan.path != 2 && plan.grid <= kMergeThreads) {
+        const int R = merge_stage_entries(plan.grid, k);
+        return launch_pdl(merge_sorted_kernel, dim3(batch), dim3(kMergeThreads),
+                          static_cast<size_t>(plan.grid) * (R + 1) * 8, stream,
                           static_cast<const uint64_t *>(part_keys), static_cast<const float2 *>(part_ms),
-                          plan.grid, static_cast<int>(batch), static_cast<int>(k), invT, ids, logits_out,
+                          plan.grid, static_cast<int>(batch), static_cast<int>(k), R, invT, ids, logits_out,
                           probs);
+    }
     return launch_merge(part_keys, part_ms, plan.grid, plan.key_stride, k, batch, k, invT, ids,
                         logits_out, probs, dev, stream);
 }

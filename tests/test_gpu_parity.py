@@ -226,7 +226,26 @@ def test_launch_count_follows_the_plan():
     assert n(64, 0, lhs.LHS_BF16) == 1
     T32 = wl.make_table(orc.F32, 1000, 64, 0.02, cid=251, threads=4)
     tab32 = upload_table(T32, orc.F32, 1000, 64)
-    assert lhs.lhs_logits_topk_launches(tab32, 4, 5, lhs.LHS_F32) == 2
+    assert lhs.lhs_logits_topk_launches(tab32, 4, 5, lhs.LHS_F32) == 2   # GEMV + merge
+
+
+def test_repeated_calls_share_a_workspace():
+    # consecutive calls on one workspace, alternating between two tables:
+    # nothing a call leaves in the workspace may leak into the next
+    V, H, k = 6000, 128, 10
+    tabs, Xs = [], []
+    for i, (dt, v) in enumerate(((orc.BF16, V), (orc.F16, V // 2 + 37))):
+        T = wl.make_table(dt, v, H, 0.02, cid=270 + i, threads=4)
+        tabs.append(upload_table(T, dt, v, H))
+    X = to_dev(wl.residuals(272, 3, H))
+    ws = torch.empty(max(lhs.lhs_logits_topk_workspace(t, 3, k, lhs.LHS_F32) for t in tabs),
+                     dtype=torch.uint8, device="cuda")
+    ref = [lhs.lhs_logits_topk(t, X, k)[0].cpu().numpy() for t in tabs]
+    for rep in range(5):
+        for t, r in zip(tabs, ref):
+            ids, _, _, err = lhs.lhs_logits_topk(t, X, k, ws=ws)
+            assert int(err.item()) == 0
+            assert np.array_equal(ids.cpu().numpy(), r), rep
 
 
 GEMM_CASES = [
@@ -341,6 +360,22 @@ def test_topk_clustered_in_one_cta_range():
     X = wl.residuals(261, 2, H)
     X[:, 0] = 4.0
     _topk_matches_own_logits(tab, to_dev(X), k, temperature=0.9)
+
+
+def test_topk_many_keys_above_the_merge_bound():
+    # 32-row CTA ranges, each with 4 high logits and k = 5: every CTA's k-th
+    # key is a low one, so the bound admits all 4 x 152 high keys
+    G = 152
+    V, H, k = 32 * G, 64, 5
+    T = wl.make_table(orc.BF16, V, H, 0.02, cid=264, threads=4)
+    rows = np.arange(V)
+    hi = rows % 32 < 4
+    col0 = np.where(hi, 2.0 + rows / V, 0.01).astype(np.float32)
+    T[:, 0] = wl.f32_to_bf16_bits(col0)
+    tab = upload_table(T, orc.BF16, V, H)
+    X = wl.residuals(265, 2, H)
+    X[:, 0] = 8.0
+    _topk_matches_own_logits(tab, to_dev(X), k, temperature=1.1)
 
 
 def test_topk_when_some_cta_lists_are_short():
