@@ -167,6 +167,7 @@ struct LmHeadPlan {
     size_t off_sample_keys, off_sample_ms, off_sample_ids, off_sample_logits;  // GEMM sample pass
     int key_stride;    // entries between consecutive partial lists
     bool sample;       // GEMM: run the sample pass
+    bool xres;         // tensor-core GEMV: residual operand resident in shared memory (no prep kernel)
     size_t bytes;      // total workspace
 };
 int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dtype,

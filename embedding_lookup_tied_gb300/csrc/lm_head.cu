@@ -706,16 +706,25 @@ struct TcParams {
     float *raw;      // raw mode: [batch_total x V]
     uint64_t *part_keys;
     float2 *part_ms;
+    const void *resid;  // XRES: this pass's residuals [Bc x K]
+    int resid_f32;      // XRES: residual dtype f32 (else bf16)
     int32_t *err;
 };
 
+// Shared memory of the tensor-core GEMV: the table-tile ring, barriers and
+// top-k state, then (at the next 1 KB boundary) the residual operand: a ring
+// of TMA tiles [kStages][16 x 64], or — when it fits — the whole operand
+// [Kpad / 64][16 x 64] resident, written by the consumers themselves.  Both
+// use the TMA 128-byte swizzle: within a 16 x 128-byte tile, row r's 16-byte
+// chunk c sits at r * 128 + ((c ^ (r & 7)) << 4).
 struct TcSmem {
     uint8_t a[kStages][kAStageBytes];
-    uint8_t x[kStages][kXStageBytes];
     uint64_t full[kStages];
     uint64_t empty[kStages];
     TopkShared tk;
 };
+constexpr size_t kTcXOffset = (sizeof(TcSmem) + 1023) & ~size_t(1023);
+constexpr size_t kTcXRingBytes = static_cast<size_t>(kStages) * kXStageBytes;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
@@ -741,13 +750,17 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <bool BF16T, bool RAW>
+// XRES: the residual operand is resident in shared memory, built by the
+// consumers from the residuals (what prep_kernel does otherwise), so the pass
+// is one launch and the producer never waits for an earlier kernel.
+template <bool BF16T, bool RAW, bool XRES>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a16,
                    const __grid_constant__ CUtensorMap tm_x, const TcParams p) {
     extern __shared__ uint8_t dyn_smem[];
     TcSmem &sm = *reinterpret_cast<TcSmem *>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *xsm = reinterpret_cast<uint8_t *>(&sm) + kTcXOffset;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     int q = 1;
@@ -797,7 +810,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int rows = block_rows(j / p.nk);
                 const int n16 = (rows + kBoxRowsSmall - 1) / kBoxRowsSmall;
                 return static_cast<uint32_t>(rows == BM ? kAStageBytes : n16 * kBoxRowsSmall * BK * 2) +
-                       kXStageBytes;
+                       (XRES ? 0u : static_cast<uint32_t>(kXStageBytes));
             };
             // The table is never written by an earlier kernel, so the first
             // ring's worth of table tiles is requested before waiting for the
@@ -807,9 +820,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_arrive_expect_tx(&sm.full[j], stage_bytes(j));
                 issue_a(j);
             }
-            pdl_wait();
-            for (uint32_t j = 0; j < pre; ++j)
-                tma_load_2d(sm.x[j], &tm_x, &sm.full[j], (j % p.nk) * BK, 0);
+            if (!XRES) {
+                pdl_wait();
+                for (uint32_t j = 0; j < pre; ++j)
+                    tma_load_2d(xsm + j * kXStageBytes, &tm_x, &sm.full[j], (j % p.nk) * BK, 0);
+            }
             uint32_t it = pre;
             for (; it < total; ++it) {
                 const int s = it % kStages;
@@ -823,7 +838,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (ld_volatile(&sm.tk.abort_flag)) break;
                 mbar_arrive_expect_tx(&sm.full[s], stage_bytes(it));
                 issue_a(it);
-                tma_load_2d(sm.x[s], &tm_x, &sm.full[s], (it % p.nk) * BK, 0);
+                if (!XRES) tma_load_2d(xsm + s * kXStageBytes, &tm_x, &sm.full[s], (it % p.nk) * BK, 0);
             }
             // drain: every issued stage must land before the CTA exits
             const uint32_t issued = it;
@@ -845,6 +860,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int x_row = (lane & 7) + ((lane >> 4) << 3);
     const int x_csel = (lane >> 3) & 1;
     float m_st[2] = {-INFINITY, -INFINITY}, s_st[2] = {0.0f, 0.0f};
+    if (XRES) {
+        // the residuals may come from the previous kernel, and the partial
+        // lists written below may still be read by it
+        pdl_wait();
+        const int Kp = p.nk * BK;
+        int bad = 0;
+        for (int b = 0; b < 8; ++b) {
+            for (int kk = tid; kk < Kp; kk += kConsumers) {
+                float v = 0.0f;
+                if (b < p.Bc && kk < p.K) {
+                    const int64_t src = static_cast<int64_t>(b) * p.K + kk;
+                    if (p.resid_f32) v = __ldg(static_cast<const float *>(p.resid) + src);
+                    else v = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(p.resid) + src)) << 16);
+                }
+                uint16_t hi, lo;
+                if (BF16T) {
+                    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+                    hi = __bfloat16_as_ushort(h);
+                    lo = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
+                } else {
+                    if (!(fabsf(v) < 65504.0f)) bad = 1;
+                    const __half h = __float2half_rn(v);
+                    hi = __half_as_ushort(h);
+                    lo = __half_as_ushort(__float2half_rn(v - __half2float(h)));
+                }
+                // rows b (hi) and 8 + b (lo) of tile kk / 64; both rows have r & 7 == b
+                const int e = kk & (BK - 1);
+                uint8_t *cell = xsm + (kk / BK) * kXStageBytes + ((((e >> 3) ^ b) << 4) | ((e & 7) * 2));
+                *reinterpret_cast<uint16_t *>(cell + b * 128) = hi;
+                *reinterpret_cast<uint16_t *>(cell + (8 + b) * 128) = lo;
+            }
+        }
+        if (bad && p.Bc > 0) set_err(p.err, LHS_ERRBIT_NONFINITE);
+        named_bar_sync(kBarAll, kConsumers);
+    }
     uint32_t it = 0;
     for (int blk = 0; blk < nblk; ++blk) {
         const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
@@ -862,7 +912,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 } else if (active) {
                     const uint32_t abase = smem_u32(sm.a[s]);
-                    const uint32_t xbase = smem_u32(sm.x[s]);
+                    const uint32_t xbase = smem_u32(xsm + (XRES ? kc : s) * kXStageBytes);
 #pragma unroll
                     for (int ks = 0; ks < BK / 16; ++ks) {
                         const int ca = 2 * ks + a_csel;
@@ -1094,7 +1144,10 @@ bool make_tma_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint6
 
 namespace {
 
-constexpr size_t kTcSmemBytes = sizeof(TcSmem) + 1024;
+// dynamic shared memory of the tensor-core GEMV: alignment slack + layout
+size_t tc_smem_bytes(bool xres, int kpad) {
+    return 1024 + kTcXOffset + (xres ? static_cast<size_t>(kpad) * 32 : kTcXRingBytes);
+}
 constexpr size_t kSimtXBytesMax = 96 * 1024;
 
 size_t simt_smem_bytes(int Bc, int K) {
@@ -1140,7 +1193,8 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
         // nothing else to size: the GEMM reads the residuals in place
     } else if (tc) {
         p.batch_chunk = kBatchChunk;
-        if (kTcSmemBytes > static_cast<size_t>(dev.max_smem_optin)) return LHS_ERR_UNSUPPORTED;
+        p.xres = tc_smem_bytes(true, p.kpad) <= static_cast<size_t>(dev.max_smem_optin);
+        if (tc_smem_bytes(p.xres, p.kpad) > static_cast<size_t>(dev.max_smem_optin)) return LHS_ERR_UNSUPPORTED;
     } else {
         int bc = static_cast<int>(kSimtXBytesMax / (static_cast<size_t>(t.hidden) * 4));
         if (bc > kBatchChunk) bc = kBatchChunk;
@@ -1182,7 +1236,7 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
 int lm_head_launches(const LmHeadPlan &plan, int32_t batch, bool raw) {
     if (plan.path == 2) return raw ? 1 : (plan.sample ? 4 : 2);
     const int chunks = (batch + plan.batch_chunk - 1) / plan.batch_chunk;
-    const int per_chunk = plan.path == 0 ? 2 : 1;  // (prep +) projection
+    const int per_chunk = (plan.path == 0 && !plan.xres) ? 2 : 1;  // (prep +) projection
     return chunks * per_chunk + (raw ? 0 : 1);
 }
 
@@ -1219,17 +1273,22 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             !make_tma_map_16bit(&tm_a16, t.data, t.hidden, t.vocab, t.row_bytes, BK, kBoxRowsSmall, bf16) ||
             !make_tma_map_16bit(&tm_x, xs, plan.kpad, 16, static_cast<uint64_t>(plan.kpad) * 2, BK, 16, bf16))
             return cudaErrorInvalidValue;
-        auto kern = bf16 ? (raw ? gemv_tc_kernel<true, true> : gemv_tc_kernel<true, false>)
-                         : (raw ? gemv_tc_kernel<false, true> : gemv_tc_kernel<false, false>);
+        using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams);
+        static const TcKernel kTable[2][2][2] = {
+            {{gemv_tc_kernel<false, false, false>, gemv_tc_kernel<false, false, true>},
+             {gemv_tc_kernel<false, true, false>, gemv_tc_kernel<false, true, true>}},
+            {{gemv_tc_kernel<true, false, false>, gemv_tc_kernel<true, false, true>},
+             {gemv_tc_kernel<true, true, false>, gemv_tc_kernel<true, true, true>}}};
+        const TcKernel kern = kTable[bf16][raw][plan.xres];
+        const size_t smem = tc_smem_bytes(plan.xres, plan.kpad);
         {
-            // one attribute flag per instantiation
+            // one attribute flag per instantiation: the largest size this device allows
             static std::mutex mu;
-            static bool done[4][64] = {};
-            const int which = (bf16 ? 2 : 0) + (raw ? 1 : 0);
+            static bool done[8][64] = {};
+            const int which = (bf16 ? 4 : 0) + (raw ? 2 : 0) + (plan.xres ? 1 : 0);
             std::lock_guard<std::mutex> lock(mu);
             if (!done[which][dev.device]) {
-                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kTcSmemBytes));
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
                 if (e != cudaSuccess) return e;
                 done[which][dev.device] = true;
             }
@@ -1237,12 +1296,14 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
         for (int c0 = 0; c0 < batch; c0 += plan.batch_chunk) {
             const int Bc = batch - c0 < plan.batch_chunk ? batch - c0 : plan.batch_chunk;
             const void *rc = static_cast<const uint8_t *>(resid) + static_cast<size_t>(c0) * t.hidden * relt;
-            const int pgrid = static_cast<int>((static_cast<int64_t>(8) * plan.kpad + 255) / 256);
-            auto prep = bf16 ? (resid_dtype == LHS_F32 ? prep_kernel<true, LHS_F32> : prep_kernel<true, LHS_BF16>)
-                             : (resid_dtype == LHS_F32 ? prep_kernel<false, LHS_F32> : prep_kernel<false, LHS_BF16>);
-            e = launch_pdl(prep, dim3(pgrid), dim3(256), 0, stream, rc, Bc, static_cast<int>(t.hidden),
-                           plan.kpad, xs, err);
-            if (e != cudaSuccess) return e;
+            if (!plan.xres) {
+                const int pgrid = static_cast<int>((static_cast<int64_t>(8) * plan.kpad + 255) / 256);
+                auto prep = bf16 ? (resid_dtype == LHS_F32 ? prep_kernel<true, LHS_F32> : prep_kernel<true, LHS_BF16>)
+                                 : (resid_dtype == LHS_F32 ? prep_kernel<false, LHS_F32> : prep_kernel<false, LHS_BF16>);
+                e = launch_pdl(prep, dim3(pgrid), dim3(256), 0, stream, rc, Bc, static_cast<int>(t.hidden),
+                               plan.kpad, xs, err);
+                if (e != cudaSuccess) return e;
+            }
             TcParams p;
             p.V = t.vocab;
             p.K = t.hidden;
@@ -1255,9 +1316,10 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             p.raw = raw_logits;
             p.part_keys = part_keys;
             p.part_ms = part_ms;
+            p.resid = rc;
+            p.resid_f32 = resid_dtype == LHS_F32;
             p.err = err;
-            e = launch_pdl(kern, dim3(plan.grid), dim3(kTcThreads), kTcSmemBytes, stream, tm_a, tm_a16,
-                           tm_x, p);
+            e = launch_pdl(kern, dim3(plan.grid), dim3(kTcThreads), smem, stream, tm_a, tm_a16, tm_x, p);
             if (e != cudaSuccess) return e;
         }
     } else {
