@@ -240,9 +240,14 @@ def setup(name, batch, device, vocab=None):
                              c.dec.data_ptr(), c.err.data_ptr(), c.sptr)),
     ]
     c.lm_call = c.calls[1]
+    c.flush_l2 = w.table_bytes < 2 * L2_BYTES
+    if c.flush_l2:
+        c.flush_buf = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=device)
     # kernels per step: embed 1, the lm_head call as the library reports it
     # for this plan, wire encode 1, decode 1
     lm = lhs.lhs_logits_topk_launches(c.table, c.B, c.k, rd)
+    c.lm_launches = lm
+    c.gemm = (w.dtype == wl.BF16 and w.resid_dtype == wl.BF16 and c.B > 8)
     c.launches_per_step = 1 + lm + 1 + 1
     return c
 
@@ -252,6 +257,53 @@ def run_step(c):
         rc = fn(*args)
         if rc != 0:
             raise RuntimeError(f"{fn.__name__} -> {rc}")
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one lm_head
+# call, from the ncu captures summarised under profiles/, with a digest of
+# the kernel sources they were taken on: once the sources change, the
+# recorded traffic no longer describes the kernel and is reported as null.
+TRAFFIC_RECORDS = {
+    # workload: (source digest, bytes per call, summary)
+    "qwen05b": ("732e4ed56b14bf2b", 276.10e6, "profiles/gemv_tc_qwen05b.md"),
+    "batched": ("732e4ed56b14bf2b", 2.948e9, "profiles/gemm_tc_batched.md"),
+}
+KERNEL_SOURCES = ("embedding_lookup_tied_gb300/csrc/lm_head.cu",
+                  "embedding_lookup_tied_gb300/csrc/gemm_tc.cu",
+                  "embedding_lookup_tied_gb300/csrc/lhs_internal.cuh")
+L2_BYTES = 129 * 1024 * 1024
+
+
+def kernel_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name):
+    rec = TRAFFIC_RECORDS.get(name)
+    if rec is None:
+        return None, "no ncu capture recorded for this workload"
+    digest, nbytes, src = rec
+    if kernel_digest() != digest:
+        return None, f"kernel sources changed since the capture in {src}"
+    return nbytes, src
+
+
+def workload_config(w, B, k, fmt, n_ids, world):
+    """The `config` object of the JSON line (both arms)."""
+    flush = w.table_bytes < 2 * L2_BYTES
+    return {"workload": w.name, "vocab": w.vocab, "hidden": w.hidden,
+            "table_dtype": wl.DTYPE_NAMES[w.dtype], "table_bytes": w.table_bytes,
+            "embed_ids": n_ids, "lm_batch": B, "k": k,
+            "wire": {0: "f32", 1: "f16", 2: "i8"}[fmt],
+            "l2": ("flushed before every timed iteration (a 258 MB buffer rewritten outside the "
+                   "timed events): the table fits in L2" if flush else
+                   "no flush: the table is larger than twice the L2 and is streamed every step"),
+            "parallelism": f"replicas x{world}"}
 
 
 def lm_bytes(c):
@@ -275,6 +327,30 @@ def step_bytes(c):
 # timing
 # ---------------------------------------------------------------------------
 
+def timed_loop(c, body, n):
+    """Device time of `body` per iteration.  When the table fits in L2 a
+    buffer larger than L2 is overwritten before every iteration, outside the
+    timed events, so every iteration starts with the table in HBM."""
+    import torch
+    if not c.flush_l2:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(c.stream)
+        for _ in range(n):
+            body()
+        e1.record(c.stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in ev:
+        c.flush_buf.add_(1)
+        a.record(c.stream)
+        body()
+        b.record(c.stream)
+    ev[-1][1].synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / n
+
+
 def time_device(c, steps, warmup, world):
     import torch
     for _ in range(warmup):
@@ -287,32 +363,18 @@ def time_device(c, steps, warmup, world):
     fn, args = c.lm_call
     for _ in range(5):
         fn(*args)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    e0.record(c.stream)
-    for _ in range(lm_steps):
-        fn(*args)
-    e1.record(c.stream)
-    e1.synchronize()
-    lm_ms = e0.elapsed_time(e1) / lm_steps
+    lm_ms = timed_loop(c, lambda: fn(*args), lm_steps)
     # whole step
     barrier(world)
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
-    s0 = torch.cuda.Event(enable_timing=True)
-    s1 = torch.cuda.Event(enable_timing=True)
-    s0.record(c.stream)
-    for _ in range(steps):
-        run_step(c)
-    s1.record(c.stream)
-    s1.synchronize()
+    ms = timed_loop(c, lambda: run_step(c), steps)
     torch.cuda.synchronize()
     barrier(world)
     ck = clocks.stop()
-    ms = s0.elapsed_time(s1) / steps
     if int(c.err.item()) != 0:
         raise RuntimeError(f"error word {int(c.err.item())} in the timed region")
     return ms, lm_ms, ck
@@ -431,8 +493,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * B / value, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "vocab": w.vocab, "hidden": w.hidden,
-                       "table_dtype": wl.DTYPE_NAMES[w.dtype], "lm_batch": B, "k": k},
+            "config": workload_config(w, B, k, fmt, w.n_ids or 1, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -465,6 +526,7 @@ def main():
     value = world * c.B / (ms / 1e3)
     lmb = lm_bytes(c)
     achieved = lmb / (lm_ms / 1e3) / 1e9
+    traffic, traffic_src = recorded_traffic(c.w.name) if not args.vocab else (None, "vocab override")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
@@ -472,24 +534,30 @@ def main():
         "dtype": {wl.F32: "f32", wl.F16: "f16", wl.BF16: "bf16", wl.Q8_0: "q8_0"}[c.w.dtype]
                  + "-table/f32-accumulate",
         "data": "synthetic",
-        "config": {"workload": c.w.name, "vocab": c.w.vocab, "hidden": c.w.hidden,
-                   "table_dtype": wl.DTYPE_NAMES[c.w.dtype], "table_bytes": c.w.table_bytes,
-                   "embed_ids": c.n_ids, "lm_batch": c.B, "k": c.k,
-                   "wire": {0: "f32", 1: "f16", 2: "i8"}[c.fmt],
-                   "l2": "no flush: the table is larger than L2 and is streamed every step",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(c.w, c.B, c.k, c.fmt, c.n_ids, world),
         "hbm_gbs_step": world * step_bytes(c) / (ms / 1e3) / 1e9,
         "embed_rows_per_s": world * c.n_ids / (ms / 1e3),
-        "roofline": {"kernel": "lhs_logits_topk (prep + GEMV/top-k + merge)",
+        "roofline": {"kernel": f"lhs_logits_topk call ({c.lm_launches} kernels)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": None, "algorithmic_bytes": lmb, "avg_ms": lm_ms},
+                     "traffic": traffic, "traffic_source": traffic_src,
+                     "algorithmic_bytes": lmb, "avg_ms": lm_ms},
         "gpu_launches": c.launches_per_step * steps,
         "clocks": clocks,
         "e2e": {"value": world * c.B / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": e2e_ms},
     }
+    if c.gemm:
+        # a dense contraction near the ridge point: its tensor-core fraction too
+        _, _, pk = load_peaks()
+        flops = 2.0 * c.B * c.w.vocab * c.w.hidden
+        tf = flops / (lm_ms / 1e3) / 1e12
+        tpk = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", 1700.0)))
+        line["roofline_tensor"] = {"bound": "tensor", "achieved": tf, "peak": tpk, "unit": "TFLOP/s",
+                                   "frac": tf / tpk,
+                                   "peak_source": "measured bf16_tflops_sustained" if pk else "fallback",
+                                   "flops": flops}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         r, sample = oracle_rate(c.w, c.T_host, c.ids_host, c.R_host, c.B, c.k, c.fmt,
