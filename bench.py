@@ -51,6 +51,9 @@ def parse_args():
                     help="override the workload's vocab rows (small cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="steady-state sweep of the sub-10-us steps (gather, wire codecs): one "
+                         "JSON line per point instead of the step line")
     return ap.parse_args()
 
 
@@ -504,11 +507,111 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------------------
 
+SWEEP_HIDDEN = (2560, 4096, 5120, 5376)   # ADR-0009 benchmark sizes
+SWEEP_SEQ = (1, 32, 256, 65536)
+
+
+def run_sweep(dev, peak):
+    """Steady-state numbers for the steps that take a few microseconds at
+    the configs' sizes: the gather over 2^20 Zipf ids of the gemma_q8 and
+    qwen05b tables, and f16 / i8 encode and decode over the ADR-0009 sizes.
+    Points moving >= 1 GB per call report a bandwidth fraction; the others
+    are latency (their bytes sit in L2 between iterations)."""
+    import torch
+
+    import embedding_lookup_tied_gb300 as lhs
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    def t_us(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    def emit(kind, cfg, us, nbytes):
+        d = {"sweep": kind, "config": cfg, "us_per_call": us, "algorithmic_bytes": nbytes,
+             "gbs": nbytes / (us * 1e-6) / 1e9}
+        if nbytes >= 1e9:
+            d["frac_of_measured_hbm"] = d["gbs"] / peak
+        else:
+            d["latency_only"] = True
+        print(json.dumps(d), flush=True)
+
+    L = lhs.lib()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    import ctypes
+    n_ids = 1 << 20
+    for name in ("gemma_q8", "qwen05b"):
+        w = wl.WORKLOADS[name]
+        T = wl.table_for(w)
+        tab = lhs.lhs_table_init(up(T), w.vocab, w.hidden, w.dtype)
+        ids_h = wl.zipf_ids(w.cid, n_ids, w.vocab, w.zipf_s, w.session_vocab)
+        ids = up(ids_h)
+        out = torch.empty((n_ids, w.hidden), dtype=torch.float32, device=dev)
+        distinct = len(np.unique(ids_h))
+        args = (ctypes.byref(tab.c), ids.data_ptr(), n_ids, ctypes.c_float(float(w.embed_scale)),
+                out.data_ptr(), err.data_ptr(), sp)
+        us = t_us(lambda: L.lhs_embed(*args), 10)
+        nbytes = n_ids * (4 + w.hidden * 4) + distinct * w.row_bytes
+        emit("gather", {"table": name, "ids": n_ids, "distinct": distinct, "hidden": w.hidden}, us, nbytes)
+        del out
+        # the gather written straight into f16 / i8 wire messages
+        for fmt, fname in ((lhs.LHS_WIRE_F16, "f16"), (lhs.LHS_WIRE_I8, "i8")):
+            nb = lhs.lhs_wire_bytes(fmt, n_ids, w.hidden)
+            buf = torch.empty(nb, dtype=torch.uint8, device=dev)
+            wa = (ctypes.byref(tab.c), ids.data_ptr(), n_ids, ctypes.c_float(float(w.embed_scale)), fmt,
+                  0, 0, 0, buf.data_ptr(), nb, err.data_ptr(), sp)
+            us = t_us(lambda: L.lhs_embed_wire(*wa), 10)
+            emit("embed_wire", {"table": name, "format": fname, "ids": n_ids, "distinct": distinct,
+                                "hidden": w.hidden}, us, n_ids * 4 + distinct * w.row_bytes + nb)
+            del buf
+        del T, tab
+        torch.cuda.empty_cache()
+    for H in SWEEP_HIDDEN:
+        for S in SWEEP_SEQ:
+            x = torch.randn((S, H), dtype=torch.float32, device=dev)
+            dec = torch.empty_like(x)
+            for fmt, fname in ((lhs.LHS_WIRE_F16, "f16"), (lhs.LHS_WIRE_I8, "i8")):
+                nb = lhs.lhs_wire_bytes(fmt, S, H)
+                buf = torch.empty(nb, dtype=torch.uint8, device=dev)
+                ea = (fmt, x.data_ptr(), lhs.LHS_F32, S, H, 0, 0, 0, buf.data_ptr(), nb, err.data_ptr(), sp)
+                da = (fmt, buf.data_ptr(), nb, S, H, dec.data_ptr(), err.data_ptr(), sp)
+                n = 10 if S == 65536 else 200
+                us = t_us(lambda: L.lhs_wire_encode(*ea), n)
+                emit("wire_encode", {"format": fname, "seq_len": S, "hidden": H}, us, S * H * 4 + nb)
+                us = t_us(lambda: L.lhs_wire_decode(*da), n)
+                emit("wire_decode", {"format": fname, "seq_len": S, "hidden": H}, us, nb + S * H * 4)
+                del buf
+            del x, dec
+            torch.cuda.empty_cache()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"error word {int(err.item())} in the sweep")
+    return 0
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.sweep:
+        import torch
+        torch.cuda.set_device(local)
+        return run_sweep(torch.device("cuda", local), load_peaks()[0])
     import torch
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")

@@ -31,7 +31,7 @@ LIB_PATH = _build.LIB
 
 # Exported symbols of the C-ABI, in declaration order.
 ABI_SYMBOLS = (
-    "lhs_table_init", "lhs_table_info", "lhs_embed", "lhs_logits_topk_workspace",
+    "lhs_table_init", "lhs_table_info", "lhs_embed", "lhs_embed_wire", "lhs_logits_topk_workspace",
     "lhs_logits_topk_launches", "lhs_logits_topk", "lhs_logits", "lhs_logits_topk_noalloc", "lhs_wire_bytes",
     "lhs_wire_encode",
     "lhs_wire_decode", "lhs_selftest_bounded_wait", "lhs_strerror",
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         "lhs_table_init": (ctypes.c_int, [T, P, i64, i32, i32]),
         "lhs_table_info": (ctypes.c_int, [T, P, P, P, P]),
         "lhs_embed": (ctypes.c_int, [T, P, i64, ctypes.c_float, P, P, P]),
+        "lhs_embed_wire": (ctypes.c_int, [T, P, i64, ctypes.c_float, i32, u32, u32, u32, P,
+                                          ctypes.c_size_t, P, P]),
         "lhs_logits_topk_workspace": (ctypes.c_int, [T, i32, i32, i32, P]),
         "lhs_logits_topk_launches": (ctypes.c_int, [T, i32, i32, i32, P]),
         "lhs_logits_topk": (ctypes.c_int, [T, P, i32, i32, i32, ctypes.c_float, P, P, P,
@@ -179,6 +181,24 @@ def lhs_embed(table: Table, ids: torch.Tensor, scale: float, out=None, err=None,
                            float(scale), _dev(out, "out") if n else None,
                            _dev(err, "err"), _stream(stream)), "lhs_embed")
     return out, err
+
+
+def lhs_embed_wire(table: Table, ids: torch.Tensor, scale: float, fmt: int, layer: int = 0,
+                   flags: int = 0, top_k: int = 0, buf=None, err=None, stream=None):
+    """Gather rows ``ids`` scaled by ``scale`` straight into a wire message of
+    format ``fmt`` (uint8 tensor).  Returns (buf, err word)."""
+    n = ids.numel()
+    if ids.dtype != torch.int32:
+        raise ValueError("ids must be int32")
+    nb = lhs_wire_bytes(fmt, n, table.hidden)
+    if nb < 0:
+        raise ValueError("bad wire format or shape")
+    buf = torch.empty(nb, dtype=torch.uint8, device=table.device) if buf is None else buf
+    err = _err_word(err, table.device)
+    _check(lib().lhs_embed_wire(ctypes.byref(table.c), _dev(ids, "ids") if n else None, n,
+                                float(scale), fmt, layer, flags, top_k, _dev(buf, "buf"),
+                                buf.numel(), _dev(err, "err"), _stream(stream)), "lhs_embed_wire")
+    return buf, err
 
 
 def _resid_dtype(resid: torch.Tensor) -> int:

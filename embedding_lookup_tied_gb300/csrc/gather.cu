@@ -21,27 +21,11 @@ namespace {
 
 constexpr int kWarps = 8;
 
-__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
-}
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
 __device__ __forceinline__ float4 scale4(float a, float b, float c, float d, float s) {
     return make_float4(__fmul_rn(a, s), __fmul_rn(b, s), __fmul_rn(c, s), __fmul_rn(d, s));
 }
 
-// Scalar element decode (any hidden, any alignment of rows).
-template <int DT>
-__device__ __forceinline__ float element(const uint8_t *row, int j) {
-    if (DT == LHS_F32) return __ldg(reinterpret_cast<const float *>(row) + j);
-    if (DT == LHS_F16) return f16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short *>(row) + j));
-    if (DT == LHS_BF16) return bf16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short *>(row) + j));
-    // Q8_0: block j/32 = [f16 d][32 x int8]
-    const uint8_t *blk = row + (j >> 5) * 34;
-    const float d = f16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short *>(blk)));
-    const float q = static_cast<float>(static_cast<int8_t>(__ldg(blk + 2 + (j & 31))));
-    return __fmul_rn(d, q);
-}
 
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -68,7 +52,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         }
         const uint8_t *row = table + static_cast<int64_t>(id) * row_bytes;
         if (!VEC) {
-            for (int j = lane; j < hidden; j += 32) o[j] = __fmul_rn(element<DT>(row, j), scale);
+            for (int j = lane; j < hidden; j += 32) o[j] = __fmul_rn(row_element<DT>(row, j), scale);
             continue;
         }
         float4 *o4 = reinterpret_cast<float4 *>(o);

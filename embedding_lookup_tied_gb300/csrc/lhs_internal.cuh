@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -106,6 +107,191 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Element decode and wire encoding helpers shared by the gather, the wire
+// codecs and the fused embed -> wire kernel.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// Stored element j of a table row, widened exactly to binary32 (Q8_0: d*q,
+// exact: an 11-bit by 8-bit significand product fits in 24 bits).
+template <int DT>
+__device__ __forceinline__ float row_element(const uint8_t *row, int j) {
+    if (DT == LHS_F32) return __ldg(reinterpret_cast<const float *>(row) + j);
+    if (DT == LHS_F16) return f16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short *>(row) + j));
+    if (DT == LHS_BF16) return bf16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short *>(row) + j));
+    const uint8_t *blk = row + (j >> 5) * 34;  // Q8_0 block: [f16 d][32 x int8]
+    const float d = f16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short *>(blk)));
+    const float q = static_cast<float>(static_cast<int8_t>(__ldg(blk + 2 + (j & 31))));
+    return __fmul_rn(d, q);
+}
+
+// Elements 8g .. 8g+7 of a row (hidden % 8 == 0; f32/f16/bf16 rows 16-byte
+// aligned; Q8_0 rows 2-byte aligned).
+template <int DT>
+__device__ __forceinline__ void row_elements8(const uint8_t *row, int g, float (&v)[8]) {
+    if (DT == LHS_F32) {
+        const float4 *p = reinterpret_cast<const float4 *>(row) + 2 * g;
+        const float4 a = __ldg(p), b = __ldg(p + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else if (DT == LHS_F16 || DT == LHS_BF16) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(row) + g);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = DT == LHS_F16 ? f16_bits_to_f32(u[i] & 0xFFFFu) : bf16_bits_to_f32(u[i] & 0xFFFFu);
+            v[2 * i + 1] = DT == LHS_F16 ? f16_bits_to_f32(u[i] >> 16) : bf16_bits_to_f32(u[i] >> 16);
+        }
+    } else {
+        const uint8_t *blk = row + (g >> 2) * 34;
+        const unsigned short *b16 = reinterpret_cast<const unsigned short *>(blk);
+        const float d = f16_bits_to_f32(__ldg(b16));
+        const int q0 = 1 + (g & 3) * 4;  // codes (g & 3) * 8 .. +7, two per 16-bit word
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w = __ldg(b16 + q0 + i);
+            v[2 * i] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(w & 0xFF)));
+            v[2 * i + 1] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(w >> 8)));
+        }
+    }
+}
+
+// binary16 bits of x, round to nearest even; a finite x whose rounding
+// overflows saturates to +-65504, inf stays inf, NaN becomes 0x7E00.
+__device__ __forceinline__ uint32_t f16_sat_bits(float x) {
+    if (x != x) return 0x7E00u;
+    uint32_t b = __half_as_ushort(__float2half_rn(x));
+    if ((b & 0x7FFFu) == 0x7C00u && isfinite(x)) b = (b & 0x8000u) | 0x7BFFu;
+    return b;
+}
+
+// Eight binary16 values packed in a 16-byte word with f16_sat_bits' rules.
+// When every value is finite and below 65504 in magnitude (no saturation,
+// no inf/NaN), the conversion is two-at-a-time round-to-nearest-even.
+__device__ __forceinline__ uint4 pack_f16x8(const float (&v)[8]) {
+    bool plain = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) plain = plain && (fabsf(v[i]) < 65504.0f);  // false for NaN
+    uint32_t w[4];
+    if (plain) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = f16_sat_bits(v[2 * i]) | (f16_sat_bits(v[2 * i + 1]) << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// i8 code of v: round half to even of the correctly rounded binary32
+// quotient v / scale, clamped to [-127, 127]; 0 when scale is 0.
+// rcp = __frcp_rn(scale).  The product t = RN(v * rcp) is within
+// |v/scale| * 2^-23 of the exact quotient Q, and RN(Q) within |Q| * 2^-24
+// of it; for |t| < 256 the two therefore differ by less than 2^-14.4, so
+// unless t lies within 2^-12 of a half-integer (a rounding boundary of rint)
+// both round to the same integer.  Near a boundary — or when t is out of
+// that range, e.g. a reciprocal that overflowed — the quotient is formed by
+// the correctly rounded divide instead.
+__device__ __forceinline__ int8_t i8_code(float v, float scale, float rcp) {
+    if (scale == 0.0f) return 0;
+    const float t = __fmul_rn(v, rcp);
+    const float a = fabsf(t);
+    float r;
+    if (a < 256.0f && fabsf((a - floorf(a)) - 0.5f) > 0x1p-12f) r = rintf(t);
+    else r = rintf(__fdiv_rn(v, scale));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int8_t>(static_cast<int>(r));
+}
+
+// Block-wide max of non-negative values and OR of a flag; every thread gets
+// the result.  sm_m / sm_f hold one entry per warp.
+__device__ __forceinline__ void block_max_or(float &m, int &flag, float *sm_m, int *sm_f) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, o);
+    }
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_f[warp] = flag;
+    }
+    __syncthreads();
+    m = sm_m[0];
+    flag = sm_f[0];
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) {
+        m = fmaxf(m, sm_m[w]);
+        flag |= sm_f[w];
+    }
+    __syncthreads();
+}
+
+// One i8 position by one warp, in two passes over its values: max|x| (and
+// whether any value is inf/NaN), then scale = RN(m / 127) and the codes.
+// load8(g, v) yields values 8g .. 8g+7 (ng groups); the second pass reads
+// them again, from L1/L2.  pos: [scale f32][zero point f32 = 0][codes],
+// 8-byte aligned.
+template <typename Load8>
+__device__ __forceinline__ void i8_position_warp(const Load8 &load8, int ng, uint8_t *pos, int lane,
+                                                 int32_t *err) {
+    float m = 0.0f;
+    bool nonfinite = false;
+#pragma unroll 4
+    for (int g = lane; g < ng; g += 32) {
+        float v[8];
+        load8(g, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (!isfinite(v[i])) nonfinite = true;
+            else m = fmaxf(m, fabsf(v[i]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    nonfinite = __any_sync(0xFFFFFFFFu, nonfinite);
+    const float scale = nonfinite ? 0.0f : __fdiv_rn(m, 127.0f);
+    const float rcp = __frcp_rn(scale);
+    if (lane == 0) {
+        *reinterpret_cast<uint2 *>(pos) = make_uint2(__float_as_uint(scale), 0u);
+        if (nonfinite) set_err(err, LHS_ERRBIT_NONFINITE);
+    }
+    uint2 *codes = reinterpret_cast<uint2 *>(pos + 8);
+#pragma unroll 2
+    for (int g = lane; g < ng; g += 32) {
+        float v[8];
+        load8(g, v);
+        uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w0 |= static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i], scale, rcp))) << (8 * i);
+            w1 |= static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i + 4], scale, rcp))) << (8 * i);
+        }
+        codes[g] = make_uint2(w0, w1);
+    }
+}
+
+// Warps per SM for the warp-per-position i8 kernels: as many as keep the
+// positions' values (the second pass re-reads them) within about 192 KB of
+// L1, between 8 and 48.
+inline int i8_warps_per_sm(int64_t bytes_per_position) {
+    int64_t w = (192 * 1024) / (bytes_per_position > 0 ? bytes_per_position : 1);
+    if (w > 48) w = 48;
+    if (w < 8) w = 8;
+    return static_cast<int>(w);
+}
+
+__device__ __forceinline__ void write_wire_header(uint8_t *buf, uint32_t layer, uint32_t seq_len,
+                                                  uint32_t flags, uint32_t top_k) {
+    *reinterpret_cast<uint4 *>(buf) = make_uint4(layer, seq_len, flags, top_k);
+}
+
 // Programmatic dependent launch.  pdl_wait(): block until the preceding
 // kernel in the stream has completed and its memory is visible (a no-op when
 // this kernel was not launched as a dependent).  pdl_trigger(): allow the
@@ -147,6 +333,9 @@ cudaError_t device_info(DeviceInfo *out);
 cudaError_t launch_embed(const lhs_table &t, const int32_t *ids, int64_t n, float scale,
                          float *out, int32_t *err, cudaStream_t stream);
 
+cudaError_t launch_embed_wire(const lhs_table &t, const int32_t *ids, int64_t n, float scale, int fmt,
+                              uint32_t layer, uint32_t flags, uint32_t top_k, void *buf, int32_t *err,
+                              cudaStream_t stream);
 cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_len,
                                int32_t hidden, uint32_t layer, uint32_t flags, uint32_t top_k,
                                void *buf, int32_t *err, cudaStream_t stream);

@@ -8,10 +8,12 @@
 // clamps to the largest finite value instead of producing inf/NaN.
 //
 // f32 / f16: one elementwise pass, 8 values per thread (16-byte accesses).
-// i8: one CTA per position — block max-reduce of |x|, one correctly rounded
-// divide for the scale, then round-half-even of x/scale (correctly rounded
-// divide) for every element.  Positions start at 16 + p*(hidden+8): 8-byte
-// aligned when hidden % 8 == 0, so the codes move as 8-byte words.
+// i8: one warp per position for rows up to 1024 values, one CTA per position
+// for longer or unaligned rows —
+// max-reduce of |x|, one correctly rounded divide for the scale, then
+// round-half-even of the binary32 quotient x/scale for every element.
+// Positions start at 16 + p*(hidden+8): 8-byte aligned when hidden % 8 == 0,
+// so the codes move as 8-byte words.
 #include <cuda_fp16.h>
 
 #include "lhs_internal.cuh"
@@ -21,14 +23,7 @@ namespace {
 
 constexpr int kEwThreads = 256;
 constexpr int kI8Threads = 128;
-constexpr int kI8Cache = 6;  // 8-value groups a thread keeps in registers
-
-__device__ __forceinline__ uint32_t f16_sat_bits(float x) {
-    if (x != x) return 0x7E00u;
-    uint32_t b = __half_as_ushort(__float2half_rn(x));
-    if ((b & 0x7FFFu) == 0x7C00u && isfinite(x)) b = (b & 0x8000u) | 0x7BFFu;
-    return b;
-}
+constexpr int kI8Cache = 6;  // 8-value groups a thread keeps in registers (CTA path)
 
 template <int XDT>
 __device__ __forceinline__ float load_x(const void *x, int64_t i) {
@@ -56,11 +51,6 @@ __device__ __forceinline__ void load_x8(const void *x, int64_t g, float (&v)[8])
     }
 }
 
-__device__ __forceinline__ void write_header(uint8_t *buf, uint32_t layer, uint32_t seq_len,
-                                             uint32_t flags, uint32_t top_k) {
-    *reinterpret_cast<uint4 *>(buf) = make_uint4(layer, seq_len, flags, top_k);
-}
-
 // ---- f32 / f16 encode ------------------------------------------------------
 template <int FMT, int XDT, bool VEC>
 __global__ void __launch_bounds__(kEwThreads)
@@ -70,19 +60,14 @@ __global__ void __launch_bounds__(kEwThreads)
     pdl_wait();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    if (tid == 0) write_header(buf, layer, seq_len, flags, top_k);
+    if (tid == 0) write_wire_header(buf, layer, seq_len, flags, top_k);
     uint8_t *pay = buf + 16;
     const int64_t ng = VEC ? n / 8 : 0;
     for (int64_t g = tid; g < ng; g += nth) {
         float v[8];
         load_x8<XDT>(x, g, v);
         if (FMT == LHS_WIRE_F16) {
-            uint4 w;
-            w.x = f16_sat_bits(v[0]) | (f16_sat_bits(v[1]) << 16);
-            w.y = f16_sat_bits(v[2]) | (f16_sat_bits(v[3]) << 16);
-            w.z = f16_sat_bits(v[4]) | (f16_sat_bits(v[5]) << 16);
-            w.w = f16_sat_bits(v[6]) | (f16_sat_bits(v[7]) << 16);
-            reinterpret_cast<uint4 *>(pay)[g] = w;
+            reinterpret_cast<uint4 *>(pay)[g] = pack_f16x8(v);
         } else {
             float4 *p = reinterpret_cast<float4 *>(pay) + 2 * g;
             p[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -142,37 +127,8 @@ __global__ void __launch_bounds__(kEwThreads)
 }
 
 // ---- i8 encode -------------------------------------------------------------
-__device__ __forceinline__ int8_t i8_code(float v, float scale) {
-    if (scale == 0.0f) return 0;
-    float r = rintf(__fdiv_rn(v, scale));  // round half to even of the binary32 quotient
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return static_cast<int8_t>(static_cast<int>(r));
-}
-
-// Block-wide max of non-negative values and OR of a flag; every thread gets
-// the result.
-__device__ __forceinline__ void block_max_or(float &m, int &flag, float *sm_m, int *sm_f) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, o);
-    }
-    if (lane == 0) {
-        sm_m[warp] = m;
-        sm_f[warp] = flag;
-    }
-    __syncthreads();
-    m = sm_m[0];
-    flag = sm_f[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
-        m = fmaxf(m, sm_m[w]);
-        flag |= sm_f[w];
-    }
-    __syncthreads();
-}
-
-template <int XDT, bool VEC>
+// i8 encode, any alignment or hidden: one CTA per position, element by element.
+template <int XDT>
 __global__ void __launch_bounds__(kI8Threads)
     encode_i8_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
                      uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
@@ -181,91 +137,136 @@ __global__ void __launch_bounds__(kI8Threads)
     __shared__ float sm_m[kI8Threads / 32];
     __shared__ int sm_f[kI8Threads / 32];
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
+        write_wire_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
     for (int64_t p = blockIdx.x; p < seq_len; p += gridDim.x) {
         uint8_t *pos = buf + 16 + p * stride;
         const int64_t xrow = p * static_cast<int64_t>(hidden);
         float m = 0.0f;
         int nonfinite = 0;
-        if (VEC) {
-            const int ng = hidden >> 3;
-            const void *xp = XDT == LHS_F32
-                                 ? static_cast<const void *>(static_cast<const float *>(x) + xrow)
-                                 : static_cast<const void *>(static_cast<const unsigned short *>(x) + xrow);
-            float cache[kI8Cache][8];
+        for (int j = threadIdx.x; j < hidden; j += kI8Threads) {
+            const float v = load_x<XDT>(x, xrow + j);
+            if (!isfinite(v)) nonfinite = 1;
+            else m = fmaxf(m, fabsf(v));
+        }
+        block_max_or(m, nonfinite, sm_m, sm_f);
+        const float scale = nonfinite ? 0.0f : __fdiv_rn(m, 127.0f);
+        const float rcp = __frcp_rn(scale);
+        if (threadIdx.x == 0) {
+            const uint32_t sb = __float_as_uint(scale);
 #pragma unroll
-            for (int c = 0; c < kI8Cache; ++c) {
-                const int g = threadIdx.x + c * kI8Threads;
-                if (g < ng) {
-                    load_x8<XDT>(xp, g, cache[c]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (!isfinite(cache[c][i])) nonfinite = 1;
-                        else m = fmaxf(m, fabsf(cache[c][i]));
-                    }
-                }
+            for (int i = 0; i < 4; ++i) {
+                pos[i] = static_cast<uint8_t>(sb >> (8 * i));
+                pos[4 + i] = 0;
             }
-            for (int g = threadIdx.x + kI8Cache * kI8Threads; g < ng; g += kI8Threads) {
-                float v[8];
-                load_x8<XDT>(xp, g, v);
+            if (nonfinite) set_err(err, LHS_ERRBIT_NONFINITE);
+        }
+        for (int j = threadIdx.x; j < hidden; j += kI8Threads)
+            pos[8 + j] = static_cast<uint8_t>(i8_code(load_x<XDT>(x, xrow + j), scale, rcp));
+    }
+}
+
+// i8 encode of long 16-byte-aligned rows (hidden % 8 == 0, hidden > 1024):
+// one CTA per position, up to kI8Cache 8-value groups per thread held in
+// registers between the block max-reduce and the quantisation.
+template <int XDT>
+__global__ void __launch_bounds__(kI8Threads)
+    encode_i8_cta_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
+                         uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float sm_m[kI8Threads / 32];
+    __shared__ int sm_f[kI8Threads / 32];
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        write_wire_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
+    const int64_t stride = static_cast<int64_t>(hidden) + 8;
+    for (int64_t p = blockIdx.x; p < seq_len; p += gridDim.x) {
+        uint8_t *pos = buf + 16 + p * stride;
+        const int64_t xrow = p * static_cast<int64_t>(hidden);
+        float m = 0.0f;
+        int nonfinite = 0;
+        const int ng = hidden >> 3;
+        const void *xp = XDT == LHS_F32
+                             ? static_cast<const void *>(static_cast<const float *>(x) + xrow)
+                             : static_cast<const void *>(static_cast<const unsigned short *>(x) + xrow);
+        float cache[kI8Cache][8];
+#pragma unroll
+        for (int c = 0; c < kI8Cache; ++c) {
+            const int g = threadIdx.x + c * kI8Threads;
+            if (g < ng) {
+                load_x8<XDT>(xp, g, cache[c]);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    if (!isfinite(v[i])) nonfinite = 1;
-                    else m = fmaxf(m, fabsf(v[i]));
+                    if (!isfinite(cache[c][i])) nonfinite = 1;
+                    else m = fmaxf(m, fabsf(cache[c][i]));
                 }
             }
-            block_max_or(m, nonfinite, sm_m, sm_f);
-            const float scale = nonfinite ? 0.0f : __fdiv_rn(m, 127.0f);
-            if (threadIdx.x == 0) {
-                *reinterpret_cast<uint2 *>(pos) = make_uint2(__float_as_uint(scale), 0u);
-                if (nonfinite) set_err(err, LHS_ERRBIT_NONFINITE);
-            }
-            uint2 *codes = reinterpret_cast<uint2 *>(pos + 8);
+        }
+        for (int g = threadIdx.x + kI8Cache * kI8Threads; g < ng; g += kI8Threads) {
+            float v[8];
+            load_x8<XDT>(xp, g, v);
 #pragma unroll
-            for (int c = 0; c < kI8Cache; ++c) {
-                const int g = threadIdx.x + c * kI8Threads;
-                if (g < ng) {
-                    uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        w0 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(cache[c][i], scale)))) << (8 * i);
-                        w1 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(cache[c][i + 4], scale)))) << (8 * i);
-                    }
-                    codes[g] = make_uint2(w0, w1);
-                }
+            for (int i = 0; i < 8; ++i) {
+                if (!isfinite(v[i])) nonfinite = 1;
+                else m = fmaxf(m, fabsf(v[i]));
             }
-            for (int g = threadIdx.x + kI8Cache * kI8Threads; g < ng; g += kI8Threads) {
-                float v[8];
-                load_x8<XDT>(xp, g, v);
+        }
+        block_max_or(m, nonfinite, sm_m, sm_f);
+        const float scale = nonfinite ? 0.0f : __fdiv_rn(m, 127.0f);
+        const float rcp = __frcp_rn(scale);
+        if (threadIdx.x == 0) {
+            *reinterpret_cast<uint2 *>(pos) = make_uint2(__float_as_uint(scale), 0u);
+            if (nonfinite) set_err(err, LHS_ERRBIT_NONFINITE);
+        }
+        uint2 *codes = reinterpret_cast<uint2 *>(pos + 8);
+#pragma unroll
+        for (int c = 0; c < kI8Cache; ++c) {
+            const int g = threadIdx.x + c * kI8Threads;
+            if (g < ng) {
                 uint32_t w0 = 0, w1 = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    w0 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i], scale)))) << (8 * i);
-                    w1 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i + 4], scale)))) << (8 * i);
+                    w0 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(cache[c][i], scale, rcp)))) << (8 * i);
+                    w1 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(cache[c][i + 4], scale, rcp)))) << (8 * i);
                 }
                 codes[g] = make_uint2(w0, w1);
             }
-        } else {
-            for (int j = threadIdx.x; j < hidden; j += kI8Threads) {
-                const float v = load_x<XDT>(x, xrow + j);
-                if (!isfinite(v)) nonfinite = 1;
-                else m = fmaxf(m, fabsf(v));
-            }
-            block_max_or(m, nonfinite, sm_m, sm_f);
-            const float scale = nonfinite ? 0.0f : __fdiv_rn(m, 127.0f);
-            if (threadIdx.x == 0) {
-                const uint32_t sb = __float_as_uint(scale);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    pos[i] = static_cast<uint8_t>(sb >> (8 * i));
-                    pos[4 + i] = 0;
-                }
-                if (nonfinite) set_err(err, LHS_ERRBIT_NONFINITE);
-            }
-            for (int j = threadIdx.x; j < hidden; j += kI8Threads)
-                pos[8 + j] = static_cast<uint8_t>(i8_code(load_x<XDT>(x, xrow + j), scale));
         }
+        for (int g = threadIdx.x + kI8Cache * kI8Threads; g < ng; g += kI8Threads) {
+            float v[8];
+            load_x8<XDT>(xp, g, v);
+            uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                w0 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i], scale, rcp)))) << (8 * i);
+                w1 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i + 4], scale, rcp)))) << (8 * i);
+            }
+            codes[g] = make_uint2(w0, w1);
+        }
+    }
+}
+
+// i8 encode with 16-byte-aligned rows (hidden % 8 == 0): one warp per
+// position, two passes (i8_position_warp).
+template <int XDT>
+__global__ void __launch_bounds__(128)
+    encode_i8_warp_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
+                          uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    pdl_trigger();
+    pdl_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        write_wire_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
+    const int lane = threadIdx.x & 31;
+    const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t stride = static_cast<int64_t>(hidden) + 8;
+    const int ng = hidden >> 3;
+    for (int64_t p = w0; p < seq_len; p += nw) {
+        const int64_t xrow = p * static_cast<int64_t>(hidden);
+        const void *xp = XDT == LHS_F32 ? static_cast<const void *>(static_cast<const float *>(x) + xrow)
+                                        : static_cast<const void *>(static_cast<const unsigned short *>(x) + xrow);
+        i8_position_warp([&](int g, float (&v)[8]) { load_x8<XDT>(xp, g, v); }, ng, buf + 16 + p * stride,
+                         lane, err);
     }
 }
 
@@ -344,13 +345,27 @@ cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_
     const int64_t n = static_cast<int64_t>(seq_len) * hidden;
     const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(buf)) % 16) == 0;
     const uint32_t s = static_cast<uint32_t>(seq_len);
+    if (fmt == LHS_WIRE_I8 && aligned && hidden % 8 == 0 && hidden > 1024) {
+        const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
+        const int grid = static_cast<int>(seq_len < 1 ? 1 : (seq_len < cap ? seq_len : cap));
+        auto kern = x_dtype == LHS_F32 ? encode_i8_cta_kernel<LHS_F32> : encode_i8_cta_kernel<LHS_BF16>;
+        return launch_pdl(kern, dim3(grid), dim3(kI8Threads), 0, stream, x, seq_len, hidden, layer, flags, top_k,
+                          b, err);
+    }
+    if (fmt == LHS_WIRE_I8 && aligned && hidden % 8 == 0) {
+        const int wps = i8_warps_per_sm(static_cast<int64_t>(hidden) * (x_dtype == LHS_F32 ? 4 : 2));
+        const int64_t warps = seq_len < static_cast<int64_t>(dev.num_sms) * wps ? seq_len
+                                                                                  : static_cast<int64_t>(dev.num_sms) * wps;
+        const int grid = static_cast<int>(warps < 4 ? 1 : (warps + 3) / 4);
+        auto kern = x_dtype == LHS_F32 ? encode_i8_warp_kernel<LHS_F32> : encode_i8_warp_kernel<LHS_BF16>;
+        return launch_pdl(kern, dim3(grid), dim3(128), 0, stream, x, seq_len, hidden, layer, flags, top_k, b,
+                          err);
+    }
     if (fmt == LHS_WIRE_I8) {
-        const bool vec = aligned && (hidden % 8 == 0);
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
         int grid = static_cast<int>(seq_len < cap ? seq_len : cap);
         if (grid < 1) grid = 1;
-        auto kern = x_dtype == LHS_F32 ? (vec ? encode_i8_kernel<LHS_F32, true> : encode_i8_kernel<LHS_F32, false>)
-                                       : (vec ? encode_i8_kernel<LHS_BF16, true> : encode_i8_kernel<LHS_BF16, false>);
+        auto kern = x_dtype == LHS_F32 ? encode_i8_kernel<LHS_F32> : encode_i8_kernel<LHS_BF16>;
         return launch_pdl(kern, dim3(grid), dim3(kI8Threads), 0, stream, x, seq_len, hidden, layer,
                           flags, top_k, b, err);
     }

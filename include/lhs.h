@@ -112,6 +112,22 @@ LHS_API int lhs_table_info(const lhs_table *t, int64_t *vocab, int32_t *hidden,
 LHS_API int lhs_embed(const lhs_table *t, const int32_t *d_ids, int64_t n, float scale,
               float *d_out, int32_t *d_err, void *stream);
 
+/* Steps 1+4 fused — the embed lookup written straight into a wire message
+ * (ADR-0008 POST /v1/embed: the looked-up rows travel in the same codec as
+ * the FFN grid; ADR-0009 Wire Layout).  d_buf receives, byte for byte, what
+ * lhs_wire_encode(fmt, x, LHS_F32, n, hidden, layer, flags, top_k, ...)
+ * writes for the rows x = lhs_embed(t, d_ids, n, scale): the 16-byte header
+ * [layer][n][flags][top_k], then the f32, f16 or per-position i8 payload.
+ * The binary32 rows are never materialised.  An id outside [0, vocab) gives
+ * a zero row and LHS_ERRBIT_BAD_TOKEN; an i8 position holding inf/NaN is
+ * written as scale 0, codes 0 with LHS_ERRBIT_NONFINITE.
+ *   0 <= n <= INT32_MAX (n == 0 writes the header only); scale finite;
+ *   d_buf 16-byte aligned, buf_bytes >= lhs_wire_bytes(fmt, n, hidden).
+ * Errors: LHS_ERR_INVALID_ARG, LHS_ERR_BUFFER_TOO_SMALL, LHS_ERR_CUDA. */
+LHS_API int lhs_embed_wire(const lhs_table *t, const int32_t *d_ids, int64_t n, float scale,
+                   int32_t fmt, uint32_t layer, uint32_t flags, uint32_t top_k, void *d_buf,
+                   size_t buf_bytes, int32_t *d_err, void *stream);
+
 /* Workspace bytes lhs_logits_topk / lhs_logits need for this table, batch,
  * k (0 for the raw-logits call) and residual dtype.  Depends on the current
  * device's SM count.  Errors as for lhs_logits_topk. */

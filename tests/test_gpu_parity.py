@@ -95,7 +95,8 @@ def _special(x):
     return x
 
 
-@pytest.mark.parametrize("shape", [(4, 256), (1, 896), (8, 5376), (3, 100), (2, 9), (0, 64)])
+@pytest.mark.parametrize("shape", [(4, 256), (1, 896), (8, 5376), (3, 100), (2, 9), (0, 64), (2, 8200),
+                                   (40, 1024)])
 @pytest.mark.parametrize("xdt", [orc.F32, orc.BF16])
 @pytest.mark.parametrize("fmt", [orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8])
 def test_wire_parity(shape, xdt, fmt):
@@ -127,6 +128,91 @@ def test_wire_parity(shape, xdt, fmt):
     y, derr = lhs.lhs_wire_decode(fmt, buf, s, h)
     assert same_f32(y.cpu().numpy(), ref_x)
     assert int(derr.item()) == ref_derr == 0
+
+
+# ---------------------------------------------------------------------------
+# steps 1+4 fused: embed straight into a wire message
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,H", [(orc.F32, 256), (orc.F16, 96), (orc.BF16, 64), (orc.Q8_0, 128),
+                                     (orc.F32, 36), (orc.BF16, 7), (orc.F16, 5376), (orc.Q8_0, 6656)])
+@pytest.mark.parametrize("fmt", [orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8])
+def test_embed_wire_matches_embed_then_encode(dtype, H, fmt):
+    V = 700
+    T = wl.make_table(dtype, V, H, 0.02, cid=600 + H, threads=4)
+    ids = np.concatenate([[0, V - 1, -1, V, 5, 5],
+                          wl.zipf_ids(600 + H, 37, V)]).astype(np.int32)
+    scale = float(np.float32(np.sqrt(np.float64(H))))
+    tab = upload_table(T, dtype, V, H)
+    x_ref, e_ref = orc.embed(T, dtype, V, H, ids, scale)
+    ref_buf, e2 = orc.wire_encode(fmt, x_ref, layer=7, flags=2, top_k=9)
+    raw, buf, pad = guarded((ref_buf.size,), torch.uint8)
+    _, err = lhs.lhs_embed_wire(tab, to_dev(ids), scale, fmt, 7, 2, 9, buf=buf)
+    assert np.array_equal(buf.cpu().numpy(), ref_buf)
+    assert int(err.item()) == (e_ref | e2)
+    assert canaries_intact(raw, pad)
+
+
+def test_embed_wire_empty_and_nonfinite_rows():
+    V, H = 64, 64
+    T = wl.make_table(orc.F16, V, H, 0.02, cid=610, threads=1)
+    T[3, 5] = 0x7C00                       # +inf in row 3
+    T[4, :] = 0x7BFF                       # 65504 everywhere in row 4: f16 stays finite
+    tab = upload_table(T, orc.F16, V, H)
+    for fmt in (orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8):
+        buf, err = lhs.lhs_embed_wire(tab, torch.empty(0, dtype=torch.int32, device="cuda"), 1.0, fmt,
+                                      1, 2, 3)
+        ref, _ = orc.wire_encode(fmt, np.zeros((0, H), np.float32), layer=1, flags=2, top_k=3)
+        assert np.array_equal(buf.cpu().numpy(), ref) and int(err.item()) == 0
+        ids = np.array([3, 4, 1], np.int32)
+        x_ref, e_ref = orc.embed(T, orc.F16, V, H, ids, 2.0)    # row 4 x 2 overflows f16 on the wire
+        ref, e2 = orc.wire_encode(fmt, x_ref)
+        buf, err = lhs.lhs_embed_wire(tab, to_dev(ids), 2.0, fmt)
+        assert np.array_equal(buf.cpu().numpy(), ref)
+        assert int(err.item()) == (e_ref | e2)
+
+
+def test_embed_wire_full_size_gemma_q8():
+    w = wl.WORKLOADS["gemma_q8"]
+    T = wl.table_for(w)
+    tab = upload_table(T, w.dtype, w.vocab, w.hidden)
+    ids = wl.ids_for(w)
+    x_ref, _ = orc.embed(T, w.dtype, w.vocab, w.hidden, ids, float(w.embed_scale))
+    for fmt in (orc.WIRE_F16, orc.WIRE_I8):
+        ref, e2 = orc.wire_encode(fmt, x_ref, layer=0, flags=0, top_k=0)
+        buf, err = lhs.lhs_embed_wire(tab, to_dev(ids), float(w.embed_scale), fmt)
+        assert np.array_equal(buf.cpu().numpy(), ref)
+        assert int(err.item()) == e2
+
+
+@pytest.mark.parametrize("xdt", [orc.F32, orc.BF16])
+def test_i8_codes_at_rounding_boundaries(xdt):
+    # quotients x / scale at, just below and just above every half-integer:
+    # the encoder's product-with-reciprocal shortcut must fall back to the
+    # correctly rounded divide exactly where rounding could differ
+    H = 1024
+    rows = []
+    for m in (1.0, 3.0, 1e-3, 7.5e-39):      # last: a subnormal scale
+        scale = np.float32(np.float32(m) / np.float32(127.0))
+        k = np.arange(-127, 127, dtype=np.float32)
+        base = ((k + np.float32(0.5)) * scale).astype(np.float32)
+        vals = np.concatenate([base, np.nextafter(base, np.float32(np.inf)),
+                               np.nextafter(base, np.float32(-np.inf)), [np.float32(m)]])
+        row = np.zeros(H, np.float32)
+        row[:vals.size] = vals[:H]
+        row[H - 1] = np.float32(m)
+        rows.append(row)
+    x = np.stack(rows)
+    if xdt == orc.BF16:
+        xs = wl.f32_to_bf16_bits(x)
+        xv = orc.bf16_to_f32(xs).reshape(x.shape)
+        xd = to_dev(xs).view(torch.bfloat16).reshape(x.shape)
+    else:
+        xv, xd = x, to_dev(x)
+    ref, ref_err = orc.wire_encode(orc.WIRE_I8, xv)
+    buf, err = lhs.lhs_wire_encode(orc.WIRE_I8, xd)
+    assert np.array_equal(buf.cpu().numpy(), ref)
+    assert int(err.item()) == ref_err
 
 
 def test_wire_decode_malformed():
