@@ -51,6 +51,13 @@ def parse_args():
                     help="override the workload's vocab rows (small cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--untied", action="store_true",
+                    help="lm_head on a second table of the same shape (an untied lm_head)")
+    ap.add_argument("--raw-logits", action="store_true",
+                    help="the step's lm_head call returns the full logits (raw-logits mode)")
+    ap.add_argument("--wire-accuracy", action="store_true",
+                    help="top-k agreement of logits from wire-decoded residuals with the "
+                         "originals (f16: top-5, i8: top-1) on the gemma31b and batched workloads")
     ap.add_argument("--sweep", action="store_true",
                     help="steady-state sweep of the sub-10-us steps (gather, wire codecs): one "
                          "JSON line per point instead of the step line")
@@ -179,7 +186,7 @@ class Ctx:
     pass
 
 
-def setup(name, batch, device, vocab=None):
+def setup(name, batch, device, vocab=None, untied=False, raw=False):
     import dataclasses
 
     import torch
@@ -204,6 +211,13 @@ def setup(name, batch, device, vocab=None):
 
     c.T_host = wl.table_for(w)
     c.table = lhs.lhs_table_init(up(c.T_host), w.vocab, w.hidden, w.dtype)
+    c.untied, c.raw = untied, raw
+    if untied:
+        # a second table, same shape and distribution, other seed
+        c.lm_table = lhs.lhs_table_init(up(wl.make_table(w.dtype, w.vocab, w.hidden, 0.02, cid=w.cid + 50)),
+                                        w.vocab, w.hidden, w.dtype)
+    else:
+        c.lm_table = c.table
     c.ids_host = wl.ids_for(w) if w.n_ids else wl.zipf_ids(w.cid, 1, w.vocab)
     c.R_host = wl.residuals_for(w, c.B)
     c.ids = up(c.ids_host)
@@ -215,8 +229,9 @@ def setup(name, batch, device, vocab=None):
     c.emb_out = torch.empty((c.n_ids, H), dtype=torch.float32, device=device)
     rd = lhs.LHS_F32 if w.resid_dtype == wl.F32 else lhs.LHS_BF16
     c.rd = rd
-    c.ws = torch.empty(lhs.lhs_logits_topk_workspace(c.table, c.B, c.k, rd), dtype=torch.uint8,
-                       device=device)
+    c.ws = torch.empty(lhs.lhs_logits_topk_workspace(c.lm_table, c.B, 0 if raw else c.k, rd),
+                       dtype=torch.uint8, device=device)
+    c.raw_out = torch.empty((c.B, w.vocab), dtype=torch.float32, device=device) if raw else None
     c.top_ids = torch.empty((c.B, c.k), dtype=torch.int32, device=device)
     c.top_logits = torch.empty((c.B, c.k), dtype=torch.float32, device=device)
     c.top_probs = torch.empty((c.B, c.k), dtype=torch.float32, device=device)
@@ -230,13 +245,19 @@ def setup(name, batch, device, vocab=None):
     import ctypes
     L = lhs.lib()
     tb = ctypes.byref(c.table.c)
+    lb = ctypes.byref(c.lm_table.c)
+    if raw:
+        lm_call = (L.lhs_logits, (lb, c.resid.data_ptr(), rd, c.B, c.raw_out.data_ptr(), c.ws.data_ptr(),
+                                  c.ws.numel(), c.err.data_ptr(), c.sptr))
+    else:
+        lm_call = (L.lhs_logits_topk, (lb, c.resid.data_ptr(), rd, c.B, c.k, ctypes.c_float(1.0),
+                                       c.top_ids.data_ptr(), c.top_logits.data_ptr(),
+                                       c.top_probs.data_ptr(), c.ws.data_ptr(), c.ws.numel(),
+                                       c.err.data_ptr(), c.sptr))
     c.calls = [
         (L.lhs_embed, (tb, c.ids.data_ptr(), c.n_ids, ctypes.c_float(c.scale),
                        c.emb_out.data_ptr(), c.err.data_ptr(), c.sptr)),
-        (L.lhs_logits_topk, (tb, c.resid.data_ptr(), rd, c.B, c.k, ctypes.c_float(1.0),
-                             c.top_ids.data_ptr(), c.top_logits.data_ptr(),
-                             c.top_probs.data_ptr(), c.ws.data_ptr(), c.ws.numel(),
-                             c.err.data_ptr(), c.sptr)),
+        lm_call,
         (L.lhs_wire_encode, (c.fmt, c.resid.data_ptr(), rd, c.B, H, 0, 0, c.k,
                              c.wire_buf.data_ptr(), c.wire_bytes, c.err.data_ptr(), c.sptr)),
         (L.lhs_wire_decode, (c.fmt, c.wire_buf.data_ptr(), c.wire_bytes, c.B, H,
@@ -248,7 +269,7 @@ def setup(name, batch, device, vocab=None):
         c.flush_buf = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=device)
     # kernels per step: embed 1, the lm_head call as the library reports it
     # for this plan, wire encode 1, decode 1
-    lm = lhs.lhs_logits_topk_launches(c.table, c.B, c.k, rd)
+    lm = lhs.lhs_logits_topk_launches(c.lm_table, c.B, 0 if raw else c.k, rd)
     c.lm_launches = lm
     c.gemm = (w.dtype == wl.BF16 and w.resid_dtype == wl.BF16 and c.B > 8)
     c.launches_per_step = 1 + lm + 1 + 1
@@ -296,12 +317,14 @@ def recorded_traffic(name):
     return nbytes, src
 
 
-def workload_config(w, B, k, fmt, n_ids, world):
+def workload_config(w, B, k, fmt, n_ids, world, untied=False, raw=False):
     """The `config` object of the JSON line (both arms)."""
     flush = w.table_bytes < 2 * L2_BYTES
     return {"workload": w.name, "vocab": w.vocab, "hidden": w.hidden,
             "table_dtype": wl.DTYPE_NAMES[w.dtype], "table_bytes": w.table_bytes,
             "embed_ids": n_ids, "lm_batch": B, "k": k,
+            "lm_table": "untied (second table, same shape)" if untied else "tied (the embedding table)",
+            "lm_output": "raw logits [batch x vocab]" if raw else "top-k ids, logits, probs",
             "wire": {0: "f32", 1: "f16", 2: "i8"}[fmt],
             "l2": ("flushed before every timed iteration (a 258 MB buffer rewritten outside the "
                    "timed events): the table fits in L2" if flush else
@@ -314,7 +337,8 @@ def lm_bytes(c):
     residuals once, the top-k outputs once."""
     w = c.w
     relt = 4 if w.resid_dtype == wl.F32 else 2
-    return w.vocab * w.row_bytes + c.B * w.hidden * relt + c.B * c.k * 12
+    out = c.B * w.vocab * 4 if c.raw else c.B * c.k * 12
+    return w.vocab * w.row_bytes + c.B * w.hidden * relt + out
 
 
 def step_bytes(c):
@@ -394,6 +418,7 @@ def time_e2e(c, steps):
     if c.w.resid_dtype == wl.BF16:
         h_res = h_res.view(torch.bfloat16)
     h_emb = torch.empty(c.emb_out.shape, dtype=torch.float32).pin_memory()
+    h_raw = torch.empty(c.raw_out.shape, dtype=torch.float32).pin_memory() if c.raw else None
     h_tid = torch.empty(c.top_ids.shape, dtype=torch.int32).pin_memory()
     h_tlg = torch.empty(c.top_logits.shape, dtype=torch.float32).pin_memory()
     h_tpr = torch.empty(c.top_probs.shape, dtype=torch.float32).pin_memory()
@@ -402,21 +427,27 @@ def time_e2e(c, steps):
     d_ids = torch.empty_like(c.ids)
     d_res = torch.empty_like(c.resid)
     h2d = h_ids.numel() * 4 + h_res.numel() * h_res.element_size()
-    d2h = (h_emb.numel() * 4 + h_tid.numel() * 4 + h_tlg.numel() * 4 + h_tpr.numel() * 4
-           + h_buf.numel() + 4)
+    lm_out = h_raw.numel() * 4 if c.raw else h_tid.numel() * 4 + h_tlg.numel() * 4 + h_tpr.numel() * 4
+    d2h = h_emb.numel() * 4 + lm_out + h_buf.numel() + 4
 
     def one():
         d_ids.copy_(h_ids, non_blocking=True)
         d_res.copy_(h_res, non_blocking=True)
         c.err.zero_()
         lhs.lhs_embed(c.table, d_ids, c.scale, out=c.emb_out, err=c.err)
-        lhs.lhs_logits_topk(c.table, d_res, c.k, 1.0, ws=c.ws, ids=c.top_ids,
-                            logits=c.top_logits, probs=c.top_probs, err=c.err)
+        if c.raw:
+            lhs.lhs_logits(c.lm_table, d_res, out=c.raw_out, ws=c.ws, err=c.err)
+        else:
+            lhs.lhs_logits_topk(c.lm_table, d_res, c.k, 1.0, ws=c.ws, ids=c.top_ids,
+                                logits=c.top_logits, probs=c.top_probs, err=c.err)
         lhs.lhs_wire_encode(c.fmt, d_res, 0, 0, c.k, buf=c.wire_buf, err=c.err)
         h_emb.copy_(c.emb_out, non_blocking=True)
-        h_tid.copy_(c.top_ids, non_blocking=True)
-        h_tlg.copy_(c.top_logits, non_blocking=True)
-        h_tpr.copy_(c.top_probs, non_blocking=True)
+        if c.raw:
+            h_raw.copy_(c.raw_out, non_blocking=True)
+        else:
+            h_tid.copy_(c.top_ids, non_blocking=True)
+            h_tlg.copy_(c.top_logits, non_blocking=True)
+            h_tpr.copy_(c.top_probs, non_blocking=True)
         h_buf.copy_(c.wire_buf, non_blocking=True)
         h_err.copy_(c.err, non_blocking=True)
 
@@ -496,7 +527,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * B / value, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, B, k, fmt, w.n_ids or 1, world),
+            "config": workload_config(w, B, k, fmt, w.n_ids or 1, world, args.untied, args.raw_logits),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -603,6 +634,49 @@ def run_sweep(dev, peak):
     return 0
 
 
+def wire_agreement(lhs, tab, x, k, fmt):
+    """Fractions of residuals whose top-k ids from decode(encode(x)) equal
+    those from x: (same ordered ids, same set).  x: f32 CUDA tensor [B, H]."""
+    import torch
+    ref, _, _, e0 = lhs.lhs_logits_topk(tab, x, k, want_probs=False)
+    buf, e1 = lhs.lhs_wire_encode(fmt, x)
+    y, e2 = lhs.lhs_wire_decode(fmt, buf, x.shape[0], x.shape[1])
+    got, _, _, e3 = lhs.lhs_logits_topk(tab, y, k, want_probs=False)
+    torch.cuda.synchronize()
+    for e in (e0, e1, e2, e3):
+        if int(e.item()) != 0:
+            raise RuntimeError(f"error word {int(e.item())}")
+    a, b = ref.cpu().numpy(), got.cpu().numpy()
+    ordered = float(np.mean(np.all(a == b, axis=1)))
+    same_set = float(np.mean([set(r) == set(g) for r, g in zip(a, b)]))
+    return ordered, same_set
+
+
+def run_wire_accuracy(dev):
+    """ADR-0009 Validation: f16 wire must keep the top-5 tokens, i8 the top-1,
+    measured on synthetic tables and residuals of the C4 and C5 shapes."""
+    import torch
+
+    import embedding_lookup_tied_gb300 as lhs
+    for name, B in (("gemma31b", 64), ("batched", 256)):
+        w = wl.WORKLOADS[name]
+        T = wl.table_for(w)
+        t = torch.from_numpy(T.view(np.int16)).to(dev)
+        del T
+        tab = lhs.lhs_table_init(t, w.vocab, w.hidden, w.dtype)
+        R = wl.residuals_for(w, B)
+        xv = R if w.resid_dtype == wl.F32 else (R.astype(np.uint32) << 16).view(np.float32)  # bf16 -> f32, exact
+        x = torch.from_numpy(np.ascontiguousarray(xv)).to(dev)
+        for fmt, fname, k in ((lhs.LHS_WIRE_F16, "f16", 5), (lhs.LHS_WIRE_I8, "i8", 1)):
+            ordered, same_set = wire_agreement(lhs, tab, x, k, fmt)
+            print(json.dumps({"wire_accuracy": fname, "workload": name, "residuals": B, "top_k": k,
+                              "agreement_ordered": ordered, "agreement_set": same_set,
+                              "data": "synthetic table and residuals"}), flush=True)
+        del t, tab
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -612,13 +686,17 @@ def main():
         import torch
         torch.cuda.set_device(local)
         return run_sweep(torch.device("cuda", local), load_peaks()[0])
+    if args.wire_accuracy:
+        import torch
+        torch.cuda.set_device(local)
+        return run_wire_accuracy(torch.device("cuda", local))
     import torch
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
-    c = setup(args.workload, args.batch, dev, args.vocab)
+    c = setup(args.workload, args.batch, dev, args.vocab, args.untied, args.raw_logits)
     steps = args.steps or default_steps(args.workload)
     ms, lm_ms, clocks = time_device(c, steps, max(3, args.warmup), world)
     ms = max_over_ranks(ms, world, dev)
@@ -629,7 +707,8 @@ def main():
     value = world * c.B / (ms / 1e3)
     lmb = lm_bytes(c)
     achieved = lmb / (lm_ms / 1e3) / 1e9
-    traffic, traffic_src = recorded_traffic(c.w.name) if not args.vocab else (None, "vocab override")
+    traffic, traffic_src = (recorded_traffic(c.w.name) if not (args.vocab or args.raw_logits or args.untied)
+                            else (None, "no capture recorded for this variant"))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
@@ -637,10 +716,10 @@ def main():
         "dtype": {wl.F32: "f32", wl.F16: "f16", wl.BF16: "bf16", wl.Q8_0: "q8_0"}[c.w.dtype]
                  + "-table/f32-accumulate",
         "data": "synthetic",
-        "config": workload_config(c.w, c.B, c.k, c.fmt, c.n_ids, world),
+        "config": workload_config(c.w, c.B, c.k, c.fmt, c.n_ids, world, c.untied, c.raw),
         "hbm_gbs_step": world * step_bytes(c) / (ms / 1e3) / 1e9,
         "embed_rows_per_s": world * c.n_ids / (ms / 1e3),
-        "roofline": {"kernel": f"lhs_logits_topk call ({c.lm_launches} kernels)",
+        "roofline": {"kernel": f"{'lhs_logits' if c.raw else 'lhs_logits_topk'} call ({c.lm_launches} kernels)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": traffic, "traffic_source": traffic_src,

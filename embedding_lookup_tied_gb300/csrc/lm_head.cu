@@ -1005,7 +1005,35 @@ __device__ __forceinline__ float table_elem(const uint8_t *row, int j) {
     return __fmul_rn(d, static_cast<float>(static_cast<int8_t>(__ldg(blk + 2 + (j & 31)))));
 }
 
-template <int DT, bool RAW>
+// Dot products of kSimtRows rows with the Bc residuals in shared memory,
+// 8 elements per lane step (rows 16-byte aligned, Q8_0 2-byte; K % 8 == 0):
+// every row's loads of a step are issued before its multiplies.
+constexpr int kSimtRows = 4;
+
+template <int DT>
+__device__ __forceinline__ void simt_rows8(const uint8_t *const (&rows)[kSimtRows], int K, const float *xs,
+                                           int Bc, int lane, float (&acc)[kSimtRows][kBatchChunk]) {
+    const int ng = K >> 3;
+    for (int g = lane; g < ng; g += 32) {
+        float e[kSimtRows][8];
+#pragma unroll
+        for (int r = 0; r < kSimtRows; ++r) row_elements8<DT>(rows[r], g, e[r]);
+#pragma unroll
+        for (int b = 0; b < kBatchChunk; ++b) {
+            if (b < Bc) {
+                const float4 x0 = *reinterpret_cast<const float4 *>(xs + b * K + 8 * g);
+                const float4 x1 = *reinterpret_cast<const float4 *>(xs + b * K + 8 * g + 4);
+                const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int r = 0; r < kSimtRows; ++r)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[r][b] = fmaf(e[r][i], xv[i], acc[r][b]);
+            }
+        }
+    }
+}
+
+template <int DT, bool RAW, bool VEC>
 __global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtParams p) {
     extern __shared__ uint8_t dyn_smem[];
     TopkShared &tk = *reinterpret_cast<TopkShared *>(dyn_smem);
@@ -1032,34 +1060,51 @@ __global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtPa
     float m_st = -INFINITY, s_st = 0.0f;  // lane b < Bc: column b
     for (int blk = 0; blk < nblk; ++blk) {
         const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
-        for (int rr = 0; rr < 16; ++rr) {
-            const int64_t v = row0 + warp * 16 + rr;
-            if (v >= r1) break;
-            const uint8_t *row = p.table + v * p.row_bytes;
-            float acc[kBatchChunk];
+        for (int rr = 0; rr < 16; rr += kSimtRows) {
+            const int64_t v0 = row0 + warp * 16 + rr;
+            if (v0 >= r1) break;
+            float acc[kSimtRows][kBatchChunk];
 #pragma unroll
-            for (int b = 0; b < kBatchChunk; ++b) acc[b] = 0.0f;
-            for (int j = lane; j < p.K; j += 32) {
-                const float e = table_elem<DT>(row, j);
+            for (int r = 0; r < kSimtRows; ++r)
+#pragma unroll
+                for (int b = 0; b < kBatchChunk; ++b) acc[r][b] = 0.0f;
+            if (VEC) {
+                // rows past the range read row v0 again; their sums are dropped
+                const uint8_t *rows[kSimtRows];
+#pragma unroll
+                for (int r = 0; r < kSimtRows; ++r) rows[r] = p.table + (v0 + r < r1 ? v0 + r : v0) * p.row_bytes;
+                simt_rows8<DT>(rows, p.K, xs, p.Bc, lane, acc);
+            } else {
+#pragma unroll
+                for (int r = 0; r < kSimtRows; ++r) {
+                    const uint8_t *row = p.table + (v0 + r < r1 ? v0 + r : v0) * p.row_bytes;
+                    for (int j = lane; j < p.K; j += 32) {
+                        const float e = table_elem<DT>(row, j);
+#pragma unroll
+                        for (int b = 0; b < kBatchChunk; ++b)
+                            if (b < p.Bc) acc[r][b] = fmaf(e, xs[b * p.K + j], acc[r][b]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kSimtRows; ++r) {
+                const int64_t v = v0 + r;
+#pragma unroll
+                for (int b = 0; b < kBatchChunk; ++b) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc[r][b] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][b], o);
+                }
+                float mine = 0.0f;
 #pragma unroll
                 for (int b = 0; b < kBatchChunk; ++b)
-                    if (b < p.Bc) acc[b] = fmaf(e, xs[b * p.K + j], acc[b]);
-            }
-#pragma unroll
-            for (int b = 0; b < kBatchChunk; ++b) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xFFFFFFFFu, acc[b], o);
-            }
-            float mine = 0.0f;
-#pragma unroll
-            for (int b = 0; b < kBatchChunk; ++b)
-                if (lane == b) mine = acc[b];
-            if (lane < p.Bc) {
-                if (RAW) {
-                    p.raw[static_cast<int64_t>(p.b_off + lane) * p.V + v] = mine;
-                } else {
-                    ms_update(m_st, s_st, mine, p.invT);
-                    topk_offer(tk, lane, cap, mine, static_cast<int32_t>(v));
+                    if (lane == b) mine = acc[r][b];
+                if (v < r1 && lane < p.Bc) {
+                    if (RAW) {
+                        p.raw[static_cast<int64_t>(p.b_off + lane) * p.V + v] = mine;
+                    } else {
+                        ms_update(m_st, s_st, mine, p.invT);
+                        topk_offer(tk, lane, cap, mine, static_cast<int32_t>(v));
+                    }
                 }
             }
         }
@@ -1324,13 +1369,20 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
         }
     } else {
         const size_t smem = simt_smem_bytes(plan.batch_chunk, t.hidden);
+        // 8-element steps: K % 8 == 0, rows 16-byte aligned (Q8_0: 2-byte, always)
+        bool vec = t.hidden % 8 == 0;
+        if (t.dtype != LHS_Q8_0)
+            vec = vec && reinterpret_cast<uintptr_t>(t.data) % 16 == 0 && t.row_bytes % 16 == 0;
         void (*kern)(const SimtParams);
+#define LHS_SIMT(DT) (raw ? (vec ? gemv_simt_kernel<DT, true, true> : gemv_simt_kernel<DT, true, false>) \
+                          : (vec ? gemv_simt_kernel<DT, false, true> : gemv_simt_kernel<DT, false, false>))
         switch (t.dtype) {
-        case LHS_F32: kern = raw ? gemv_simt_kernel<LHS_F32, true> : gemv_simt_kernel<LHS_F32, false>; break;
-        case LHS_F16: kern = raw ? gemv_simt_kernel<LHS_F16, true> : gemv_simt_kernel<LHS_F16, false>; break;
-        case LHS_BF16: kern = raw ? gemv_simt_kernel<LHS_BF16, true> : gemv_simt_kernel<LHS_BF16, false>; break;
-        default: kern = raw ? gemv_simt_kernel<LHS_Q8_0, true> : gemv_simt_kernel<LHS_Q8_0, false>; break;
+        case LHS_F32: kern = LHS_SIMT(LHS_F32); break;
+        case LHS_F16: kern = LHS_SIMT(LHS_F16); break;
+        case LHS_BF16: kern = LHS_SIMT(LHS_BF16); break;
+        default: kern = LHS_SIMT(LHS_Q8_0); break;
         }
+#undef LHS_SIMT
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         for (int c0 = 0; c0 < batch; c0 += plan.batch_chunk) {

@@ -215,6 +215,25 @@ def test_i8_codes_at_rounding_boundaries(xdt):
     assert int(err.item()) == ref_err
 
 
+def test_wire_accuracy_topk_agreement():
+    # ADR-0009 Validation on a synthetic C4-shaped case: logits from
+    # wire-decoded residuals keep the top-5 (f16) and the top-1 (i8).  The
+    # tables are Gaussian, whose top logits sit closer together than a trained
+    # model's; the bounds below follow from the codecs' error against those
+    # spacings (f16: relative 2^-11 per value -> swaps a few in 10^3; i8: noise
+    # about 0.02 sigma on a logit difference against a top-1 margin of about
+    # 0.3 sigma -> a few in 10^2).
+    import bench
+    V, H, B = 16384, 5376, 64
+    T = wl.make_table(orc.F16, V, H, 0.02, cid=700, threads=8)
+    tab = upload_table(T, orc.F16, V, H)
+    x = to_dev(wl.residuals(701, B, H, (0.5, 8.0)))
+    ordered, same_set = bench.wire_agreement(lhs, tab, x, 5, orc.WIRE_F16)
+    assert same_set >= 0.95 and ordered >= 0.9
+    ordered, _ = bench.wire_agreement(lhs, tab, x, 1, orc.WIRE_I8)
+    assert ordered >= 0.85
+
+
 def test_wire_decode_malformed():
     x = np.ones((3, 64), np.float32)
     for fmt in (orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8):
@@ -299,6 +318,29 @@ def test_lm_head_parity(case):
         rp = orc.softmax_probs(Lg[b], 0.7, rid)
         assert np.all(np.abs(probs[b] - rp) <= PROB_RTOL * rp), b
         check_topk_against_fp64(ids[b], vals[b], L64[b], S64[b], k, rtol)
+
+
+@pytest.mark.parametrize("lm_dtype", [orc.BF16, orc.Q8_0, orc.F32])
+def test_untied_lm_head_on_embedded_rows(lm_dtype):
+    # untied: rows gathered from one table, projected on another
+    V, H, k = 3000, 128, 8
+    E = wl.make_table(orc.F16, V, H, 0.02, cid=280, threads=4)
+    T = wl.make_table(lm_dtype, V, H, 0.02, cid=281, threads=4)
+    et, lt = upload_table(E, orc.F16, V, H), upload_table(T, lm_dtype, V, H)
+    ids = wl.zipf_ids(282, 5, V)
+    x, err = lhs.lhs_embed(et, to_dev(ids), 11.0)
+    assert int(err.item()) == 0
+    xv, _ = orc.embed(E, orc.F16, V, H, ids, 11.0)
+    assert same_f32(x.cpu().numpy(), xv)
+    L64, S64 = orc.logits(T, lm_dtype, V, H, xv, threads=8, with_sumabs=True)
+    top, vals, _, err = lhs.lhs_logits_topk(lt, x, k)
+    assert int(err.item()) == 0
+    raw, _ = lhs.lhs_logits(lt, x)
+    Lg = raw.cpu().numpy()
+    assert np.all(np.abs(Lg.astype(np.float64) - L64) <= RTOL[lm_dtype] * S64 + 1e-30)
+    for b in range(len(ids)):
+        rid, rv = orc.topk_f32(Lg[b], k)
+        assert np.array_equal(top.cpu().numpy()[b], rid)
 
 
 def test_launch_count_follows_the_plan():
