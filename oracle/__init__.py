@@ -37,7 +37,7 @@ _CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
            "-Wall", "-Wextra"]
 
 # Oracle's own numbering of table types, wire formats and error bits.
-F32, F16, BF16, Q8_0 = 0, 1, 2, 3
+F32, F16, BF16, Q8_0, FP8_E4M3 = 0, 1, 2, 3, 4
 WIRE_F32, WIRE_F16, WIRE_I8 = 0, 1, 2
 ERR_BAD_TOKEN, ERR_MALFORMED, ERR_NONFINITE = 1, 2, 4
 Q8_BLOCK, Q8_BLOCK_BYTES = 32, 34
@@ -89,6 +89,9 @@ def _load():
                                                ctypes.c_uint32, ctypes.c_uint32,
                                                ctypes.c_uint32, P, P]),
             "orc_wire_decode": (ctypes.c_int, [ctypes.c_int, P, i64, i32, i32, P, P]),
+            "orc_fp8_e4m3_value": (f64, [ctypes.c_uint8]),
+            "orc_mixed_row_bytes": (i64, [ctypes.c_int, i32]),
+            "orc_embed_mixed": (None, [P, P, P, i64, i32, P, i64, f32, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -169,6 +172,50 @@ def embed(table: np.ndarray, dtype: int, vocab: int, hidden: int, ids,
     if rc:
         raise ValueError(f"orc_embed rc={rc}")
     return out, int(err.value)
+
+
+def fp8_e4m3_value(codes) -> np.ndarray:
+    """Exact values (float64) of OCP FP8 E4M3 codes."""
+    c = _c(codes, np.uint8)
+    L = _load()
+    return np.array([L.orc_fp8_e4m3_value(int(v)) for v in c.reshape(-1)], np.float64).reshape(c.shape)
+
+
+def mixed_row_bytes(dtype: int, hidden: int) -> int:
+    return int(_load().orc_mixed_row_bytes(dtype, hidden))
+
+
+def embed_mixed(data: np.ndarray, row_offset, row_dtype, vocab: int, hidden: int, ids,
+                scale: float):
+    """Gather from a table whose rows carry their own element type (HELIX §3
+    sidecar): row r decoded as row_dtype[r] from data[row_offset[r]:]."""
+    db = np.ascontiguousarray(data).view(np.uint8).reshape(-1)
+    off = _c(row_offset, np.int64)
+    dts = _c(row_dtype, np.uint8)
+    ids = _c(ids, np.int32)
+    if off.size < vocab or dts.size < vocab:
+        raise ValueError("sidecar shorter than vocab")
+    for r in range(vocab):
+        rb = mixed_row_bytes(int(dts[r]), hidden)
+        if rb > 0 and off[r] + rb > db.size:
+            raise ValueError("row past the end of the data")
+    out = np.empty((ids.size, hidden), np.float32)
+    err = ctypes.c_int32(0)
+    _load().orc_embed_mixed(_ptr(db), _ptr(off), _ptr(dts), vocab, hidden, _ptr(ids), ids.size,
+                            ctypes.c_float(np.float32(scale)), _ptr(out), ctypes.byref(err))
+    return out, int(err.value)
+
+
+def unique_ids(ids, vocab: int):
+    """HELIX Appendix B "tokenize, dedupe, fetch": the distinct valid ids in
+    ascending order, each position's index into them (-1 for an id outside
+    [0, vocab)) and the BAD_TOKEN bit if there was one."""
+    ids = np.asarray(ids, np.int64).reshape(-1)
+    ok = (ids >= 0) & (ids < vocab)
+    uniq, inv = np.unique(ids[ok], return_inverse=True)
+    inverse = np.full(ids.size, -1, np.int32)
+    inverse[ok] = inv.astype(np.int32)
+    return uniq.astype(np.int32), inverse, (1 if not ok.all() else 0)
 
 
 def decode_rows(table: np.ndarray, dtype: int, hidden: int, row0: int,

@@ -39,7 +39,7 @@
 
 /* Table element types (the oracle's own numbering; the public header uses
  * the same values because both follow the same documented enumeration). */
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_Q8_0 = 3 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_Q8_0 = 3, ORC_FP8_E4M3 = 4 };
 /* Wire formats: [ADR-0009] Decision table — f32, f16, i8. */
 enum { ORC_WIRE_F32 = 0, ORC_WIRE_F16 = 1, ORC_WIRE_I8 = 2 };
 /* Data-dependent error bits ([ADR-0008] Error contract: bad token ids,
@@ -233,6 +233,72 @@ int orc_embed(const uint8_t *table, int dtype, int64_t vocab, int32_t hidden,
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Mixed-precision rows ([HELIX] §3, optional sidecar embed-rows.idx: rows   */
+/* of one table stored at different precisions, e.g. fp16 for common tokens */
+/* and fp8 for the long tail, or quantised rows with their dequantisation    */
+/* header inline).  Reading: the sidecar gives, per row, its byte offset in  */
+/* the data and its element type; "fp8" is the OCP 8-bit E4M3 format.        */
+/* ------------------------------------------------------------------------- */
+
+/* OCP FP8 E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; no
+ * infinities; exponent and fraction all ones is NaN.  Exact in binary64. */
+double orc_fp8_e4m3_value(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xf;
+    int m = c & 0x7;
+    double v;
+    if (e == 15 && m == 7) {
+        v = NAN;
+    } else if (e == 0) {
+        v = ldexp((double)m, -9);                /* subnormal: (m/8) * 2^-6 */
+    } else {
+        v = ldexp((double)(8 + m), e - 10);      /* (1 + m/8) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+int64_t orc_mixed_row_bytes(int dtype, int32_t hidden)
+{
+    if (dtype == ORC_FP8_E4M3) return hidden > 0 ? (int64_t)hidden : -1;
+    return orc_row_bytes(dtype, hidden);
+}
+
+/* out[t][j] = f32(element(row ids[t], j) * scale) where row r is decoded
+ * with its own type row_dtype[r] from data + row_offset[r].  A bad id gives a
+ * zero row and BAD_TOKEN; a row whose type code is not a row type gives a
+ * zero row and MALFORMED. */
+void orc_embed_mixed(const uint8_t *data, const int64_t *row_offset, const uint8_t *row_dtype,
+                     int64_t vocab, int32_t hidden, const int32_t *ids, int64_t n, float scale,
+                     float *out, int32_t *err_bits)
+{
+    int64_t t;
+    int32_t j;
+    for (t = 0; t < n; ++t) {
+        int64_t id = ids[t];
+        float *o = out + t * (int64_t)hidden;
+        int dt;
+        const uint8_t *row;
+        if (id < 0 || id >= vocab) {
+            for (j = 0; j < hidden; ++j) o[j] = 0.0f;
+            *err_bits |= ORC_ERR_BAD_TOKEN;
+            continue;
+        }
+        dt = row_dtype[id];
+        row = data + row_offset[id];
+        if (dt < ORC_F32 || dt > ORC_FP8_E4M3 || orc_mixed_row_bytes(dt, hidden) < 0) {
+            for (j = 0; j < hidden; ++j) o[j] = 0.0f;
+            *err_bits |= ORC_ERR_MALFORMED;
+            continue;
+        }
+        for (j = 0; j < hidden; ++j) {
+            float e = dt == ORC_FP8_E4M3 ? (float)orc_fp8_e4m3_value(row[j]) : orc_row_element(row, dt, j);
+            o[j] = e * scale;                     /* one binary32 multiply */
+        }
+    }
 }
 
 /* Decode whole tables / residual arrays to f32 (test convenience). */

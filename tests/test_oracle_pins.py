@@ -451,3 +451,91 @@ def test_wire_i8_nonfinite_and_malformed():
     assert err == orc.ERR_MALFORMED and np.all(y == 7.0)
     with pytest.raises(ValueError):       # buffer shorter than the message
         orc.wire_decode(orc.WIRE_F16, orc.wire_encode(orc.WIRE_F16, x)[0], 4, 16)
+
+
+# ---------------------------------------------------------------------------
+# Mixed-precision rows (HELIX §3 sidecar) and dedup (HELIX Appendix B)
+# ---------------------------------------------------------------------------
+
+def test_fp8_e4m3_published_values():
+    # OCP 8-bit floating point, E4M3: bias 7, no infinities, S.1111.111 NaN,
+    # largest finite 448, smallest normal 2^-6, smallest subnormal 2^-9
+    v = orc.fp8_e4m3_value(np.arange(256, dtype=np.uint8))
+    assert v[0x38] == 1.0 and v[0xB8] == -1.0
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert v[0x08] == 2.0 ** -6 and v[0x01] == 2.0 ** -9
+    assert v[0x00] == 0.0 and math.copysign(1.0, v[0x80]) == -1.0
+    nan = np.isnan(v)
+    assert sorted(np.nonzero(nan)[0].tolist()) == [0x7F, 0xFF]
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)                       # codes order like values
+    assert np.array_equal(v[0x80:0xFF], -v[:0x7F])         # sign bit only flips the sign
+    # within each binade the eight codes are evenly spaced by 2^(e-10)
+    for e in range(1, 16):
+        codes = [(e << 3) | m for m in range(8) if (e << 3) | m <= 0x7E]
+        step = np.diff(v[codes])
+        assert np.all(step == 2.0 ** (e - 10))
+
+
+def _mixed_table(values, dtypes):
+    """Rows of `values` (k * 2^-3, |k| <= 15: exact in every row type) stored
+    each in its own type; returns (data, offsets)."""
+    vocab, hidden = values.shape
+    chunks, offsets, off = [], [], 0
+    for r in range(vocab):
+        x = values[r].astype(np.float32)
+        dt = int(dtypes[r])
+        if dt == orc.F32:
+            b = x.tobytes()
+        elif dt == orc.F16:
+            b = x.astype(np.float16).tobytes()
+        elif dt == orc.BF16:
+            b = (x.view(np.uint32) >> 16).astype(np.uint16).tobytes()
+        elif dt == orc.Q8_0:
+            q = np.rint(x * 8).astype(np.int8).reshape(-1, 32)
+            d = np.float16(0.125).tobytes()
+            b = b"".join(d + blk.tobytes() for blk in q)
+        else:   # fp8 e4m3: pick the code whose exact value equals x
+            table = orc.fp8_e4m3_value(np.arange(0x7F, dtype=np.uint8))
+            codes = []
+            for val in x:
+                c = int(np.nonzero(table == abs(val))[0][0])
+                codes.append(c | (0x80 if val < 0 else 0))
+            b = bytes(codes)
+        b += bytes((-len(b)) % 16)        # 16-byte row alignment in the data
+        offsets.append(off)
+        chunks.append(b)
+        off += len(b)
+    return np.frombuffer(b"".join(chunks), np.uint8), np.array(offsets, np.int64)
+
+
+def test_mixed_rows_match_the_homogeneous_gather():
+    g = np.random.default_rng(5)
+    vocab, hidden = 40, 64
+    values = (g.integers(-15, 16, (vocab, hidden)) * 0.125).astype(np.float32)
+    dtypes = np.array([r % 5 for r in range(vocab)], np.uint8)   # every row type
+    data, offs = _mixed_table(values, dtypes)
+    ids = np.array([0, 1, 2, 3, 4, 39, 17, 17, -1, 40], np.int32)
+    got, err = orc.embed_mixed(data, offs, dtypes, vocab, hidden, ids, 3.0)
+    ref, ref_err = orc.embed(values, orc.F32, vocab, hidden, ids, 3.0)
+    assert np.array_equal(got, ref) and err == ref_err == orc.ERR_BAD_TOKEN
+    # an unknown row type: zero row, MALFORMED
+    bad = dtypes.copy()
+    bad[7] = 9
+    got, err = orc.embed_mixed(data, offs, bad, vocab, hidden, [7, 6], 1.0)
+    assert np.all(got[0] == 0.0) and np.array_equal(got[1], values[6]) and err == orc.ERR_MALFORMED
+
+
+def test_unique_ids_against_brute_force():
+    g = np.random.default_rng(9)
+    for n, vocab in ((0, 10), (1, 10), (50, 7), (300, 1000)):
+        ids = g.integers(-3, vocab + 3, n).astype(np.int32)
+        uniq, inv, bad = orc.unique_ids(ids, vocab)
+        valid = [int(i) for i in ids if 0 <= i < vocab]
+        assert uniq.tolist() == sorted(set(valid))
+        for i, x in enumerate(ids):
+            if 0 <= x < vocab:
+                assert uniq[inv[i]] == x
+            else:
+                assert inv[i] == -1
+        assert bad == (1 if len(valid) < n else 0)
