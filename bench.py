@@ -598,7 +598,14 @@ def run_sweep(dev, peak):
         us = t_us(lambda: L.lhs_embed(*args), 10)
         nbytes = n_ids * (4 + w.hidden * 4) + distinct * w.row_bytes
         emit("gather", {"table": name, "ids": n_ids, "distinct": distinct, "hidden": w.hidden}, us, nbytes)
-        del out
+        # the same gather through the distinct ids (each distinct row decoded once)
+        dws = torch.empty(lhs.lib().lhs_embed_dedup_workspace(ctypes.byref(tab.c), n_ids), dtype=torch.uint8,
+                          device=dev)
+        da = (ctypes.byref(tab.c), ids.data_ptr(), n_ids, ctypes.c_float(float(w.embed_scale)), out.data_ptr(),
+              dws.data_ptr(), dws.numel(), err.data_ptr(), sp)
+        us = t_us(lambda: L.lhs_embed_dedup(*da), 10)
+        emit("gather_dedup", {"table": name, "ids": n_ids, "distinct": distinct, "hidden": w.hidden}, us, nbytes)
+        del out, dws
         # the gather written straight into f16 / i8 wire messages
         for fmt, fname in ((lhs.LHS_WIRE_F16, "f16"), (lhs.LHS_WIRE_I8, "i8")):
             nb = lhs.lhs_wire_bytes(fmt, n_ids, w.hidden)

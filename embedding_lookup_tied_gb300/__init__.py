@@ -23,7 +23,7 @@ LHS_ERRBIT_BAD_TOKEN = 1
 LHS_ERRBIT_MALFORMED = 2
 LHS_ERRBIT_NONFINITE = 4
 LHS_ERRBIT_TIMEOUT = 8
-LHS_F32, LHS_F16, LHS_BF16, LHS_Q8_0 = 0, 1, 2, 3
+LHS_F32, LHS_F16, LHS_BF16, LHS_Q8_0, LHS_FP8_E4M3 = 0, 1, 2, 3, 4
 LHS_WIRE_F32, LHS_WIRE_F16, LHS_WIRE_I8 = 0, 1, 2
 LHS_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -31,7 +31,9 @@ LIB_PATH = _build.LIB
 
 # Exported symbols of the C-ABI, in declaration order.
 ABI_SYMBOLS = (
-    "lhs_table_init", "lhs_table_info", "lhs_embed", "lhs_embed_wire", "lhs_logits_topk_workspace",
+    "lhs_table_init", "lhs_table_info", "lhs_embed", "lhs_embed_wire", "lhs_unique_ids_workspace",
+    "lhs_unique_ids", "lhs_embed_dedup_workspace", "lhs_embed_dedup", "lhs_embed_mixed",
+    "lhs_logits_topk_workspace",
     "lhs_logits_topk_launches", "lhs_logits_topk", "lhs_logits", "lhs_logits_topk_noalloc", "lhs_wire_bytes",
     "lhs_wire_encode",
     "lhs_wire_decode", "lhs_selftest_bounded_wait", "lhs_strerror",
@@ -75,6 +77,11 @@ def lib() -> ctypes.CDLL:
         "lhs_embed": (ctypes.c_int, [T, P, i64, ctypes.c_float, P, P, P]),
         "lhs_embed_wire": (ctypes.c_int, [T, P, i64, ctypes.c_float, i32, u32, u32, u32, P,
                                           ctypes.c_size_t, P, P]),
+        "lhs_unique_ids_workspace": (i64, [i64]),
+        "lhs_unique_ids": (ctypes.c_int, [i64, P, i64, P, P, P, P, sz, P, P]),
+        "lhs_embed_dedup_workspace": (i64, [T, i64]),
+        "lhs_embed_dedup": (ctypes.c_int, [T, P, i64, ctypes.c_float, P, P, sz, P, P]),
+        "lhs_embed_mixed": (ctypes.c_int, [P, i64, P, P, i64, i32, P, i64, ctypes.c_float, P, P, P]),
         "lhs_logits_topk_workspace": (ctypes.c_int, [T, i32, i32, i32, P]),
         "lhs_logits_topk_launches": (ctypes.c_int, [T, i32, i32, i32, P]),
         "lhs_logits_topk": (ctypes.c_int, [T, P, i32, i32, i32, ctypes.c_float, P, P, P,
@@ -199,6 +206,65 @@ def lhs_embed_wire(table: Table, ids: torch.Tensor, scale: float, fmt: int, laye
                                 float(scale), fmt, layer, flags, top_k, _dev(buf, "buf"),
                                 buf.numel(), _dev(err, "err"), _stream(stream)), "lhs_embed_wire")
     return buf, err
+
+
+def lhs_unique_ids(ids: torch.Tensor, vocab: int, ws=None, err=None, stream=None):
+    """Distinct ids in [0, vocab), ascending, and each position's index into
+    them (-1 for a bad id).  Returns (unique, inverse, count tensor, err word);
+    unique holds min(n, vocab) entries, the first `count` of them valid."""
+    n = ids.numel()
+    dev = ids.device
+    if ids.dtype != torch.int32:
+        raise ValueError("ids must be int32")
+    need = lib().lhs_unique_ids_workspace(vocab)
+    if need < 0:
+        raise ValueError("bad vocab")
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if ws is None else ws
+    unique = torch.empty(max(1, min(n, vocab)), dtype=torch.int32, device=dev)
+    inverse = torch.empty(max(1, n), dtype=torch.int32, device=dev)
+    count = torch.empty(1, dtype=torch.int32, device=dev)
+    err = _err_word(err, dev)
+    _check(lib().lhs_unique_ids(vocab, _dev(ids, "ids") if n else None, n, _dev(unique, "unique"),
+                                _dev(inverse, "inverse"), _dev(count, "count"), _dev(ws, "ws"),
+                                ws.numel(), _dev(err, "err"), _stream(stream)), "lhs_unique_ids")
+    return unique, inverse[:n], count, err
+
+
+def lhs_embed_dedup(table: Table, ids: torch.Tensor, scale: float, out=None, ws=None, err=None,
+                    stream=None):
+    """lhs_embed through the distinct ids (each distinct row decoded once).
+    Returns (out, err word)."""
+    n = ids.numel()
+    if ids.dtype != torch.int32:
+        raise ValueError("ids must be int32")
+    if out is None:
+        out = torch.empty((n, table.hidden), dtype=torch.float32, device=table.device)
+    err = _err_word(err, table.device)
+    if n == 0:
+        return out, err
+    need = lib().lhs_embed_dedup_workspace(ctypes.byref(table.c), n)
+    ws = torch.empty(need, dtype=torch.uint8, device=table.device) if ws is None else ws
+    _check(lib().lhs_embed_dedup(ctypes.byref(table.c), _dev(ids, "ids"), n, float(scale), _dev(out, "out"),
+                                 _dev(ws, "ws"), ws.numel(), _dev(err, "err"), _stream(stream)),
+           "lhs_embed_dedup")
+    return out, err
+
+
+def lhs_embed_mixed(data: torch.Tensor, row_offset: torch.Tensor, row_dtype: torch.Tensor, vocab: int,
+                    hidden: int, ids: torch.Tensor, scale: float, out=None, err=None, stream=None):
+    """Gather from a table whose rows carry their own element type (uint8
+    data, int64 row offsets, uint8 row types).  Returns (out, err word)."""
+    n = ids.numel()
+    dev = data.device
+    if out is None:
+        out = torch.empty((n, hidden), dtype=torch.float32, device=dev)
+    err = _err_word(err, dev)
+    _check(lib().lhs_embed_mixed(_dev(data, "data"), data.numel() * data.element_size(),
+                                 _dev(row_offset, "row_offset"), _dev(row_dtype, "row_dtype"), vocab, hidden,
+                                 _dev(ids, "ids") if n else None, n, float(scale),
+                                 _dev(out, "out") if n else None, _dev(err, "err"), _stream(stream)),
+           "lhs_embed_mixed")
+    return out, err
 
 
 def _resid_dtype(resid: torch.Tensor) -> int:

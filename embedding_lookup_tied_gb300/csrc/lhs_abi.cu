@@ -128,6 +128,56 @@ int lhs_embed_wire(const lhs_table *t, const int32_t *d_ids, int64_t n, float sc
                                          static_cast<cudaStream_t>(stream)));
 }
 
+int64_t lhs_unique_ids_workspace(int64_t vocab) {
+    if (vocab < 1 || vocab > INT32_MAX) return -1;
+    return static_cast<int64_t>(unique_ids_workspace(vocab));
+}
+
+int lhs_unique_ids(int64_t vocab, const int32_t *d_ids, int64_t n, int32_t *d_unique, int32_t *d_inverse,
+                   int32_t *d_count, void *d_ws, size_t ws_bytes, int32_t *d_err, void *stream) {
+    if (vocab < 1 || vocab > INT32_MAX || n < 0) return LHS_ERR_INVALID_ARG;
+    if (!d_count || !d_ws || !d_err || !aligned(d_count, 4) || !aligned(d_ws, 16) || !aligned(d_err, 4))
+        return LHS_ERR_INVALID_ARG;
+    if (n > 0 && (!d_ids || !d_unique || !d_inverse || !aligned(d_ids, 4) || !aligned(d_unique, 4) ||
+                  !aligned(d_inverse, 4)))
+        return LHS_ERR_INVALID_ARG;
+    if (ws_bytes < unique_ids_workspace(vocab)) return LHS_ERR_BUFFER_TOO_SMALL;
+    return cuda_status(launch_unique_ids(vocab, d_ids, n, d_unique, d_inverse, d_count, d_ws, d_err,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int64_t lhs_embed_dedup_workspace(const lhs_table *t, int64_t n) {
+    if (check_table(t) || n < 0) return -1;
+    return static_cast<int64_t>(embed_dedup_workspace(*t, n));
+}
+
+int lhs_embed_dedup(const lhs_table *t, const int32_t *d_ids, int64_t n, float scale, float *d_out, void *d_ws,
+                    size_t ws_bytes, int32_t *d_err, void *stream) {
+    int rc = check_table(t);
+    if (rc) return rc;
+    if (n < 0 || !std::isfinite(scale)) return LHS_ERR_INVALID_ARG;
+    if (n == 0) return LHS_OK;
+    if (!d_ids || !d_out || !d_ws || !d_err || !aligned(d_ids, 4) || !aligned(d_out, 16) || !aligned(d_ws, 16) ||
+        !aligned(d_err, 4))
+        return LHS_ERR_INVALID_ARG;
+    if (ws_bytes < embed_dedup_workspace(*t, n)) return LHS_ERR_BUFFER_TOO_SMALL;
+    return cuda_status(launch_embed_dedup(*t, d_ids, n, scale, d_out, d_ws, d_err, static_cast<cudaStream_t>(stream)));
+}
+
+int lhs_embed_mixed(const void *d_data, int64_t data_bytes, const int64_t *d_row_offset, const uint8_t *d_row_dtype,
+                    int64_t vocab, int32_t hidden, const int32_t *d_ids, int64_t n, float scale, float *d_out,
+                    int32_t *d_err, void *stream) {
+    if (!d_data || !aligned(d_data, 16) || data_bytes < 0 || !d_row_offset || !aligned(d_row_offset, 8) ||
+        !d_row_dtype)
+        return LHS_ERR_INVALID_ARG;
+    if (vocab < 1 || vocab > INT32_MAX || hidden < 1 || n < 0 || !std::isfinite(scale)) return LHS_ERR_INVALID_ARG;
+    if (n == 0) return LHS_OK;
+    if (!d_ids || !d_out || !d_err || !aligned(d_ids, 4) || !aligned(d_out, 16) || !aligned(d_err, 4))
+        return LHS_ERR_INVALID_ARG;
+    return cuda_status(launch_embed_mixed(d_data, data_bytes, d_row_offset, d_row_dtype, vocab, hidden, d_ids, n,
+                                          scale, d_out, d_err, static_cast<cudaStream_t>(stream)));
+}
+
 int lhs_logits_topk_workspace(const lhs_table *t, int32_t batch, int32_t k, int32_t resid_dtype,
                               size_t *bytes) {
     if (!bytes) return LHS_ERR_INVALID_ARG;

@@ -333,6 +333,15 @@ cudaError_t device_info(DeviceInfo *out);
 cudaError_t launch_embed(const lhs_table &t, const int32_t *ids, int64_t n, float scale,
                          float *out, int32_t *err, cudaStream_t stream);
 
+size_t unique_ids_workspace(int64_t vocab);
+cudaError_t launch_unique_ids(int64_t vocab, const int32_t *ids, int64_t n, int32_t *unique, int32_t *inverse,
+                              int32_t *count, void *ws, int32_t *err, cudaStream_t stream);
+size_t embed_dedup_workspace(const lhs_table &t, int64_t n);
+cudaError_t launch_embed_dedup(const lhs_table &t, const int32_t *ids, int64_t n, float scale, float *out,
+                               void *ws, int32_t *err, cudaStream_t stream);
+cudaError_t launch_embed_mixed(const void *data, int64_t data_bytes, const int64_t *row_offset,
+                               const uint8_t *row_dtype, int64_t vocab, int32_t hidden, const int32_t *ids,
+                               int64_t n, float scale, float *out, int32_t *err, cudaStream_t stream);
 cudaError_t launch_embed_wire(const lhs_table &t, const int32_t *ids, int64_t n, float scale, int fmt,
                               uint32_t layer, uint32_t flags, uint32_t top_k, void *buf, int32_t *err,
                               cudaStream_t stream);

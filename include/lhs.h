@@ -64,7 +64,9 @@ typedef enum {
     LHS_F32 = 0,   /* IEEE binary32, little-endian */
     LHS_F16 = 1,   /* IEEE binary16 ("f16 store", ADR-0008 memory footprint) */
     LHS_BF16 = 2,  /* bfloat16 */
-    LHS_Q8_0 = 3   /* blocks of 32: [f16 d (LE)][32 x int8 q], value d*q (Port Spec) */
+    LHS_Q8_0 = 3,  /* blocks of 32: [f16 d (LE)][32 x int8 q], value d*q (Port Spec) */
+    LHS_FP8_E4M3 = 4 /* OCP FP8 E4M3: a row type of mixed-precision tables only
+                        (lhs_embed_mixed); lhs_table_init rejects it */
 } lhs_dtype;
 
 typedef enum {
@@ -127,6 +129,49 @@ LHS_API int lhs_embed(const lhs_table *t, const int32_t *d_ids, int64_t n, float
 LHS_API int lhs_embed_wire(const lhs_table *t, const int32_t *d_ids, int64_t n, float scale,
                    int32_t fmt, uint32_t layer, uint32_t flags, uint32_t top_k, void *d_buf,
                    size_t buf_bytes, int32_t *d_err, void *stream);
+
+/* Dedup (HELIX Columnar Embedding, Appendix B: tokenize, dedupe, then fetch
+ * the distinct rows).  For ids d_ids[0..n) and a vocabulary of `vocab` rows:
+ *   d_unique  int32 [min(n, vocab)]: the distinct ids in [0, vocab), ascending;
+ *             entries past *d_count are left as they were
+ *   d_inverse int32 [n]: position of d_ids[i] in d_unique, or -1 for an id
+ *             outside [0, vocab) (and LHS_ERRBIT_BAD_TOKEN)
+ *   d_count   int32 [1]: number of distinct ids
+ * Scratch: lhs_unique_ids_workspace(vocab) bytes (a flag per vocabulary row
+ * and per-1024-row sums).  n >= 0.  Errors: LHS_ERR_INVALID_ARG,
+ * LHS_ERR_BUFFER_TOO_SMALL, LHS_ERR_CUDA.  No counterpart as a call on the
+ * pages: the distinct-id plan the pages describe, as a device step. */
+LHS_API int64_t lhs_unique_ids_workspace(int64_t vocab);
+LHS_API int lhs_unique_ids(int64_t vocab, const int32_t *d_ids, int64_t n, int32_t *d_unique,
+                   int32_t *d_inverse, int32_t *d_count, void *d_ws, size_t ws_bytes,
+                   int32_t *d_err, void *stream);
+
+/* lhs_embed through the distinct ids: every distinct row is read, decoded
+ * and scaled once (into scratch), then copied to each position that names
+ * it.  d_out [n x hidden] f32 equals lhs_embed's output bit for bit, and the
+ * error bits are the same.  Scratch: lhs_embed_dedup_workspace(t, n) bytes,
+ * 16-byte aligned.  Errors as lhs_embed, plus LHS_ERR_BUFFER_TOO_SMALL. */
+LHS_API int64_t lhs_embed_dedup_workspace(const lhs_table *t, int64_t n);
+LHS_API int lhs_embed_dedup(const lhs_table *t, const int32_t *d_ids, int64_t n, float scale,
+                    float *d_out, void *d_ws, size_t ws_bytes, int32_t *d_err, void *stream);
+
+/* Gather from a mixed-precision table (HELIX Columnar Embedding, §3: the
+ * optional sidecar for heterogeneous rows — mixed precision per row, e.g.
+ * fp16 for common tokens and fp8 for the long tail, or quantised rows with an
+ * inline dequantisation header).  Row r's bytes start at
+ * d_data + d_row_offset[r] and hold hidden elements of type d_row_dtype[r]:
+ * LHS_F32, LHS_F16, LHS_BF16, LHS_Q8_0 (hidden % 32 == 0) or LHS_FP8_E4M3.
+ *   d_out[t*hidden + j] = f32(element(row ids[t], j) * scale)
+ * An id outside [0, vocab) gives a zero row and LHS_ERRBIT_BAD_TOKEN; a row
+ * with an unknown type, an offset that is not a multiple of its element size
+ * (4 for f32, 2 for f16 / bf16 / Q8_0) or bytes outside [0, data_bytes) gives
+ * a zero row and LHS_ERRBIT_MALFORMED (nothing outside the data is read).
+ * d_data 16-byte aligned; d_out 16-byte aligned.  Errors: LHS_ERR_INVALID_ARG,
+ * LHS_ERR_CUDA. */
+LHS_API int lhs_embed_mixed(const void *d_data, int64_t data_bytes, const int64_t *d_row_offset,
+                    const uint8_t *d_row_dtype, int64_t vocab, int32_t hidden,
+                    const int32_t *d_ids, int64_t n, float scale, float *d_out,
+                    int32_t *d_err, void *stream);
 
 /* Workspace bytes lhs_logits_topk / lhs_logits need for this table, batch,
  * k (0 for the raw-logits call) and residual dtype.  Depends on the current

@@ -91,7 +91,7 @@ def _load():
             "orc_wire_decode": (ctypes.c_int, [ctypes.c_int, P, i64, i32, i32, P, P]),
             "orc_fp8_e4m3_value": (f64, [ctypes.c_uint8]),
             "orc_mixed_row_bytes": (i64, [ctypes.c_int, i32]),
-            "orc_embed_mixed": (None, [P, P, P, i64, i32, P, i64, f32, P, P]),
+            "orc_embed_mixed": (None, [P, i64, P, P, i64, i32, P, i64, f32, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -195,13 +195,9 @@ def embed_mixed(data: np.ndarray, row_offset, row_dtype, vocab: int, hidden: int
     ids = _c(ids, np.int32)
     if off.size < vocab or dts.size < vocab:
         raise ValueError("sidecar shorter than vocab")
-    for r in range(vocab):
-        rb = mixed_row_bytes(int(dts[r]), hidden)
-        if rb > 0 and off[r] + rb > db.size:
-            raise ValueError("row past the end of the data")
     out = np.empty((ids.size, hidden), np.float32)
     err = ctypes.c_int32(0)
-    _load().orc_embed_mixed(_ptr(db), _ptr(off), _ptr(dts), vocab, hidden, _ptr(ids), ids.size,
+    _load().orc_embed_mixed(_ptr(db), db.size, _ptr(off), _ptr(dts), vocab, hidden, _ptr(ids), ids.size,
                             ctypes.c_float(np.float32(scale)), _ptr(out), ctypes.byref(err))
     return out, int(err.value)
 

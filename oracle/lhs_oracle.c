@@ -271,9 +271,9 @@ int64_t orc_mixed_row_bytes(int dtype, int32_t hidden)
  * with its own type row_dtype[r] from data + row_offset[r].  A bad id gives a
  * zero row and BAD_TOKEN; a row whose type code is not a row type gives a
  * zero row and MALFORMED. */
-void orc_embed_mixed(const uint8_t *data, const int64_t *row_offset, const uint8_t *row_dtype,
-                     int64_t vocab, int32_t hidden, const int32_t *ids, int64_t n, float scale,
-                     float *out, int32_t *err_bits)
+void orc_embed_mixed(const uint8_t *data, int64_t data_bytes, const int64_t *row_offset,
+                     const uint8_t *row_dtype, int64_t vocab, int32_t hidden, const int32_t *ids,
+                     int64_t n, float scale, float *out, int32_t *err_bits)
 {
     int64_t t;
     int32_t j;
@@ -288,12 +288,17 @@ void orc_embed_mixed(const uint8_t *data, const int64_t *row_offset, const uint8
             continue;
         }
         dt = row_dtype[id];
-        row = data + row_offset[id];
-        if (dt < ORC_F32 || dt > ORC_FP8_E4M3 || orc_mixed_row_bytes(dt, hidden) < 0) {
+        /* Reading: a row whose type is unknown, whose offset is not a
+         * multiple of its element size (4 bytes f32, 2 bytes f16 / bf16 /
+         * Q8_0) or whose bytes fall outside the data is malformed. */
+        if (dt < ORC_F32 || dt > ORC_FP8_E4M3 || orc_mixed_row_bytes(dt, hidden) < 0 ||
+            row_offset[id] < 0 || row_offset[id] > data_bytes - orc_mixed_row_bytes(dt, hidden) ||
+            row_offset[id] % (dt == ORC_F32 ? 4 : (dt == ORC_FP8_E4M3 ? 1 : 2)) != 0) {
             for (j = 0; j < hidden; ++j) o[j] = 0.0f;
             *err_bits |= ORC_ERR_MALFORMED;
             continue;
         }
+        row = data + row_offset[id];
         for (j = 0; j < hidden; ++j) {
             float e = dt == ORC_FP8_E4M3 ? (float)orc_fp8_e4m3_value(row[j]) : orc_row_element(row, dt, j);
             o[j] = e * scale;                     /* one binary32 multiply */

@@ -584,3 +584,102 @@ def test_bounded_wait_gives_up_and_context_survives():
     out, e2 = lhs.lhs_embed(tab, to_dev(np.array([3, 4], np.int32)), 1.0)
     ref, _ = orc.embed(T, orc.F16, V, H, np.array([3, 4], np.int32), 1.0)
     assert int(e2.item()) == 0 and np.array_equal(out.cpu().numpy(), ref)
+
+
+# ---------------------------------------------------------------------------
+# dedup-then-gather and mixed-precision rows
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,vocab", [(0, 50), (1, 50), (300, 40), (5000, 262144), (70000, 3000)])
+def test_unique_ids_parity(n, vocab):
+    g = np.random.default_rng(n + vocab)
+    ids = wl.zipf_ids(n % 97, n, vocab) if n else np.zeros(0, np.int32)
+    if n > 10:
+        ids[g.integers(0, n, 5)] = np.array([-1, vocab, vocab + 7, -1000, 2 ** 31 - 1], np.int32)
+    uniq, inv, cnt, err = lhs.lhs_unique_ids(to_dev(ids) if n else torch.empty(0, dtype=torch.int32,
+                                                                               device="cuda"), vocab)
+    ru, ri, rbad = orc.unique_ids(ids, vocab)
+    c = int(cnt.item())
+    assert c == ru.size
+    assert np.array_equal(uniq.cpu().numpy()[:c], ru)
+    assert np.array_equal(inv.cpu().numpy(), ri)
+    assert int(err.item()) == rbad
+
+
+@pytest.mark.parametrize("dtype,H", [(orc.F32, 256), (orc.BF16, 896), (orc.Q8_0, 768), (orc.F16, 36)])
+def test_embed_dedup_equals_embed(dtype, H):
+    V = 5000
+    T = wl.make_table(dtype, V, H, 0.02, cid=800 + H, threads=4)
+    tab = upload_table(T, dtype, V, H)
+    ids = wl.zipf_ids(801, 3000, V)
+    ids[[5, 77]] = [-1, V]
+    ids_d = to_dev(ids)
+    out, err = lhs.lhs_embed_dedup(tab, ids_d, 27.712812)
+    ref, rerr = orc.embed(T, dtype, V, H, ids, 27.712812)
+    assert same_f32(out.cpu().numpy(), ref) and int(err.item()) == rerr
+    plain, _ = lhs.lhs_embed(tab, ids_d, 27.712812)
+    assert torch.equal(plain.view(torch.int32), out.view(torch.int32))
+
+
+def test_embed_dedup_full_size_gemma_q8():
+    w = wl.WORKLOADS["gemma_q8"]
+    T = wl.table_for(w)
+    tab = upload_table(T, w.dtype, w.vocab, w.hidden)
+    ids = wl.ids_for(w)
+    out, err = lhs.lhs_embed_dedup(tab, to_dev(ids), float(w.embed_scale))
+    ref, rerr = orc.embed(T, w.dtype, w.vocab, w.hidden, ids, float(w.embed_scale))
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert int(err.item()) == rerr
+
+
+def _random_mixed_table(vocab, hidden, seed):
+    """Rows of random values stored in random row types (every type present),
+    16-byte aligned; returns (data, offsets, types)."""
+    g = np.random.default_rng(seed)
+    types = g.integers(0, 5, vocab).astype(np.uint8)
+    types[:5] = np.arange(5)
+    if hidden % 32:
+        types[types == orc.Q8_0] = orc.F32           # Q8_0 rows need hidden % 32 == 0
+    chunks, offs, off = [], [], 0
+    for r in range(vocab):
+        dt = int(types[r])
+        x = (g.standard_normal(hidden) * 0.05).astype(np.float32)
+        if dt == orc.F32:
+            b = x.tobytes()
+        elif dt == orc.F16:
+            b = x.astype(np.float16).tobytes()
+        elif dt == orc.BF16:
+            b = wl.f32_to_bf16_bits(x).tobytes()
+        elif dt == orc.Q8_0:
+            q = g.integers(-127, 128, hidden).astype(np.int8).reshape(-1, 32)
+            d = np.abs(g.standard_normal(q.shape[0]) * 0.002).astype(np.float16)
+            b = b"".join(d[i:i + 1].tobytes() + q[i].tobytes() for i in range(q.shape[0]))
+        else:
+            c = g.integers(0, 256, hidden).astype(np.uint8)
+            c[(c & 0x7F) == 0x7F] = 0x3C                  # no NaN codes in the data
+            b = c.tobytes()
+        b += bytes((-len(b)) % 16)
+        offs.append(off)
+        chunks.append(b)
+        off += len(b)
+    return np.frombuffer(b"".join(chunks), np.uint8).copy(), np.array(offs, np.int64), types
+
+
+@pytest.mark.parametrize("H", [64, 72, 256])
+def test_embed_mixed_parity(H):
+    V = 600
+    data, offs, types = _random_mixed_table(V, H, seed=H)
+    ids = wl.zipf_ids(H, 400, V)
+    ids[[0, 1, 2, 3, 4]] = [0, 1, 2, 3, 4]
+    ids[[7, 9]] = [-5, V]
+    # malformed sidecar entries: unknown type, misaligned f32, past the end
+    bad_types = types.copy()
+    bad_offs = offs.copy()
+    bad_types[10] = 9
+    bad_types[11], bad_offs[11] = orc.F32, offs[11] + 2
+    bad_offs[12] = data.size
+    ids[[20, 21, 22]] = [10, 11, 12]
+    ref, rerr = orc.embed_mixed(data, bad_offs, bad_types, V, H, ids, 1.5)
+    out, err = lhs.lhs_embed_mixed(to_dev(data), to_dev(bad_offs), to_dev(bad_types), V, H, to_dev(ids), 1.5)
+    assert same_f32(out.cpu().numpy(), ref)
+    assert int(err.item()) == rerr == (orc.ERR_BAD_TOKEN | orc.ERR_MALFORMED)
