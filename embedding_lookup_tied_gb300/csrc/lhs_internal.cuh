@@ -93,6 +93,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// One contiguous bulk copy global -> shared, completing on `bar` (both
+// addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :
+                 : "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes),
+                   "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -354,8 +364,9 @@ cudaError_t launch_wire_decode(int fmt, const void *buf, int32_t seq_len, int32_
 // lm_head: plan (workspace layout + kernel choice) and launch
 struct LmHeadPlan {
     int path;          // 0 = tensor-core streaming GEMV (f16/bf16 table, batch <= 8 per pass)
-                       // 1 = CUDA-core streaming GEMV (any table dtype)
+                       // 1 = CUDA-core GEMV (any table dtype)
                        // 2 = tcgen05 GEMM (bf16 table, bf16 residuals, batch > 8)
+                       // 3 = bulk-stream CUDA-core GEMV (f32 / Q8_0, rows of 16..1024 bytes)
     int grid;          // CTAs of the projection kernel (= partial top-k lists)
     int batch_chunk;   // residuals per pass of the projection
     int kpad;          // hidden rounded up for the tensor-core operand

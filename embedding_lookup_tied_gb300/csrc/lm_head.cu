@@ -51,7 +51,8 @@ constexpr int kXStageBytes = 16 * BK * 2;    // 2 KB: 8 hi rows + 8 lo rows
 constexpr int kBoxRowsSmall = 16;            // TMA box for the ragged last block
 constexpr int kCandTotal = 4096;             // candidate keys per CTA (all residuals)
 constexpr int kBatchChunk = 8;               // residuals per projection pass
-constexpr int kBarAll = 5;                   // named barrier: all consumers
+constexpr int kBarAll = 15;                  // named barrier: all consumers (groups use 1..8)
+constexpr int kMaxConsumerWarps = 16;        // largest consumer group of the top-k state
 constexpr int kSimtThreads = 256;
 
 // ---------------------------------------------------------------------------
@@ -63,7 +64,7 @@ struct TopkShared {
     uint64_t tau[kBatchChunk];
     uint64_t tmin[kBatchChunk];
     unsigned hist[kBatchChunk][256];
-    float2 ms_warp[kConsumerWarps][kBatchChunk];
+    float2 ms_warp[kMaxConsumerWarps][kBatchChunk];
     int cnt[kBatchChunk];
     int nsel[kBatchChunk];
     int sel_digit[kBatchChunk];
@@ -166,10 +167,32 @@ __device__ void group_radix_select(const uint64_t *keys, int cnt, int kk, unsign
 
 // Cut keys[0..*cnt) down to its kk best (kk <= kMaxK), in place; *tau
 // becomes the kk-th best key.  Group-collective.
+// Short lists (n^2 / group size <= kDirectWork compares per thread) are cut
+// by ranking every key against all the others (keys are unique: its rank is
+// its place), one pass instead of the radix select's digit passes.
+constexpr int kDirectWork = 512;
+
 __device__ void group_compact(uint64_t *keys, int *cnt, uint64_t *tau, int kk, TopkShared &sm,
                               const Group &g) {
     const int n = *cnt;
     if (n <= kk) return;  // uniform across the group
+    if (n <= kMaxK * 2 + 128 && n * n <= g.T * kDirectWork) {
+        for (int i = g.gtid; i < n; i += g.T) {
+            const uint64_t key = keys[i];
+            int rank = 0;
+#pragma unroll 4
+            for (int q = 0; q < n; ++q) rank += keys[q] > key;
+            if (rank < kk) sm.scratch[g.col][rank] = key;
+        }
+        group_sync(g);
+        for (int i = g.gtid; i < kk; i += g.T) keys[i] = sm.scratch[g.col][i];
+        if (g.gtid == 0) {
+            *cnt = kk;
+            *tau = sm.scratch[g.col][kk - 1];
+        }
+        group_sync(g);
+        return;
+    }
     uint64_t prefix, mask;
     group_radix_select(keys, n, kk, sm.hist[g.col], &sm.sel_digit[g.col], &sm.sel_above[g.col], g,
                        prefix, mask);
@@ -295,6 +318,7 @@ __device__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, in
         const uint64_t *src = sm.cand + b * cap;
         const uint64_t key = src[j];
         int rank = 0;
+#pragma unroll 4
         for (int q = 0; q < n; ++q) rank += src[q] > key;
         if (rank < k)
             part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + rank] = key;
@@ -306,7 +330,7 @@ __device__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, in
     }
     if (tid < ncols) {
         float2 acc = make_float2(-INFINITY, 0.0f);
-        for (int w = 0; w < kConsumerWarps; ++w) acc = ms_combine(acc, sm.ms_warp[w][tid], invT);
+        for (int w = 0; w < nthreads / 32; ++w) acc = ms_combine(acc, sm.ms_warp[w][tid], invT);
         part_ms[static_cast<size_t>(blockIdx.x) * batch_total + b_off + tid] = acc;
     }
 }
@@ -1117,6 +1141,239 @@ __global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtPa
 }
 
 // ---------------------------------------------------------------------------
+// Bulk-stream CUDA-core GEMV (f32 and Q8_0 tables, rows a multiple of 16
+// bytes and at most kBulkRowBytesMax): a producer warp copies 32 whole rows
+// per stage — one contiguous cp.async.bulk — into a 4-stage ring (one top-k
+// round of 128 rows in flight); each of 16 consumer warps multiplies two
+// rows of each stage (w and w + 16) side by side, 8 elements per lane step,
+// with the residuals in shared memory.  The same per-CTA top-k lists as the
+// other GEMVs.
+// ---------------------------------------------------------------------------
+constexpr int kBulkRows = 32;                // rows per stage: 4 per consumer warp
+constexpr int kBulkStages = BM / kBulkRows;  // 4: one top-k round of 128 rows in flight
+constexpr int kBulkWarps = 16;               // consumer warps
+constexpr int kBulkConsumers = kBulkWarps * 32;
+constexpr int kBulkThreads = kBulkConsumers + 32;  // + the producer warp
+constexpr int kBulkRowsPerWarp = kBulkRows / kBulkWarps;
+constexpr int kBulkRowBytesMax = 1024;  // ring: 4 x 32 rows <= 128 KB
+
+// Elements 8g .. 8g+7 of a row held in shared memory.
+template <int DT>
+__device__ __forceinline__ void smem_row8(const uint8_t *row, int g, float (&v)[8]) {
+    if (DT == LHS_F32) {
+        const float4 a = *reinterpret_cast<const float4 *>(row + 32 * g);
+        const float4 b = *reinterpret_cast<const float4 *>(row + 32 * g + 16);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {  // Q8_0: block g / 4, codes (g % 4) * 8 .. +7
+        const unsigned short *b16 = reinterpret_cast<const unsigned short *>(row + (g >> 2) * 34);
+        const float d = f16_bits_to_f32(b16[0]);
+        const int q0 = 1 + (g & 3) * 4;
+        // int8 -> binary32 without a conversion instruction: with u = q + 128
+        // (the code's bits with the top bit flipped), the bits 0x4B000000 | u
+        // are the float 2^23 + u, so subtracting 2^23 + 128 leaves q exactly
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w = static_cast<uint32_t>(b16[q0 + i]) ^ 0x8080u;
+            const float f0 = __int_as_float(static_cast<int>(__byte_perm(w, 0x4B000000u, 0x7540))) - 8388736.0f;
+            const float f1 = __int_as_float(static_cast<int>(__byte_perm(w, 0x4B000000u, 0x7541))) - 8388736.0f;
+            v[2 * i] = __fmul_rn(d, f0);
+            v[2 * i + 1] = __fmul_rn(d, f1);
+        }
+    }
+}
+
+struct BulkParams {
+    const uint8_t *table;
+    int64_t V;
+    int K;
+    int64_t row_bytes;
+    const void *resid;
+    int resid_dtype;
+    int Bc, b_off, batch_total, k;
+    float invT;
+    float *raw;
+    uint64_t *part_keys;
+    float2 *part_ms;
+    int32_t *err;
+};
+
+// Shared memory: [ring kBulkStages x 16 rows][full, empty][TopkShared][xs Bc x K f32]
+__host__ __device__ __forceinline__ size_t bulk_ring_bytes(int64_t row_bytes) {
+    return static_cast<size_t>(kBulkStages) * kBulkRows * static_cast<size_t>(row_bytes);
+}
+__host__ __device__ __forceinline__ size_t bulk_tk_offset(int64_t row_bytes) {
+    return ((bulk_ring_bytes(row_bytes) + 2 * kBulkStages * 8) + 127) & ~size_t(127);
+}
+__host__ __device__ __forceinline__ size_t bulk_xs_offset(int64_t row_bytes) {
+    return (bulk_tk_offset(row_bytes) + sizeof(TopkShared) + 15) & ~size_t(15);
+}
+
+// BC: residual columns the loops are unrolled for (p.Bc <= BC).
+template <int DT, bool RAW, int BC>
+__global__ void __launch_bounds__(kBulkThreads, 1) gemv_bulk_kernel(const BulkParams p) {
+    extern __shared__ uint8_t dyn_smem[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~uintptr_t(127));
+    uint8_t *ring = base;
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + bulk_ring_bytes(p.row_bytes));
+    uint64_t *empty = full + kBulkStages;
+    TopkShared &tk = *reinterpret_cast<TopkShared *>(base + bulk_tk_offset(p.row_bytes));
+    float *xs = reinterpret_cast<float *>(base + bulk_xs_offset(p.row_bytes));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int q = 1;
+    while (q < p.Bc) q <<= 1;
+    const int cap = kCandTotal / q;
+    const size_t stage_bytes = static_cast<size_t>(kBulkRows) * p.row_bytes;
+
+    int64_t r0, r1;
+    cta_rows(p.V, gridDim.x, blockIdx.x, r0, r1);
+    const uint32_t total = static_cast<uint32_t>((r1 - r0 + kBulkRows - 1) / kBulkRows);
+
+    if (tid == 0) {
+        for (int s = 0; s < kBulkStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kBulkWarps);
+        }
+        fence_mbar_init();
+    }
+    if (tid < kBulkConsumers) topk_init(tk, tid, kBulkConsumers);
+    __syncthreads();
+    pdl_trigger();
+
+    if (warp == kBulkWarps) {
+        // ---------------- producer: the table only, never written by an earlier kernel
+        if (lane == 0) {
+            auto issue = [&](uint32_t j) {
+                const int s = j % kBulkStages;
+                const int64_t row0 = r0 + static_cast<int64_t>(j) * kBulkRows;
+                const int64_t nrows = (r1 - row0) < kBulkRows ? (r1 - row0) : kBulkRows;
+                const uint32_t bytes = static_cast<uint32_t>(nrows * p.row_bytes);
+                mbar_arrive_expect_tx(&full[s], bytes);
+                bulk_load(ring + s * stage_bytes, p.table + row0 * p.row_bytes, bytes, &full[s]);
+            };
+            const uint32_t pre = total < kBulkStages ? total : kBulkStages;
+            for (uint32_t j = 0; j < pre; ++j) issue(j);
+            uint32_t it = pre;
+            for (; it < total; ++it) {
+                const int s = it % kBulkStages;
+                if (!mbar_wait(&empty[s], ((it / kBulkStages) & 1) ^ 1, kWaitTimeoutNs)) {
+                    set_err(p.err, LHS_ERRBIT_TIMEOUT);
+                    break;
+                }
+                if (ld_volatile(&tk.abort_flag)) break;
+                issue(it);
+            }
+            // drain: every issued copy must land before the CTA exits
+            for (uint32_t j = (it > kBulkStages ? it - kBulkStages : 0); j < it; ++j)
+                if (!mbar_wait(&full[j % kBulkStages], (j / kBulkStages) & 1, kWaitTimeoutNs)) {
+                    set_err(p.err, LHS_ERRBIT_TIMEOUT);
+                    break;
+                }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    pdl_wait();  // residuals may come from the previous kernel; partial lists may still be read by it
+    for (int64_t i = tid; i < static_cast<int64_t>(p.Bc) * p.K; i += kBulkConsumers) {
+        float v;
+        if (p.resid_dtype == LHS_F32) v = __ldg(static_cast<const float *>(p.resid) + i);
+        else v = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(p.resid) + i)) << 16);
+        xs[i] = v;
+    }
+    named_bar_sync(kBarAll, kBulkConsumers);
+    float m_st = -INFINITY, s_st = 0.0f;  // lane b < Bc: column b
+    const int ng = p.K >> 3;
+    for (uint32_t it = 0; it < total; ++it) {
+        const int s = it % kBulkStages;
+        const int64_t row0 = r0 + static_cast<int64_t>(it) * kBulkRows;
+        const int nrows = static_cast<int>((r1 - row0) < kBulkRows ? (r1 - row0) : kBulkRows);
+        if (!ld_volatile(&tk.abort_flag)) {
+            if (!mbar_wait(&full[s], (it / kBulkStages) & 1, kWaitTimeoutNs)) {
+                if (lane == 0) {
+                    set_err(p.err, LHS_ERRBIT_TIMEOUT);
+                    tk.abort_flag = 1;
+                }
+            } else {
+                // rows warp + 16h of the stage, side by side; two accumulation
+                // chains per row and column (even / odd elements)
+                constexpr int RW = kBulkRowsPerWarp;
+                int nr = 0;  // warp-uniform
+#pragma unroll
+                for (int h = 0; h < RW; ++h) nr += warp + kBulkWarps * h < nrows;
+                if (nr > 0) {
+                    const uint8_t *rows[RW];
+#pragma unroll
+                    for (int h = 0; h < RW; ++h)
+                        rows[h] = ring + s * stage_bytes + (h < nr ? warp + kBulkWarps * h : warp) * p.row_bytes;
+                    float c0[RW][BC], c1[RW][BC];
+#pragma unroll
+                    for (int h = 0; h < RW; ++h)
+#pragma unroll
+                        for (int b = 0; b < BC; ++b) c0[h][b] = c1[h][b] = 0.0f;
+                    for (int g = lane; g < ng; g += 32) {
+                        float e[RW][8];
+#pragma unroll
+                        for (int h = 0; h < RW; ++h) smem_row8<DT>(rows[h], g, e[h]);
+#pragma unroll
+                        for (int b = 0; b < BC; ++b) {
+                            if (BC == 1 || b < p.Bc) {
+                                const float4 x0 = *reinterpret_cast<const float4 *>(xs + b * p.K + 8 * g);
+                                const float4 x1 = *reinterpret_cast<const float4 *>(xs + b * p.K + 8 * g + 4);
+                                const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                                for (int i = 0; i < 8; i += 2)
+#pragma unroll
+                                    for (int h = 0; h < RW; ++h) {
+                                        c0[h][b] = fmaf(e[h][i], xv[i], c0[h][b]);
+                                        c1[h][b] = fmaf(e[h][i + 1], xv[i + 1], c1[h][b]);
+                                    }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < RW; ++h) {
+                        if (h < nr) {
+                            float acc[BC];
+#pragma unroll
+                            for (int b = 0; b < BC; ++b) acc[b] = c0[h][b] + c1[h][b];
+#pragma unroll
+                            for (int b = 0; b < BC; ++b)
+#pragma unroll
+                                for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xFFFFFFFFu, acc[b], o);
+                            float mine = 0.0f;
+#pragma unroll
+                            for (int b = 0; b < BC; ++b)
+                                if (lane == b) mine = acc[b];
+                            const int64_t v = row0 + warp + kBulkWarps * h;
+                            if (lane < p.Bc) {
+                                if (RAW) {
+                                    p.raw[static_cast<int64_t>(p.b_off + lane) * p.V + v] = mine;
+                                } else {
+                                    ms_update(m_st, s_st, mine, p.invT);
+                                    topk_offer(tk, lane, cap, mine, static_cast<int32_t>(v));
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if ((it % kBulkStages) == kBulkStages - 1 || it + 1 == total) {
+            if (!RAW) topk_round_end(tk, tid, kBulkConsumers, p.Bc, p.k, cap, BM);
+            else named_bar_sync(kBarAll, kBulkConsumers);
+            // the flag only changes inside the loop, before the barrier above
+            if (ld_volatile(&tk.abort_flag)) break;
+        }
+    }
+    if (RAW || ld_volatile(&tk.abort_flag)) return;
+    if (lane < kBatchChunk) tk.ms_warp[warp][lane] = make_float2(m_st, s_st);
+    topk_finish(tk, tid, kBulkConsumers, p.Bc, p.k, cap, p.b_off, p.batch_total, p.part_keys, p.part_ms, p.invT);
+}
+
+// ---------------------------------------------------------------------------
 // merge: global top-k per residual from G partial lists, sorted, + probs
 // ---------------------------------------------------------------------------
 
@@ -1198,6 +1455,9 @@ constexpr size_t kSimtXBytesMax = 96 * 1024;
 size_t simt_smem_bytes(int Bc, int K) {
     return ((sizeof(TopkShared) + 15) & ~size_t(15)) + static_cast<size_t>(Bc) * K * 4;
 }
+size_t bulk_smem_bytes(int64_t row_bytes, int Bc, int K) {
+    return 128 + bulk_xs_offset(row_bytes) + static_cast<size_t>(Bc) * K * 4;
+}
 size_t merge_smem_bytes(int G, int k) {
     return ((sizeof(MergeSmemHead) + 15) & ~size_t(15)) + static_cast<size_t>(G) * k * 8;
 }
@@ -1227,7 +1487,11 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
         const int64_t tiles = (t.vocab + 255) / 256;
         if ((tiles + clusters - 1) / clusters * 256 > 65535) gemm = false;
     }
-    p.path = gemm ? 2 : (tc ? 0 : 1);
+    // f32 / Q8_0 tables with short 16-byte-multiple rows: bulk-stream GEMV
+    const bool bulk = !tc && (t.dtype == LHS_F32 || t.dtype == LHS_Q8_0) && t.hidden % 8 == 0 &&
+                      t.row_bytes % 16 == 0 && t.row_bytes <= kBulkRowBytesMax &&
+                      bulk_smem_bytes(t.row_bytes, kBatchChunk, t.hidden) <= static_cast<size_t>(dev.max_smem_optin);
+    p.path = gemm ? 2 : (tc ? 0 : (bulk ? 3 : 1));
     if (gemm) {
         p.grid = clusters;  // partial lists: one per cluster
         p.batch_chunk = batch;
@@ -1236,6 +1500,8 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
     }
     if (gemm) {
         // nothing else to size: the GEMM reads the residuals in place
+    } else if (p.path == 3) {
+        p.batch_chunk = kBatchChunk;
     } else if (tc) {
         p.batch_chunk = kBatchChunk;
         p.xres = tc_smem_bytes(true, p.kpad) <= static_cast<size_t>(dev.max_smem_optin);
@@ -1365,6 +1631,52 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             p.resid_f32 = resid_dtype == LHS_F32;
             p.err = err;
             e = launch_pdl(kern, dim3(plan.grid), dim3(kTcThreads), smem, stream, tm_a, tm_a16, tm_x, p);
+            if (e != cudaSuccess) return e;
+        }
+    } else if (plan.path == 3) {
+        using BulkKernel = void (*)(const BulkParams);
+#define LHS_BULK(DT, R) {gemv_bulk_kernel<DT, R, 1>, gemv_bulk_kernel<DT, R, 2>, gemv_bulk_kernel<DT, R, 4>, \
+                         gemv_bulk_kernel<DT, R, 8>}
+        static const BulkKernel kTable[2][2][4] = {{LHS_BULK(LHS_Q8_0, false), LHS_BULK(LHS_Q8_0, true)},
+                                                   {LHS_BULK(LHS_F32, false), LHS_BULK(LHS_F32, true)}};
+#undef LHS_BULK
+        {
+            static std::mutex mu;
+            static bool done[16][64] = {};
+            std::lock_guard<std::mutex> lock(mu);
+            for (int d = 0; d < 2; ++d)
+                for (int r = 0; r < 2; ++r)
+                    for (int c = 0; c < 4; ++c) {
+                        const int which = d * 8 + r * 4 + c;
+                        if (!done[which][dev.device]) {
+                            e = cudaFuncSetAttribute(kTable[d][r][c], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     dev.max_smem_optin);
+                            if (e != cudaSuccess) return e;
+                            done[which][dev.device] = true;
+                        }
+                    }
+        }
+        for (int c0 = 0; c0 < batch; c0 += plan.batch_chunk) {
+            const int Bc = batch - c0 < plan.batch_chunk ? batch - c0 : plan.batch_chunk;
+            const BulkKernel kern = kTable[t.dtype == LHS_F32][raw][Bc <= 1 ? 0 : (Bc <= 2 ? 1 : (Bc <= 4 ? 2 : 3))];
+            BulkParams p;
+            p.table = static_cast<const uint8_t *>(t.data);
+            p.V = t.vocab;
+            p.K = t.hidden;
+            p.row_bytes = t.row_bytes;
+            p.resid = static_cast<const uint8_t *>(resid) + static_cast<size_t>(c0) * t.hidden * relt;
+            p.resid_dtype = resid_dtype;
+            p.Bc = Bc;
+            p.b_off = c0;
+            p.batch_total = batch;
+            p.k = k;
+            p.invT = invT;
+            p.raw = raw_logits;
+            p.part_keys = part_keys;
+            p.part_ms = part_ms;
+            p.err = err;
+            e = launch_pdl(kern, dim3(plan.grid), dim3(kBulkThreads), bulk_smem_bytes(t.row_bytes, Bc, t.hidden),
+                           stream, p);
             if (e != cudaSuccess) return e;
         }
     } else {

@@ -268,8 +268,12 @@ LM_CASES = [
     (orc.F16, 3000, 2048, 3, 10, orc.F32),    # operand too large to keep resident: prep + TMA tiles
     (orc.BF16, 2000, 1504, 2, 7, orc.BF16),   # largest resident operand, hidden % 64 != 0
     (orc.BF16, 128, 64, 2, 1, orc.F32),       # one block, k = 1
-    (orc.F32, 1000, 256, 4, 5, orc.F32),      # CUDA-core path
-    (orc.Q8_0, 700, 128, 2, 10, orc.F32),     # CUDA-core path
+    (orc.F32, 1000, 256, 4, 5, orc.F32),      # bulk-stream CUDA-core path (1 KB rows)
+    (orc.Q8_0, 700, 128, 2, 10, orc.F32),     # CUDA-core path (136-byte rows)
+    (orc.Q8_0, 5000, 768, 3, 10, orc.F32),    # bulk-stream path, 816-byte rows, ragged last stage
+    (orc.Q8_0, 2100, 256, 11, 7, orc.BF16),   # bulk-stream path, two passes, bf16 residuals
+    (orc.F32, 3001, 64, 8, 64, orc.F32),      # bulk-stream path, 256-byte rows, ragged vocab
+    (orc.F32, 900, 36, 2, 5, orc.F32),        # hidden % 8 != 0: CUDA-core path
     (orc.F16, 1000, 72, 2, 6, orc.F32),       # hidden % 64 != 0, tensor-core path
     (orc.F16, 1000, 68, 2, 6, orc.F32),       # hidden % 8 != 0 -> CUDA-core path
     (orc.BF16, 100, 64, 3, 100, orc.F32),     # vocab < 128 -> CUDA-core path, k = V
