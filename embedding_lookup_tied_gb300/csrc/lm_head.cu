@@ -447,6 +447,7 @@ constexpr int kMergeCand = 1024;
 struct MergeWork {
     uint64_t cand[kMergeCand];
     uint32_t set[kMergeSet];
+    float ssum[kMergeThreads / 32];
     uint32_t bound;
     int total;
     float2 msf;
@@ -552,15 +553,15 @@ __device__ void stage_sorted_lists(const uint64_t *part_keys, const float2 *part
 // Steps 2-4 for residual b, by 256 threads synchronised on named barrier
 // `bar_id`.  lists: [G][R] staged entries (R >= ceil(k/G)), sms: [G].  The
 // phases are short dependent chains, so independent work runs side by side:
-// the last warp folds the G (max, sum) pairs while the others rank the
-// sampled keys, and candidates are appended with one shared atomic per warp
-// instead of a block-wide scan.
+// warp 0 takes the max of the G list maxima while all warps rank the sampled
+// keys, the G softmax sums are rescaled to that max in parallel, and
+// candidates are appended with one shared atomic per warp instead of a
+// block-wide scan.
 __device__ void merge_column_sorted(const uint64_t *lists, int R, const float2 *sms, int G, int k,
                                     float invT, const uint64_t *part_keys, int batch_total, int b,
                                     int32_t *out_ids, float *out_logits, float *out_probs, MergeWork &w,
                                     int tid, int bar_id) {
     const int lane = tid & 31, warp = tid >> 5;
-    constexpr int kMsWarp = kMergeThreads / 32 - 1;
     const int m = (k + G - 1) / G;
     const int na = G * m;
     const int na4 = (na + 3) & ~3;
@@ -573,26 +574,21 @@ __device__ void merge_column_sorted(const uint64_t *lists, int R, const float2 *
         w.set[i] = i < na ? static_cast<uint32_t>(lists[gi * R + (i - gi * m)] >> 32) : 0u;
     }
     named_bar_sync(bar_id, kMergeThreads);
-    if (warp == kMsWarp) {
-        // (max, sum) over the lists
-        float2 acc = make_float2(-INFINITY, 0.0f);
-        for (int gi = lane; gi < G; gi += 32) acc = ms_combine(acc, sms[gi], invT);
+    // (max, sum) over the lists, max first: the G rescalings are then
+    // independent (one exp each, in parallel) instead of a chain of combines
+    if (tid < 32) {
+        float mx = -INFINITY;
+        for (int gi = lane; gi < G; gi += 32) mx = fmaxf(mx, sms[gi].x);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float2 other;
-            other.x = __shfl_xor_sync(0xFFFFFFFFu, acc.x, o);
-            other.y = __shfl_xor_sync(0xFFFFFFFFu, acc.y, o);
-            acc = ms_combine(acc, other, invT);
-        }
-        if (lane == 0) w.msf = acc;
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if (lane == 0) w.msf.x = mx;
     }
     // 2. the bound: the k-th largest sampled order key (ties allowed); the
     //    ms warp joins only when the sample needs every thread
     const uint4 *set4 = reinterpret_cast<const uint4 *>(w.set);
     const int nw4 = na4 / 4;
-    const int nrank = na < kMsWarp * 32 ? kMsWarp * 32 : kMergeThreads;
-    if (warp != kMsWarp || nrank == kMergeThreads) {
-        for (int i = tid; i < na; i += nrank) {
+    {
+        for (int i = tid; i < na; i += kMergeThreads) {
             const uint32_t x = w.set[i];
             int gt = 0, ge = 0;
 #pragma unroll 4
@@ -605,6 +601,18 @@ __device__ void merge_column_sorted(const uint64_t *lists, int R, const float2 *
         }
     }
     named_bar_sync(bar_id, kMergeThreads);
+    {
+        // sum of s_i * exp((m_i - M) / T), one term per thread, block-reduced
+        const float M = w.msf.x;
+        float t = 0.0f;
+        if (tid < G) {
+            const float2 v = sms[tid];
+            t = v.x == M ? v.y : v.y * expf((v.x - M) * invT);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+        if (lane == 0) w.ssum[warp] = t;
+    }
     const uint64_t L = static_cast<uint64_t>(w.bound) << 32;
     // 3. each list's prefix >= L (lists that may go on are read on from L2),
     //    appended at a position taken with one shared atomic per warp
@@ -643,7 +651,10 @@ __device__ void merge_column_sorted(const uint64_t *lists, int R, const float2 *
     named_bar_sync(bar_id, kMergeThreads);
     const int total = w.total;
     const bool slow = L == 0ull || total > kMergeCand;  // uniform
-    const float2 ms = w.msf;
+    float ssum = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kMergeThreads / 32; ++q) ssum += w.ssum[q];
+    const float2 ms = make_float2(w.msf.x, ssum);
     if (slow) {
         if (warp == 0)
             merge_extract_warp(part_keys, G, batch_total, b, k, invT, ms, out_ids, out_logits, out_probs,
