@@ -596,6 +596,9 @@ cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_t, const 
 
 size_t gemm_lm_head_smem() { return kGemmSmemBytes; }
 
+// Residuals one launch covers: a cluster's two CTAs hold 128 each.
+int gemm_lm_head_max_batch() { return 2 * GM; }
+
 // Candidate buffer entries per (cluster, residual) in the main pass: room
 // for k plus at least one full chunk of 32 after a cut.
 int gemm_lm_head_cap(int k) { return k + 32 <= 128 ? 128 : 256; }

@@ -415,6 +415,7 @@ struct GemmBuffers {
     int cap;
 };
 size_t gemm_lm_head_smem();
+int gemm_lm_head_max_batch();
 int gemm_lm_head_cap(int k);
 int gemm_lm_head_sample_len();
 int gemm_lm_head_clusters(const DeviceInfo &dev);

@@ -1505,7 +1505,9 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
     p.path = gemm ? 2 : (tc ? 0 : (bulk ? 3 : 1));
     if (gemm) {
         p.grid = clusters;  // partial lists: one per cluster
-        p.batch_chunk = batch;
+        // a cluster covers 2 x 128 residuals (one TMEM lane each): larger
+        // batches run as successive passes of that many
+        p.batch_chunk = batch < gemm_lm_head_max_batch() ? batch : gemm_lm_head_max_batch();
     } else {
         p.grid = static_cast<int>(units < dev.num_sms ? units : dev.num_sms);
     }
@@ -1532,23 +1534,24 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
     p.off_x = off;
     off += (tc && !gemm) ? align_up(static_cast<size_t>(16) * p.kpad * 2, 1024) : 0;
     p.key_stride = gemm ? gemm_lm_head_cap(kk) : kk;
+    const int wb = gemm ? p.batch_chunk : batch;  // residuals whose lists the workspace holds at once
     p.off_keys = off;
-    off += align_up(static_cast<size_t>(p.grid) * batch * p.key_stride * 8, 256);
+    off += align_up(static_cast<size_t>(p.grid) * wb * p.key_stride * 8, 256);
     p.off_ms = off;
-    off += align_up(static_cast<size_t>(p.grid) * batch * 8, 256);
+    off += align_up(static_cast<size_t>(p.grid) * wb * 8, 256);
     // GEMM sample pass: one tile per cluster, worth it when each cluster
     // owns at least two tiles
     p.sample = gemm && k > 0 && (t.vocab + 255) / 256 >= 2 * static_cast<int64_t>(p.grid);
     p.off_sample_keys = p.off_sample_ms = p.off_sample_ids = p.off_sample_logits = off;
     if (p.sample) {
         p.off_sample_keys = off;
-        off += align_up(static_cast<size_t>(p.grid) * batch * gemm_lm_head_sample_len() * 8, 256);
+        off += align_up(static_cast<size_t>(p.grid) * wb * gemm_lm_head_sample_len() * 8, 256);
         p.off_sample_ms = off;
-        off += align_up(static_cast<size_t>(p.grid) * batch * 8, 256);
+        off += align_up(static_cast<size_t>(p.grid) * wb * 8, 256);
         p.off_sample_ids = off;
-        off += align_up(static_cast<size_t>(batch) * k * 4, 256);
+        off += align_up(static_cast<size_t>(wb) * k * 4, 256);
         p.off_sample_logits = off;
-        off += align_up(static_cast<size_t>(batch) * k * 4, 256);
+        off += align_up(static_cast<size_t>(wb) * k * 4, 256);
     }
     p.bytes = off;
     *plan = p;
@@ -1556,8 +1559,8 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
 }
 
 int lm_head_launches(const LmHeadPlan &plan, int32_t batch, bool raw) {
-    if (plan.path == 2) return raw ? 1 : (plan.sample ? 4 : 2);
     const int chunks = (batch + plan.batch_chunk - 1) / plan.batch_chunk;
+    if (plan.path == 2) return chunks * (raw ? 1 : (plan.sample ? 4 : 2));
     const int per_chunk = (plan.path == 0 && !plan.xres) ? 2 : 1;  // (prep +) projection
     return chunks * per_chunk + (raw ? 0 : 1);
 }
@@ -1585,8 +1588,20 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
         gb.cand = part_keys;
         gb.ms = part_ms;
         gb.cap = plan.key_stride;
-        e = launch_gemm_lm_head(t, resid, batch, k, invT, raw_logits, gb, err, plan.grid, dev, stream);
-        if (e != cudaSuccess) return e;
+        for (int c0 = 0; c0 < batch; c0 += plan.batch_chunk) {
+            const int Bc = batch - c0 < plan.batch_chunk ? batch - c0 : plan.batch_chunk;
+            const void *rc = static_cast<const uint8_t *>(resid) + static_cast<size_t>(c0) * t.hidden * relt;
+            float *rawc = raw ? raw_logits + static_cast<size_t>(c0) * t.vocab : nullptr;
+            e = launch_gemm_lm_head(t, rc, Bc, k, invT, rawc, gb, err, plan.grid, dev, stream);
+            if (e != cudaSuccess) return e;
+            if (!raw) {
+                const size_t o = static_cast<size_t>(c0) * k;
+                e = launch_merge(part_keys, part_ms, plan.grid, plan.key_stride, k, Bc, k, invT, ids + o,
+                                 logits_out + o, probs ? probs + o : nullptr, dev, stream);
+                if (e != cudaSuccess) return e;
+            }
+        }
+        return cudaSuccess;
     } else if (plan.path == 0) {
         const bool bf16 = t.dtype == LHS_BF16;
         uint16_t *xs = reinterpret_cast<uint16_t *>(wsb + plan.off_x);

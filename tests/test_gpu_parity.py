@@ -396,6 +396,8 @@ GEMM_CASES = [
     (3000, 256, 130, 5),      # one residual in the second half
     (40000, 128, 150, 20),    # >= 2 tiles per cluster: sample pass + main pass
     (39000, 64, 256, 128),    # sample pass with k = 128 (256-entry buffers)
+    (5000, 64, 300, 10),      # beyond one cluster's 256 residuals: two passes
+    (40000, 64, 513, 50),     # three passes, each with its sample pass
 ]
 
 
