@@ -26,7 +26,10 @@
 //    exact top-k of all clusters' group maxima.  The k-th of those is a
 //    lower bound of the final k-th logit (the k-th largest of any subset of
 //    the logits never exceeds the k-th largest of all of them), and close
-//    to it: the sample's best logits almost never share a group.
+//    to it: the sample's best logits almost never share a group.  The
+//    sample tile is the first of each cluster's range, and its logits are
+//    kept in global memory (256 KB per cluster), so the main pass reads
+//    them instead of recomputing that tile.
 //  * main pass: every logit below that bound is dropped at once; the few
 //    others go to a per-(cluster, residual) candidate buffer in global
 //    memory, cut back to k by a warp-cooperative bitonic sort if it would
@@ -74,6 +77,8 @@ struct GemmParams {
     float2 *ms;                  // [clusters][B]
     const float *sample_logits;  // main: [B][k] top-k logits of the sample, or null
     int cap;                     // main: candidate buffer entries per (cluster, residual)
+    float *tile_logits;          // sample: writes, main: reads the logits of each cluster's first
+                                 // tile [clusters][2][GM][GN] (null: main computes that tile)
     int32_t *err;
 };
 
@@ -294,15 +299,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t rank = cluster_ctarank();          // residual half
     const int cl = blockIdx.x >> 1;                   // cluster index
     int t0, t1;
-    if (MODE == kModeSample) {  // one tile per cluster, spread over the vocab
+    if (MODE == kModeSample) {  // the first tile of each cluster's range
         t0 = static_cast<int>((static_cast<int64_t>(p.tiles) * cl) / p.clusters);
         t1 = t0 + 1;
     } else {
         t0 = static_cast<int>((static_cast<int64_t>(p.tiles) * cl) / p.clusters);
         t1 = static_cast<int>((static_cast<int64_t>(p.tiles) * (cl + 1)) / p.clusters);
     }
+    // main pass after a sample pass: the first tile's logits are already in
+    // global memory, so the tensor cores start at the second
+    const bool reuse = MODE == kModeMain && p.tile_logits != nullptr && t1 > t0;
+    const int tS = reuse ? t0 + 1 : t0;
     const int nk = (p.K + GK - 1) / GK;
-    const uint32_t total = static_cast<uint32_t>(t1 - t0) * nk;
+    const uint32_t total = static_cast<uint32_t>(t1 - tS) * nk;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -335,7 +344,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint16_t both = 0x3;
             auto issue_t = [&](uint32_t j) {
                 const int s = j % S;
-                const int tile = t0 + static_cast<int>(j / nk), kc = static_cast<int>(j % nk);
+                const int tile = tS + static_cast<int>(j / nk), kc = static_cast<int>(j % nk);
                 tma_load_2d_mc(sm.b[s] + rank * kBHalfBytes, &tm_t, &sm.full[s], kc * GK,
                                tile * GN + static_cast<int>(rank) * (GN / 2), both);
             };
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;
             const uint16_t both = 0x3;
-            for (int tile = t0, ti = 0; tile < t1; ++tile, ++ti) {
+            for (int tile = tS, ti = 0; tile < t1; ++tile, ++ti) {
                 const int buf = ti & 1;
                 if (!wait_or_abort(&sm.tmem_empty[buf], ((ti >> 1) & 1) ^ 1, &sm.abort_flag, p.err)) break;
                 tc_fence_after();
@@ -437,6 +446,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 uint64_t best[kSampleLen];
 #pragma unroll
                 for (int j = 0; j < kSampleLen; ++j) best[j] = 0ull;
+                float *keep = p.tile_logits ? p.tile_logits + ((static_cast<size_t>(cl) * 2 + rank) * GM + row) * GN
+                                            : nullptr;
                 for (int c = 0; c < kAccCols / 32; ++c) {
                     float vals[32];
                     tmem_ld32(tmem + lane_base + c * 32, vals);
@@ -445,6 +456,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int j = 0; j < 32; ++j) {
                         const uint64_t key = topk_key(vals[j], static_cast<int32_t>(vc + j));
                         if (vc + j < p.V && key > best[j]) best[j] = key;
+                    }
+                    if (keep) {
+                        float4 *d4 = reinterpret_cast<float4 *>(keep + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            d4[j] = make_float4(vals[4 * j], vals[4 * j + 1], vals[4 * j + 2], vals[4 * j + 3]);
                     }
                 }
                 if (valid) {
@@ -466,7 +483,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint64_t *cand = p.keys + (static_cast<size_t>(cl) * p.B + (valid ? b : 0)) * p.cap;
             uint64_t *cand_lane0 =
                 p.keys + (static_cast<size_t>(cl) * p.B + static_cast<int>(rank) * GM + q * 32) * p.cap;
-            for (int tile = t0, ti = 0; tile < t1; ++tile, ++ti) {
+            // one 32-column chunk of this residual's logits: running softmax,
+            // then the candidates (warp-collective: every lane calls it)
+            auto chunk = [&](const float (&vals)[32], int64_t vc) {
+                const int nvalid = valid ? static_cast<int>(p.V - vc < 32 ? (p.V - vc) : 32) : 0;
+                const uint32_t vmask = nvalid >= 32 ? 0xFFFFFFFFu
+                                                    : (nvalid > 0 ? ((1u << nvalid) - 1u) : 0u);
+                if (nvalid > 0) {
+                    float cmax = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if ((vmask >> j) & 1u) cmax = fmaxf(cmax, vals[j]);
+                    const float mn = fmaxf(m_run, cmax);
+                    if (mn != -INFINITY) {
+                        // exp((v - mn) / T) = 2^((v - mn) * log2(e) / T)
+                        float acc = s_run * ex2_approx((m_run - mn) * l2e_invT);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if ((vmask >> j) & 1u) acc += ex2_approx((vals[j] - mn) * l2e_invT);
+                        s_run = acc;
+                        m_run = mn;
+                    }
+                }
+                // candidates: not below the bound's value (NaN passes),
+                // then the exact (value, id) order for those only
+                uint32_t mask = 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (!(vals[j] < tau_val)) mask |= 1u << j;
+                mask &= vmask;
+                if (mask) mask = exact_mask(vals, mask, vc, tau);
+                // cut every buffer of the warp this chunk could overflow
+                unsigned need = __ballot_sync(0xFFFFFFFFu, cnt + __popc(mask) > p.cap);
+                while (need) {
+                    const int L = __ffs(need) - 1;
+                    need &= need - 1;
+                    const int nL = __shfl_sync(0xFFFFFFFFu, cnt, L);
+                    uint64_t *bufL = cand_lane0 + static_cast<size_t>(L) * p.cap;
+                    const uint64_t kth = p.cap <= 128 ? warp_cut<128>(bufL, nL, p.k, lane)
+                                                      : warp_cut<256>(bufL, nL, p.k, lane);
+                    if (lane == L) {
+                        cnt = nL < p.k ? nL : p.k;
+                        if (kth) {
+                            tau = kth;
+                            tau_val = fmaxf(tau_val, key_value(kth));
+                        }
+                        if (mask) mask = exact_mask(vals, mask, vc, tau);
+                    }
+                }
+                if (mask) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if ((mask >> j) & 1u) cand[cnt++] = topk_key(vals[j], static_cast<int32_t>(vc + j));
+                }
+            };
+            if (reuse) {
+                // the first tile, from the logits the sample pass kept
+                const float *src = p.tile_logits + ((static_cast<size_t>(cl) * 2 + rank) * GM + row) * GN;
+                const int64_t v0 = static_cast<int64_t>(t0) * GN;
+                for (int c = 0; c < kAccCols / 32; ++c) {
+                    float vals[32];
+                    const float4 *s4 = reinterpret_cast<const float4 *>(src + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 f = __ldcg(s4 + j);
+                        vals[4 * j] = f.x;
+                        vals[4 * j + 1] = f.y;
+                        vals[4 * j + 2] = f.z;
+                        vals[4 * j + 3] = f.w;
+                    }
+                    chunk(vals, v0 + c * 32);
+                }
+            }
+            for (int tile = tS, ti = 0; tile < t1; ++tile, ++ti) {
                 const int buf = ti & 1;
                 const bool ok = wait_or_abort(&sm.tmem_full[buf], (ti >> 1) & 1, &sm.abort_flag, p.err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;  // tcgen05.ld is warp-collective
@@ -475,57 +564,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int c = 0; c < kAccCols / 32; ++c) {
                     float vals[32];
                     tmem_ld32(tmem + lane_base + buf * kAccCols + c * 32, vals);
-                    const int64_t vc = v0 + c * 32;
-                    const int nvalid = valid ? static_cast<int>(p.V - vc < 32 ? (p.V - vc) : 32) : 0;
-                    const uint32_t vmask = nvalid >= 32 ? 0xFFFFFFFFu
-                                                        : (nvalid > 0 ? ((1u << nvalid) - 1u) : 0u);
-                    if (nvalid > 0) {
-                        float cmax = -INFINITY;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if ((vmask >> j) & 1u) cmax = fmaxf(cmax, vals[j]);
-                        const float mn = fmaxf(m_run, cmax);
-                        if (mn != -INFINITY) {
-                            // exp((v - mn) / T) = 2^((v - mn) * log2(e) / T)
-                            float acc = s_run * ex2_approx((m_run - mn) * l2e_invT);
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if ((vmask >> j) & 1u) acc += ex2_approx((vals[j] - mn) * l2e_invT);
-                            s_run = acc;
-                            m_run = mn;
-                        }
-                    }
-                    // candidates: not below the bound's value (NaN passes),
-                    // then the exact (value, id) order for those only
-                    uint32_t mask = 0;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (!(vals[j] < tau_val)) mask |= 1u << j;
-                    mask &= vmask;
-                    if (mask) mask = exact_mask(vals, mask, vc, tau);
-                    // cut every buffer of the warp this chunk could overflow
-                    unsigned need = __ballot_sync(0xFFFFFFFFu, cnt + __popc(mask) > p.cap);
-                    while (need) {
-                        const int L = __ffs(need) - 1;
-                        need &= need - 1;
-                        const int nL = __shfl_sync(0xFFFFFFFFu, cnt, L);
-                        uint64_t *bufL = cand_lane0 + static_cast<size_t>(L) * p.cap;
-                        const uint64_t kth = p.cap <= 128 ? warp_cut<128>(bufL, nL, p.k, lane)
-                                                          : warp_cut<256>(bufL, nL, p.k, lane);
-                        if (lane == L) {
-                            cnt = nL < p.k ? nL : p.k;
-                            if (kth) {
-                                tau = kth;
-                                tau_val = fmaxf(tau_val, key_value(kth));
-                            }
-                            if (mask) mask = exact_mask(vals, mask, vc, tau);
-                        }
-                    }
-                    if (mask) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if ((mask >> j) & 1u) cand[cnt++] = topk_key(vals[j], static_cast<int32_t>(vc + j));
-                    }
+                    chunk(vals, v0 + c * 32);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -635,6 +674,12 @@ int gemm_lm_head_clusters(const DeviceInfo &dev) {
 
 int gemm_lm_head_sample_len() { return kSampleLen; }
 
+// The sample pass keeps its tile's logits (both CTAs: 2 x GM residuals x GN
+// columns of f32 per cluster) so that the main pass need not recompute them.
+size_t gemm_lm_head_tile_logits_bytes(int clusters) {
+    return static_cast<size_t>(clusters) * 2 * GM * GN * sizeof(float);
+}
+
 cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch, int k, float invT,
                                 float *raw, const GemmBuffers &bufs, int32_t *err, int clusters,
                                 const DeviceInfo &dev, cudaStream_t stream) {
@@ -663,6 +708,7 @@ cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch
         GemmParams ps = p;
         ps.keys = bufs.sample_keys;
         ps.ms = bufs.sample_ms;
+        ps.tile_logits = bufs.tile_logits;
         e = launch_mode<kModeSample>(tm_x, tm_t, ps, dev, stream);
         if (e != cudaSuccess) return e;
         e = launch_merge(bufs.sample_keys, bufs.sample_ms, clusters, kSampleLen, kSampleLen, batch, k,
@@ -674,6 +720,7 @@ cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch
     p.ms = bufs.ms;
     p.cap = bufs.cap;
     p.sample_logits = bound;
+    p.tile_logits = bound ? bufs.tile_logits : nullptr;
     return launch_mode<kModeMain>(tm_x, tm_t, p, dev, stream);
 }
 

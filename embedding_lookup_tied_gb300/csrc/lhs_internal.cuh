@@ -374,6 +374,7 @@ struct LmHeadPlan {
     size_t off_keys;   // partial lists (GEMM: candidate buffers)
     size_t off_ms;
     size_t off_sample_keys, off_sample_ms, off_sample_ids, off_sample_logits;  // GEMM sample pass
+    size_t off_tile_logits;  // GEMM: the sampled tile's logits, reused by the main pass
     int key_stride;    // entries between consecutive partial lists
     bool sample;       // GEMM: run the sample pass
     bool xres;         // tensor-core GEMV: residual operand resident in shared memory (no prep kernel)
@@ -410,6 +411,7 @@ struct GemmBuffers {
     float2 *sample_ms;       // [clusters][batch]
     int32_t *sample_ids;     // [batch][k]
     float *sample_logits;    // [batch][k]
+    float *tile_logits;      // [clusters][256][256] logits of each cluster's sampled tile
     uint64_t *cand;          // [clusters][batch][cap]
     float2 *ms;              // [clusters][batch]
     int cap;
@@ -418,6 +420,7 @@ size_t gemm_lm_head_smem();
 int gemm_lm_head_max_batch();
 int gemm_lm_head_cap(int k);
 int gemm_lm_head_sample_len();
+size_t gemm_lm_head_tile_logits_bytes(int clusters);
 int gemm_lm_head_clusters(const DeviceInfo &dev);
 cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch, int k, float invT,
                                 float *raw, const GemmBuffers &bufs, int32_t *err, int clusters,

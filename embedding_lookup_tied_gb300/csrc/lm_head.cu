@@ -1542,7 +1542,7 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
     // GEMM sample pass: one tile per cluster, worth it when each cluster
     // owns at least two tiles
     p.sample = gemm && k > 0 && (t.vocab + 255) / 256 >= 2 * static_cast<int64_t>(p.grid);
-    p.off_sample_keys = p.off_sample_ms = p.off_sample_ids = p.off_sample_logits = off;
+    p.off_sample_keys = p.off_sample_ms = p.off_sample_ids = p.off_sample_logits = p.off_tile_logits = off;
     if (p.sample) {
         p.off_sample_keys = off;
         off += align_up(static_cast<size_t>(p.grid) * wb * gemm_lm_head_sample_len() * 8, 256);
@@ -1552,6 +1552,8 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
         off += align_up(static_cast<size_t>(wb) * k * 4, 256);
         p.off_sample_logits = off;
         off += align_up(static_cast<size_t>(wb) * k * 4, 256);
+        p.off_tile_logits = off;
+        off += align_up(gemm_lm_head_tile_logits_bytes(p.grid), 256);
     }
     p.bytes = off;
     *plan = p;
@@ -1585,6 +1587,7 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
         gb.sample_ms = reinterpret_cast<float2 *>(wsb + plan.off_sample_ms);
         gb.sample_ids = reinterpret_cast<int32_t *>(wsb + plan.off_sample_ids);
         gb.sample_logits = reinterpret_cast<float *>(wsb + plan.off_sample_logits);
+        gb.tile_logits = plan.sample ? reinterpret_cast<float *>(wsb + plan.off_tile_logits) : nullptr;
         gb.cand = part_keys;
         gb.ms = part_ms;
         gb.cap = plan.key_stride;
