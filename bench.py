@@ -288,20 +288,25 @@ def run_step(c):
 # the kernel sources they were taken on: once the sources change, the
 # recorded traffic no longer describes the kernel and is reported as null.
 TRAFFIC_RECORDS = {
-    # workload: (source digest, bytes per call, summary)
-    "qwen05b": ("732e4ed56b14bf2b", 276.10e6, "profiles/gemv_tc_qwen05b.md"),
-    "batched": ("732e4ed56b14bf2b", 2.948e9, "profiles/gemm_tc_batched.md"),
+    # workload: (digest of the dominant kernel's sources, DRAM bytes per call, summary)
+    "qwen05b": ("172b4ffc98422cd6", 275.96e6, "profiles/gemv_tc_qwen05b.md"),
+    "batched": ("512558a256a019ab", 2.722e9, "profiles/gemm_tc_batched.md"),
 }
-KERNEL_SOURCES = ("embedding_lookup_tied_gb300/csrc/lm_head.cu",
-                  "embedding_lookup_tied_gb300/csrc/gemm_tc.cu",
-                  "embedding_lookup_tied_gb300/csrc/lhs_internal.cuh")
+# the files each recorded kernel is compiled from: a change to any of them
+# voids its record
+KERNEL_SOURCES = {
+    "qwen05b": ("embedding_lookup_tied_gb300/csrc/lm_head.cu",
+                "embedding_lookup_tied_gb300/csrc/lhs_internal.cuh"),
+    "batched": ("embedding_lookup_tied_gb300/csrc/gemm_tc.cu",
+                "embedding_lookup_tied_gb300/csrc/lhs_internal.cuh"),
+}
 L2_BYTES = 129 * 1024 * 1024
 
 
-def kernel_digest() -> str:
+def kernel_digest(name) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[name]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -312,7 +317,7 @@ def recorded_traffic(name):
     if rec is None:
         return None, "no ncu capture recorded for this workload"
     digest, nbytes, src = rec
-    if kernel_digest() != digest:
+    if kernel_digest(name) != digest:
         return None, f"kernel sources changed since the capture in {src}"
     return nbytes, src
 
@@ -482,13 +487,14 @@ def oracle_rate(w, T, ids, R, B, k, fmt, budget_s, threads):
     buf, _ = orc.wire_encode(fmt, xv)
     orc.wire_decode(fmt, buf, B, w.hidden)
     t_fixed = time.perf_counter() - t0
-    rows = 64
+    rows = min(64, w.vocab)
     t_lm = 0.0
     done = 0
     while True:
-        r0 = (done * 7919) % max(1, w.vocab - rows)
+        # consecutive, disjoint slices of the vocabulary, growing until the
+        # budget is spent or every row has been done once
         t1 = time.perf_counter()
-        L = orc.logits(T, w.dtype, w.vocab, w.hidden, xv, v0=r0, v1=r0 + rows,
+        L = orc.logits(T, w.dtype, w.vocab, w.hidden, xv, v0=done, v1=done + rows,
                        threads=threads)
         for b in range(B):
             orc.topk_f64(L[b], min(k, rows))
@@ -496,7 +502,7 @@ def oracle_rate(w, T, ids, R, B, k, fmt, budget_s, threads):
         done += rows
         if t_lm + t_fixed >= budget_s or done >= w.vocab:
             break
-        rows = min(rows * 2, 1 << 14)
+        rows = min(rows * 2, 1 << 14, w.vocab - done)
     t_step = t_fixed + t_lm * (w.vocab / done)
     sample = (f"1 step: full embed ({w.n_ids} ids) + wire encode/decode; lm_head over "
               f"{done} of {w.vocab} vocab rows for {B} residual(s), time scaled x{w.vocab / done:.1f}")

@@ -7,17 +7,21 @@
 // with hundreds of residuals the projection is a dense contraction
 // (2*batch FLOP per table element), so it runs as a GEMM.
 //
-// Orientation: D[m][n] = sum_k X[m][k] * T[n][k].  The residuals are M (one
-// TMEM lane each, 128 per CTA), the vocab rows are N (256 per tile), both
-// operands K-major bf16 staged by TMA with 128-byte swizzle, the f32
-// accumulator lives in TMEM (2 x 256 columns, double-buffered so the MMAs
-// of the next tile overlap the epilogue of this one).  An epilogue thread
-// therefore owns one residual: its running (max, sum exp) and its top-k
-// candidates need no reduction across threads.
+// Orientation: D[m][n] = sum_k X[m][k] * T[n][k].  The residuals are M, the
+// vocab rows are N (256 per tile), both operands K-major bf16 staged by TMA
+// with 128-byte swizzle, the f32 accumulator in TMEM (2 x 256 columns,
+// double-buffered so the MMAs of the next tile overlap the epilogue of this
+// one).  An epilogue thread owns one residual (one TMEM lane): its running
+// (max, sum exp) and its top-k candidates need no reduction across threads.
 //
-// CTAs run in clusters of two, one per half of the residuals.  Both need the
-// same 256-row table tile per stage: each CTA loads 128 rows and multicasts
-// them to both, so HBM reads every table row once per call.
+// CTAs run in pairs (clusters of two) and the leader CTA issues one M = 256
+// MMA (tcgen05 cta_group::2) for the pair: each CTA stages its own 128
+// residuals and its own 128 of the tile's 256 table rows, and receives the
+// 128 x 256 accumulator of its residuals in its TMEM.  HBM reads every table
+// row once per call, and a stage costs each CTA 32 KB of shared memory, so
+// the ring holds seven stages in flight.  Both CTAs' copies of a stage complete
+// on the leader's barrier; the leader's commits free the stage, and hand an
+// accumulator to the epilogue, in both CTAs.
 //
 // Top-k in two passes, so that the main pass keeps almost nothing:
 //  * sample pass: every cluster computes ONE tile (a stratified sample of
@@ -35,11 +39,12 @@
 //    memory, cut back to k by a warp-cooperative bitonic sort if it would
 //    overflow.  The merge selects the final top-k from the buffers.
 //
-// Roles (192 threads): warp 0 — TMA producer; warp 1 — TMEM allocation and
-// the single MMA-issuing thread; warps 2..5 — epilogue (TMEM lane quarter =
-// warp % 4).  Every mbarrier wait is bounded; on expiry the kernel records
-// LHS_ERRBIT_TIMEOUT, every role skips its remaining waits, and the CTA
-// still frees its TMEM and meets its peer at the final cluster barrier.
+// Roles (192 threads): warp 0 — TMA producer; warp 1 — TMEM allocation
+// (with the peer's warp 1) and, in the leader, the single MMA-issuing
+// thread; warps 2..5 — epilogue (TMEM lane quarter = warp % 4).  Every
+// mbarrier wait is bounded; on expiry the kernel records LHS_ERRBIT_TIMEOUT,
+// every role skips its remaining waits, and the CTA still frees its TMEM and
+// meets its peer at the final cluster barrier.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -52,14 +57,14 @@ namespace {
 constexpr int GM = 128;                      // residuals per CTA (TMEM lanes)
 constexpr int GN = 256;                      // vocab rows per tile
 constexpr int GK = 64;                       // k per stage: 128 bytes of bf16
-constexpr int kStagesG = 4;
+constexpr int kStagesG = 7;
 constexpr int kGemmThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kAccCols = 256;                // f32 columns per accumulator buffer
 constexpr int kTmemCols = 512;               // two buffers
 constexpr int kAStageBytes = GM * GK * 2;    // 16 KB: this CTA's residuals
-constexpr int kBStageBytes = GN * GK * 2;    // 32 KB: the whole table tile
-constexpr int kBHalfBytes = kBStageBytes / 2;
+constexpr int kBHalfBytes = GN / 2 * GK * 2; // 16 KB: this CTA's half of the table tile
+constexpr int kPairStageBytes = 2 * (kAStageBytes + kBHalfBytes);  // one stage of both CTAs
 
 enum { kModeRaw = 0, kModeSample = 1, kModeMain = 2 };
 constexpr int kSampleLen = 32;               // sample keys per (cluster, residual)
@@ -84,7 +89,7 @@ struct GemmParams {
 
 struct GemmSmem {
     uint8_t a[kStagesG][kAStageBytes];
-    uint8_t b[kStagesG][kBStageBytes];
+    uint8_t b[kStagesG][kBHalfBytes];
     uint64_t full[kStagesG];
     uint64_t empty[kStagesG];
     uint64_t tmem_full[2];
@@ -103,15 +108,27 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
 }
-// TMA load of a box into the same shared-memory offset of every CTA in
-// `mask`, completing transaction bytes on the barrier at that offset in each.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                               int32_t c0, int32_t c1, uint16_t mask) {
+// The shared::cluster address of the variable at `smem_addr` in CTA `cta`
+// of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, uint32_t cta) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(cta));
+    return r;
+}
+// TMA load of a box into this CTA's shared memory whose completion is
+// counted on an mbarrier of either CTA of the pair (a shared::cluster
+// address): both CTAs' copies of a stage complete on the leader's barrier.
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                 int32_t c0, int32_t c1) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
         : "memory");
+}
+// Arrive on an mbarrier of either CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (the layout TMA writes for a box 64 bf16 wide).
@@ -120,41 +137,37 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(2) << 61);
 }
-// Instruction descriptor, kind::f16: bf16 x bf16 -> f32, both K-major.
+// Instruction descriptor, kind::f16: bf16 x bf16 -> f32, both K-major;
+// M = 256 over the CTA pair (128 TMEM lanes in each), N = 256.
 constexpr uint32_t kIdesc = (1u << 4)                        // D = f32
                             | (1u << 7) | (1u << 10)         // A, B = bf16
-                            | (static_cast<uint32_t>(GN >> 3) << 17)   // N
-                            | (static_cast<uint32_t>(GM >> 4) << 24);  // M
+                            | (static_cast<uint32_t>(GN >> 3) << 17)        // N
+                            | (static_cast<uint32_t>((2 * GM) >> 4) << 24); // M
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
         : "memory");
 }
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
 __device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(smem_u32(bar)),
         "h"(mask)
         : "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
                  "r"(ncols)
                  : "memory");
 }
 __device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -315,17 +328,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 2);       // one MMA commit from each CTA of the pair
+            mbar_init(&sm.full[s], 1);        // leader: its producer's expect_tx; both CTAs' bytes
+            mbar_init(&sm.empty[s], 1);       // the leader's MMA commit, multicast to both CTAs
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.tmem_full[i], 1);
-            mbar_init(&sm.tmem_empty[i], kEpiThreads / 32);
+            mbar_init(&sm.tmem_empty[i], 2 * kEpiThreads / 32);  // leader: both CTAs' epilogue warps
         }
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 1) {  // with the peer's warp 1: the pair's accumulator columns
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -341,23 +354,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&tm_x);
             tma_prefetch_map(&tm_t);
-            const uint16_t both = 0x3;
+            // each CTA loads its residuals and its half of the table tile
+            // into its own shared memory; both complete on the leader's
+            // barrier, which the leader's producer arms for the pair
+            auto full_lead = [&](int s) { return cluster_addr(smem_u32(&sm.full[s]), 0); };
             auto issue_t = [&](uint32_t j) {
                 const int s = j % S;
                 const int tile = tS + static_cast<int>(j / nk), kc = static_cast<int>(j % nk);
-                tma_load_2d_mc(sm.b[s] + rank * kBHalfBytes, &tm_t, &sm.full[s], kc * GK,
-                               tile * GN + static_cast<int>(rank) * (GN / 2), both);
+                tma_load_2d_pair(sm.b[s], &tm_t, full_lead(s), kc * GK,
+                                 tile * GN + static_cast<int>(rank) * (GN / 2));
             };
             auto issue_x = [&](uint32_t j) {
                 const int s = j % S;
-                tma_load_2d(sm.a[s], &tm_x, &sm.full[s], static_cast<int>(j % nk) * GK,
-                            static_cast<int>(rank) * GM);
+                tma_load_2d_pair(sm.a[s], &tm_x, full_lead(s), static_cast<int>(j % nk) * GK,
+                                 static_cast<int>(rank) * GM);
             };
             // table tiles first (never written by an earlier kernel), then
             // wait for the residuals' producer
             const uint32_t pre = total < static_cast<uint32_t>(S) ? total : S;
             for (uint32_t j = 0; j < pre; ++j) {
-                mbar_arrive_expect_tx(&sm.full[j], kAStageBytes + kBStageBytes);
+                if (rank == 0) mbar_arrive_expect_tx(&sm.full[j], kPairStageBytes);
                 issue_t(j);
             }
             pdl_wait();
@@ -366,18 +382,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (; it < total; ++it) {
                 const int s = it % S;
                 if (!wait_or_abort(&sm.empty[s], ((it / S) & 1) ^ 1, &sm.abort_flag, p.err)) break;
-                mbar_arrive_expect_tx(&sm.full[s], kAStageBytes + kBStageBytes);
+                if (rank == 0) mbar_arrive_expect_tx(&sm.full[s], kPairStageBytes);
                 issue_t(it);
                 issue_x(it);
             }
-            // drain: both CTAs have consumed every issued stage, so no copy
-            // or remote arrive is still headed for either CTA
+            // drain: the pair has consumed every issued stage, so no copy,
+            // completion or commit is still headed for either CTA
             for (uint32_t j = (it > static_cast<uint32_t>(S) ? it - S : 0); j < it; ++j)
                 if (!wait_or_abort(&sm.empty[j % S], (j / S) & 1, &sm.abort_flag, p.err)) break;
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer (the leader CTA only) ----------------
+        if (lane == 0 && rank == 0) {
             uint32_t it = 0;
             const uint16_t both = 0x3;
             for (int tile = tS, ti = 0; tile < t1; ++tile, ++ti) {
@@ -401,7 +417,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     umma_commit_mc(&sm.empty[s], both);  // frees the stage in both CTAs
                 }
                 if (!ok) break;
-                umma_commit(&sm.tmem_full[buf]);
+                umma_commit_mc(&sm.tmem_full[buf], both);
             }
         }
     } else {
@@ -432,7 +448,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+                if (lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&sm.tmem_empty[buf]), 0));
             }
         } else if (MODE == kModeSample) {
             // the single tile's logits -> for each of the 32 column groups
@@ -568,7 +584,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.tmem_empty[buf]);
+                if (lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&sm.tmem_empty[buf]), 0));
             }
             if (!ld_vol(&sm.abort_flag)) {
                 // cut buffers holding more than k, then pad to k
@@ -592,6 +608,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // the pair is done with its accumulators and barriers
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

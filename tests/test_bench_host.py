@@ -68,8 +68,8 @@ def test_reference_arm_line_on_rank0():
 
 
 def test_recorded_traffic_is_dropped_when_kernels_change(monkeypatch):
-    d = bench.kernel_digest()
-    assert len(d) == 16
+    d = bench.kernel_digest("qwen05b")
+    assert len(d) == 16 and set(bench.TRAFFIC_RECORDS) <= set(bench.KERNEL_SOURCES)
     monkeypatch.setitem(bench.TRAFFIC_RECORDS, "qwen05b", (d, 1.0e6, "x"))
     assert bench.recorded_traffic("qwen05b") == (1.0e6, "x")
     monkeypatch.setitem(bench.TRAFFIC_RECORDS, "qwen05b", ("0" * 16, 1.0e6, "x"))
