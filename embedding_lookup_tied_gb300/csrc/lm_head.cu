@@ -339,12 +339,19 @@ __device__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, in
 // merge: global top-k of one residual from G partial lists, sorted, + probs.
 // Executed by 256 threads synchronised with named barrier `bar_id`.
 // ---------------------------------------------------------------------------
+constexpr int kMergeHistCand = 1024;  // candidates the histogram merge ranks directly
+
 struct MergeSmemHead {
     uint64_t sel[kMaxK];
     uint64_t tmin;
     unsigned hist[256];
     float2 ms;
     int nsel, sel_digit, sel_above;
+    // histogram merge
+    uint64_t cand[kMergeHistCand];
+    unsigned lo, hi;            // range of the non-empty keys' order keys
+    int n, ncand, bin, above;   // non-empty keys; candidates; the k-th's bin; keys above it
+    float wmax[8], wsum[8];     // per-warp softmax (max, sum)
 };
 
 __device__ void merge_column(const uint64_t *part_keys, const float2 *part_ms, int G, int stride,
@@ -1388,6 +1395,212 @@ __global__ void __launch_bounds__(kBulkThreads, 1) gemv_bulk_kernel(const BulkPa
 // merge: global top-k per residual from G partial lists, sorted, + probs
 // ---------------------------------------------------------------------------
 
+// Top-k of G unsorted lists (a list of `len` keys every `stride`, padded
+// with 0: no real key is 0) for residual b, by 256 threads, with a few
+// histogram passes instead of a digit-by-digit radix select:
+//  A. each warp reads whole lists (no division per load) and appends their
+//     non-empty keys to shared memory, tracking the range [lo, hi] of the
+//     keys' upper 32 bits (the logit's order key);
+//  B. a histogram of (order key - base) >> sh over 256 bins, sh the smallest
+//     shift that fits the window in 256 bins (first window: [lo, hi]);
+//  C. the bin holding the k-th largest key: the keys in it and in the bins
+//     above it (at least k) are the candidates; no other key can be in the
+//     top-k.  While they are more than kMergeRankDirect, B and C repeat on
+//     that bin alone (256 sub-bins of it), down to single order keys;
+//  D. a candidate's rank among the candidates is its final position.
+// Fewer than k non-empty keys, or more than kMergeHistCand candidates that
+// share one order key (tied logits), take the radix select instead.
+constexpr int kMergeRankDirect = 256;
+
+__device__ void merge_column_hist(const uint64_t *part_keys, const float2 *part_ms, int G, int stride,
+                                  int len, int batch_total, int b, int k, float invT, int32_t *out_ids,
+                                  float *out_logits, float *out_probs, MergeSmemHead &h, uint64_t *keys,
+                                  int tid) {
+    constexpr int W = 8, U = 8;
+    const int lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        h.n = 0;
+        h.ncand = 0;
+        h.lo = 0xFFFFFFFFu;
+        h.hi = 0u;
+    }
+    // this thread's share of the softmax partials
+    float2 ms = make_float2(-INFINITY, 0.0f);
+    for (int g = tid; g < G; g += 256)
+        ms = ms_combine(ms, __ldcg(part_ms + static_cast<size_t>(g) * batch_total + b), invT);
+    __syncthreads();
+    // A. lists warp, warp + W, ...; lane walks entries lane, lane + 32, ...
+    //    of the warp's concatenated lists
+    const int ngw = warp < G ? (G - warp + W - 1) / W : 0;
+    const int tot = ngw * len;
+    int li = lane / len, lj = lane % len;
+    unsigned lo = 0xFFFFFFFFu, hi = 0u;
+    for (int base = 0; base < tot; base += 32 * U) {
+        uint64_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            v[u] = 0ull;
+            if (base + 32 * u + lane < tot)
+                v[u] = __ldcg(part_keys + (static_cast<size_t>(warp + W * li) * batch_total + b) * stride + lj);
+            lj += 32;
+            while (lj >= len) {
+                lj -= len;
+                ++li;
+            }
+        }
+        unsigned m[U];
+        int cnt = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            m[u] = __ballot_sync(0xFFFFFFFFu, v[u] != 0ull);
+            cnt += __popc(m[u]);
+        }
+        if (cnt == 0) continue;  // warp-uniform
+        int pos = 0;
+        if (lane == 0) pos = atomicAdd(&h.n, cnt);
+        pos = __shfl_sync(0xFFFFFFFFu, pos, 0);
+        const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (v[u] != 0ull) {
+                keys[pos + __popc(m[u] & below)] = v[u];
+                const unsigned up = static_cast<unsigned>(v[u] >> 32);
+                lo = min(lo, up);
+                hi = max(hi, up);
+            }
+            pos += __popc(m[u]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+    }
+    if (lane == 0 && lo <= hi) {
+        atomicMin(&h.lo, lo);
+        atomicMax(&h.hi, hi);
+    }
+    {
+        float mx = ms.x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if (lane == 0) h.wmax[warp] = mx;
+    }
+    __syncthreads();
+    const int n = h.n;
+    if (n < k) {
+        __syncthreads();  // every thread has read h.n before the radix select reuses h
+        merge_column(part_keys, part_ms, G, stride, len, batch_total, b, k, invT, out_ids, out_logits,
+                     out_probs, h, keys, tid, 1);
+        return;
+    }
+    // the softmax sum rescaled to the overall max, one term per thread
+    float M = h.wmax[0];
+#pragma unroll
+    for (int q = 1; q < W; ++q) M = fmaxf(M, h.wmax[q]);
+    {
+        float t = ms.x == M ? ms.y : (ms.x == -INFINITY ? 0.0f : ms.y * expf((ms.x - M) * invT));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+        if (lane == 0) h.wsum[warp] = t;
+    }
+    // B, C. window [base, base + span), bins of 2^sh order keys; keys above
+    // the window are counted in `above` (all candidates), `need` of the
+    // top-k are still inside it
+    unsigned base = h.lo;
+    const unsigned range = h.hi - base;
+    uint64_t span = static_cast<uint64_t>(range) + 1;
+    int sh = range < 256u ? 0 : 24 - __clz(range);  // (range >> sh) < 256
+    int need = k, above = 0;
+    unsigned edge;
+    int ncand;
+    for (;;) {
+        h.hist[tid] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n; i += 256) {
+            const unsigned up = static_cast<unsigned>(keys[i] >> 32);
+            if (up >= base && static_cast<uint64_t>(up - base) < span) atomicAdd(&h.hist[(up - base) >> sh], 1u);
+        }
+        __syncthreads();
+        // warp 0: lane L owns bins 255-8L ... 248-8L, highest first
+        if (warp == 0) {
+            unsigned c[8];
+            unsigned lsum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c[i] = h.hist[255 - 8 * lane - i];
+                lsum += c[i];
+            }
+            unsigned incl = lsum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const unsigned excl = incl - lsum;
+            if (excl < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= incl) {
+                unsigned run = excl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (run + c[i] >= static_cast<unsigned>(need)) {
+                        h.bin = 255 - 8 * lane - i;
+                        h.above = static_cast<int>(run);
+                        break;
+                    }
+                    run += c[i];
+                }
+            }
+        }
+        __syncthreads();
+        const int bin = h.bin, in_above = h.above;
+        const int in_bin = static_cast<int>(h.hist[bin]);
+        edge = base + (static_cast<unsigned>(bin) << sh);
+        ncand = above + in_above + in_bin;
+        if (ncand <= kMergeRankDirect || sh == 0) break;
+        // refine inside the bin: at most 256 sub-bins of it
+        above += in_above;
+        need -= in_above;
+        base = edge;
+        span = static_cast<uint64_t>(1) << sh;
+        sh = sh > 8 ? sh - 8 : 0;
+        __syncthreads();  // every thread has read hist / bin before they change
+    }
+    if (ncand > kMergeHistCand) {
+        __syncthreads();  // h is read; the radix select reuses it
+        merge_column(part_keys, part_ms, G, stride, len, batch_total, b, k, invT, out_ids, out_logits,
+                     out_probs, h, keys, tid, 1);
+        return;
+    }
+    // D. gather the candidates (order key >= edge), then rank them
+    for (int i0 = 0; i0 < n; i0 += 256) {
+        const int i = i0 + tid;
+        const bool c = i < n && static_cast<unsigned>(keys[i] >> 32) >= edge;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, c);
+        if (m == 0u) continue;
+        int pos = 0;
+        if (lane == 0) pos = atomicAdd(&h.ncand, __popc(m));
+        pos = __shfl_sync(0xFFFFFFFFu, pos, 0);
+        if (c) h.cand[pos + __popc(m & ((1u << lane) - 1u))] = keys[i];
+    }
+    float S = 0.0f;
+#pragma unroll
+    for (int q = 0; q < W; ++q) S += h.wsum[q];
+    __syncthreads();
+    for (int i = tid; i < ncand; i += 256) {
+        const uint64_t x = h.cand[i];
+        int rank = 0;
+#pragma unroll 4
+        for (int q = 0; q < ncand; ++q) rank += h.cand[q] > x;
+        if (rank < k) {
+            const size_t o = static_cast<size_t>(b) * k + rank;
+            const float v = key_value(x);
+            out_ids[o] = key_id(x);
+            out_logits[o] = v;
+            if (out_probs) out_probs[o] = expf((v - M) * invT) / S;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256)
     merge_kernel(const uint64_t *__restrict__ part_keys, const float2 *__restrict__ part_ms, int G,
                  int stride, int len, int batch_total, int k, float invT, int32_t *__restrict__ out_ids,
@@ -1397,8 +1610,8 @@ __global__ void __launch_bounds__(256)
     uint64_t *keys = reinterpret_cast<uint64_t *>(dyn_smem + ((sizeof(MergeSmemHead) + 15) & ~size_t(15)));
     pdl_trigger();
     pdl_wait();
-    merge_column(part_keys, part_ms, G, stride, len, batch_total, blockIdx.x, k, invT, out_ids,
-                 out_logits, out_probs, h, keys, threadIdx.x, 1);
+    merge_column_hist(part_keys, part_ms, G, stride, len, batch_total, blockIdx.x, k, invT, out_ids,
+                      out_logits, out_probs, h, keys, threadIdx.x);
 }
 
 // Merge of the GEMV kernels' sorted lists, one block per residual.  The

@@ -476,6 +476,30 @@ def test_topk_planted_ties_break_by_id(dtype):
         assert np.all(np.diff(top[same]) > 0)
 
 
+@pytest.mark.parametrize("V", [40000, 80000])
+def test_gemm_topk_planted_ties_break_by_id(V):
+    # tcgen05 path with 40 distinct rows repeated: the top logit repeats
+    # V / 40 times, so every candidate of the merge falls in one bin
+    # (1000 ranked directly; 2000 sent to the radix select)
+    H, B, k = 64, 24, 50
+    base = wl.make_table(orc.BF16, 40, H, 0.02, cid=19, threads=1)
+    T = base[np.arange(V) % 40]
+    tab = upload_table(T, orc.BF16, V, H)
+    R = wl.residuals(19, B, H, (0.5, 8.0), orc.BF16)
+    rd = _resid_dev(R, orc.BF16)
+    ids, vals, probs, err = lhs.lhs_logits_topk(tab, rd, k)
+    assert int(err.item()) == 0
+    raw, _ = lhs.lhs_logits(tab, rd)
+    Lg = raw.cpu().numpy()
+    ids, vals, probs = ids.cpu().numpy(), vals.cpu().numpy(), probs.cpu().numpy()
+    for b in range(B):
+        rid, rv = orc.topk_f32(Lg[b], k)
+        assert np.array_equal(ids[b], rid), b
+        assert np.array_equal(vals[b].view(np.uint32), rv.view(np.uint32)), b
+        rp = orc.softmax_probs(Lg[b], 1.0, rid)
+        assert np.all(np.abs(probs[b] - rp) <= PROB_RTOL * rp), b
+
+
 def _topk_matches_own_logits(tab, X, k, temperature=1.0):
     ids, vals, probs, err = lhs.lhs_logits_topk(tab, X, k, temperature=temperature)
     assert int(err.item()) == 0
