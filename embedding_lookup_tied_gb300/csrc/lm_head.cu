@@ -241,6 +241,12 @@ __device__ __forceinline__ void ms_update(float &m, float &s, float v, float inv
         m = mn;
     }
 }
+// s * exp((m - M) / T), the sum of a partial (m, s) rescaled to a max M >= m
+// (exactly s when m == M, including the empty partial m = M = -inf).
+__device__ __forceinline__ float ms_rescaled(float m, float s, float M, float invT) {
+    return m == M ? s : (m == -INFINITY ? 0.0f : s * expf((m - M) * invT));
+}
+
 __device__ __forceinline__ float2 ms_combine(float2 a, float2 b, float invT) {
     const float mn = fmaxf(a.x, b.x);
     if (mn == -INFINITY) return make_float2(-INFINITY, 0.0f);
@@ -329,9 +335,14 @@ __device__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, in
             part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + j] = 0ull;
     }
     if (tid < ncols) {
-        float2 acc = make_float2(-INFINITY, 0.0f);
-        for (int w = 0; w < nthreads / 32; ++w) acc = ms_combine(acc, sm.ms_warp[w][tid], invT);
-        part_ms[static_cast<size_t>(blockIdx.x) * batch_total + b_off + tid] = acc;
+        // the warps' (m, s): max first, then the rescaled sums (independent exps)
+        const int nw = nthreads / 32;
+        float M = -INFINITY;
+        for (int w = 0; w < nw; ++w) M = fmaxf(M, sm.ms_warp[w][tid].x);
+        float S = 0.0f;
+#pragma unroll 4
+        for (int w = 0; w < nw; ++w) S += ms_rescaled(sm.ms_warp[w][tid].x, sm.ms_warp[w][tid].y, M, invT);
+        part_ms[static_cast<size_t>(blockIdx.x) * batch_total + b_off + tid] = make_float2(M, S);
     }
 }
 
@@ -1000,18 +1011,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     // the flag only changes inside the main loop: uniform here
     if (RAW || ld_volatile(&sm.tk.abort_flag)) return;
-    // per-warp (m, s) for columns 2t, 2t+1: reduce over g (lanes t, t+4, ...)
+    // per-warp (m, s) for columns 2t, 2t+1 over g (lanes t, t+4, ...): the
+    // max first, then every lane's sum rescaled to it at once and added
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        float2 ms = make_float2(m_st[c], s_st[c]);
+        float M = m_st[c];
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            float2 other;
-            other.x = __shfl_xor_sync(0xFFFFFFFFu, ms.x, o);
-            other.y = __shfl_xor_sync(0xFFFFFFFFu, ms.y, o);
-            ms = ms_combine(ms, other, p.invT);
-        }
-        if (g == 0 && 2 * t + c < kBatchChunk) sm.tk.ms_warp[warp][2 * t + c] = ms;
+        for (int o = 4; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        float S = ms_rescaled(m_st[c], s_st[c], M, p.invT);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
+        if (g == 0 && 2 * t + c < kBatchChunk) sm.tk.ms_warp[warp][2 * t + c] = make_float2(M, S);
     }
     topk_finish(sm.tk, tid, kConsumers, p.Bc, p.k, cap, p.b_off, p.batch_total, p.part_keys,
                 p.part_ms, p.invT);

@@ -277,6 +277,8 @@ LM_CASES = [
     (orc.F16, 1000, 72, 2, 6, orc.F32),       # hidden % 64 != 0, tensor-core path
     (orc.F16, 1000, 68, 2, 6, orc.F32),       # hidden % 8 != 0 -> CUDA-core path
     (orc.BF16, 100, 64, 3, 100, orc.F32),     # vocab < 128 -> CUDA-core path, k = V
+    (orc.BF16, 100000, 64, 8, 50, orc.F32),   # several 128-row blocks on every SM
+    (orc.F16, 90001, 128, 3, 10, orc.BF16),   # the same with a ragged last block, bf16 residuals
 ]
 
 
@@ -385,6 +387,35 @@ def test_repeated_calls_share_a_workspace():
             ids, _, _, err = lhs.lhs_logits_topk(t, X, k, ws=ws)
             assert int(err.item()) == 0
             assert np.array_equal(ids.cpu().numpy(), r), rep
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xA5, 0xFF])
+def test_calls_on_a_dirty_workspace(fill):
+    # the caller's workspace holds arbitrary bytes on entry: any fill, and
+    # the previous calls' leftovers, give the same result as a fresh call,
+    # raw logits included
+    V, H, B, k = 98000, 96, 2, 16
+    T = wl.make_table(orc.BF16, V, H, 0.02, cid=291, threads=4)
+    tab = upload_table(T, orc.BF16, V, H)
+    X = to_dev(wl.residuals(292, B, H))
+    need = max(lhs.lhs_logits_topk_workspace(tab, B, k, lhs.LHS_F32),
+               lhs.lhs_logits_topk_workspace(tab, B, 0, lhs.LHS_F32))
+    ws = torch.full((need,), fill, dtype=torch.uint8, device="cuda")
+    raw, err = lhs.lhs_logits(tab, X, ws=ws)
+    assert int(err.item()) == 0
+    Lg = raw.cpu().numpy()
+    L64, S64 = orc.logits(T, orc.BF16, V, H, wl.residuals(292, B, H), threads=8, with_sumabs=True)
+    assert np.all(np.abs(Lg.astype(np.float64) - L64) <= RTOL[orc.BF16] * S64 + 1e-30)
+    for rep in range(4):
+        ids, vals, _, err = lhs.lhs_logits_topk(tab, X, k, ws=ws)
+        assert int(err.item()) == 0
+        for b in range(B):
+            rid, rv = orc.topk_f32(Lg[b], k)
+            assert np.array_equal(ids.cpu().numpy()[b], rid), (rep, b)
+            assert np.array_equal(vals.cpu().numpy()[b].view(np.uint32), rv.view(np.uint32)), (rep, b)
+        raw2, err = lhs.lhs_logits(tab, X, ws=ws)
+        assert int(err.item()) == 0
+        assert np.array_equal(raw2.cpu().numpy().view(np.uint32), Lg.view(np.uint32)), rep
 
 
 GEMM_CASES = [
