@@ -201,23 +201,36 @@ __device__ __forceinline__ uint4 pack_f16x8(const float (&v)[8]) {
 }
 
 // i8 code of v: round half to even of the correctly rounded binary32
-// quotient v / scale, clamped to [-127, 127]; 0 when scale is 0.
+// quotient v / scale, clamped to [-127, 127]; 0 when scale is 0.  Returned
+// as an int (its low byte is the code's two's-complement byte).
 // rcp = __frcp_rn(scale).  The product t = RN(v * rcp) is within
 // |v/scale| * 2^-23 of the exact quotient Q, and RN(Q) within |Q| * 2^-24
 // of it; for |t| < 256 the two therefore differ by less than 2^-14.4, so
 // unless t lies within 2^-12 of a half-integer (a rounding boundary of rint)
-// both round to the same integer.  Near a boundary — or when t is out of
-// that range, e.g. a reciprocal that overflowed — the quotient is formed by
-// the correctly rounded divide instead.
-__device__ __forceinline__ int8_t i8_code(float v, float scale, float rcp) {
+// both round to the same integer.  The test is on d = t - rint(t), exact
+// (t and rint(t) are within a factor of two, or rint(t) = 0): |d| < 1/2 -
+// 2^-12 means no boundary is near.  Near one — or when t is out of that
+// range, e.g. a reciprocal that overflowed — the quotient is formed by the
+// correctly rounded divide instead.
+__device__ __forceinline__ int i8_code(float v, float scale, float rcp) {
     if (scale == 0.0f) return 0;
     const float t = __fmul_rn(v, rcp);
-    const float a = fabsf(t);
-    float r;
-    if (a < 256.0f && fabsf((a - floorf(a)) - 0.5f) > 0x1p-12f) r = rintf(t);
-    else r = rintf(__fdiv_rn(v, scale));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return static_cast<int8_t>(static_cast<int>(r));
+    float r = rintf(t);
+    if (!(fabsf(t) < 256.0f && fabsf(t - r) < 0.5f - 0x1p-12f)) r = rintf(__fdiv_rn(v, scale));
+    return __float2int_rn(fminf(fmaxf(r, -127.0f), 127.0f));
+}
+
+// The low bytes of four codes, first in the lowest byte.
+__device__ __forceinline__ uint32_t pack_i8x4(int a, int b, int c, int d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// Eight codes as two little-endian words.
+__device__ __forceinline__ uint2 i8_code8(const float (&v)[8], float scale, float rcp) {
+    return make_uint2(pack_i8x4(i8_code(v[0], scale, rcp), i8_code(v[1], scale, rcp), i8_code(v[2], scale, rcp),
+                                i8_code(v[3], scale, rcp)),
+                      pack_i8x4(i8_code(v[4], scale, rcp), i8_code(v[5], scale, rcp), i8_code(v[6], scale, rcp),
+                                i8_code(v[7], scale, rcp)));
 }
 
 // Block-wide max of non-negative values and OR of a flag; every thread gets
@@ -277,13 +290,7 @@ __device__ __forceinline__ void i8_position_warp(const Load8 &load8, int ng, uin
     for (int g = lane; g < ng; g += 32) {
         float v[8];
         load8(g, v);
-        uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            w0 |= static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i], scale, rcp))) << (8 * i);
-            w1 |= static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i + 4], scale, rcp))) << (8 * i);
-        }
-        codes[g] = make_uint2(w0, w1);
+        codes[g] = i8_code8(v, scale, rcp);
     }
 }
 

@@ -8,13 +8,16 @@
 // clamps to the largest finite value instead of producing inf/NaN.
 //
 // f32 / f16: one elementwise pass, 8 values per thread (16-byte accesses).
-// i8: one warp per position for rows up to 1024 values, one CTA per position
-// for longer or unaligned rows —
+// i8: one warp per position for rows up to 1024 values; longer aligned rows
+// staged in shared memory by a bulk copy while the CTA quantises the previous
+// one; one CTA per position, element by element, for unaligned rows —
 // max-reduce of |x|, one correctly rounded divide for the scale, then
 // round-half-even of the binary32 quotient x/scale for every element.
 // Positions start at 16 + p*(hidden+8): 8-byte aligned when hidden % 8 == 0,
 // so the codes move as 8-byte words.
 #include <cuda_fp16.h>
+
+#include <mutex>
 
 #include "lhs_internal.cuh"
 
@@ -23,7 +26,8 @@ namespace {
 
 constexpr int kEwThreads = 256;
 constexpr int kI8Threads = 128;
-constexpr int kI8Cache = 6;  // 8-value groups a thread keeps in registers (CTA path)
+constexpr int kI8Cache = 6;     // 8-value groups a thread keeps in registers (CTA path)
+constexpr int kI8DecCache = 6;  // 8-value code groups a decoding thread loads with the header
 
 template <int XDT>
 __device__ __forceinline__ float load_x(const void *x, int64_t i) {
@@ -99,23 +103,52 @@ __global__ void __launch_bounds__(kEwThreads)
     }
     const uint8_t *pay = buf + 16;
     const int64_t ng = VEC ? n / 8 : 0;
-    for (int64_t g = tid; g < ng; g += nth) {
-        float4 *o = reinterpret_cast<float4 *>(x) + 2 * g;
+    // kDecUnroll groups of 8 values per thread step, every load issued
+    // before the first store
+    constexpr int kDecUnroll = 4;
+    for (int64_t g0 = tid; g0 < ng; g0 += kDecUnroll * nth) {
         if (FMT == LHS_WIRE_F16) {
-            const uint4 w = __ldg(reinterpret_cast<const uint4 *>(pay) + g);
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-            float v[8];
+            uint4 w[kDecUnroll];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(u[i] & 0xFFFFu)));
-                v[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(u[i] >> 16)));
+            for (int u = 0; u < kDecUnroll; ++u) {
+                const int64_t g = g0 + u * nth;
+                if (g < ng) w[u] = __ldg(reinterpret_cast<const uint4 *>(pay) + g);
             }
-            o[0] = make_float4(v[0], v[1], v[2], v[3]);
-            o[1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+            for (int u = 0; u < kDecUnroll; ++u) {
+                const int64_t g = g0 + u * nth;
+                if (g >= ng) break;
+                const uint32_t q[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&q[i]));
+                    v[2 * i] = f.x;
+                    v[2 * i + 1] = f.y;
+                }
+                float4 *o = reinterpret_cast<float4 *>(x) + 2 * g;
+                o[0] = make_float4(v[0], v[1], v[2], v[3]);
+                o[1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
         } else {
-            const float4 *p = reinterpret_cast<const float4 *>(pay) + 2 * g;
-            o[0] = __ldg(p);
-            o[1] = __ldg(p + 1);
+            float4 w[2 * kDecUnroll];
+#pragma unroll
+            for (int u = 0; u < kDecUnroll; ++u) {
+                const int64_t g = g0 + u * nth;
+                if (g < ng) {
+                    const float4 *p = reinterpret_cast<const float4 *>(pay) + 2 * g;
+                    w[2 * u] = __ldg(p);
+                    w[2 * u + 1] = __ldg(p + 1);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kDecUnroll; ++u) {
+                const int64_t g = g0 + u * nth;
+                if (g >= ng) break;
+                float4 *o = reinterpret_cast<float4 *>(x) + 2 * g;
+                o[0] = w[2 * u];
+                o[1] = w[2 * u + 1];
+            }
         }
     }
     for (int64_t i = ng * 8 + tid; i < n; i += nth) {
@@ -223,27 +256,140 @@ __global__ void __launch_bounds__(kI8Threads)
         for (int c = 0; c < kI8Cache; ++c) {
             const int g = threadIdx.x + c * kI8Threads;
             if (g < ng) {
-                uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    w0 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(cache[c][i], scale, rcp)))) << (8 * i);
-                    w1 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(cache[c][i + 4], scale, rcp)))) << (8 * i);
-                }
-                codes[g] = make_uint2(w0, w1);
+                codes[g] = i8_code8(cache[c], scale, rcp);
             }
         }
         for (int g = threadIdx.x + kI8Cache * kI8Threads; g < ng; g += kI8Threads) {
             float v[8];
             load_x8<XDT>(xp, g, v);
-            uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                w0 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i], scale, rcp)))) << (8 * i);
-                w1 |= (static_cast<uint32_t>(static_cast<uint8_t>(i8_code(v[i + 4], scale, rcp)))) << (8 * i);
-            }
-            codes[g] = make_uint2(w0, w1);
+            codes[g] = i8_code8(v, scale, rcp);
         }
     }
+}
+
+// i8 encode of long rows staged in shared memory: each CTA walks positions
+// blockIdx.x, + gridDim.x, ...; one thread keeps the next kI8Bufs - 1
+// positions' rows in flight (cp.async.bulk into a ring of kI8Bufs row
+// buffers) while the CTA quantises the current one from shared memory —
+// max|x| block-reduced, then 8 codes per thread step.  Two barriers per
+// position: the one that makes the row visible to every thread (and frees
+// the previous position's buffer for the next copy), and the max
+// reduction's, whose per-warp slots alternate between two sets.  Rows of
+// hidden values (f32 or bf16) at 16-byte aligned addresses, hidden % 8 == 0.
+constexpr int kI8BulkThreads = 256;
+constexpr int kI8Bufs = 2;
+constexpr int64_t kI8BulkMaxSmem = 200 * 1024;  // kI8Bufs rows: f32 rows up to 25,600 values
+
+template <int XDT>
+__global__ void __launch_bounds__(kI8BulkThreads)
+    encode_i8_bulk_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
+                          uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    extern __shared__ __align__(128) uint8_t rows[];  // [kI8Bufs][row bytes]
+    __shared__ uint64_t bar[kI8Bufs];
+    __shared__ float sm_m[2][kI8BulkThreads / 32];
+    __shared__ int sm_f[2][kI8BulkThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rb = static_cast<uint32_t>(hidden) * (XDT == LHS_F32 ? 4u : 2u);
+    const uint8_t *xb = static_cast<const uint8_t *>(x);
+    pdl_trigger();
+    if (tid == 0) {
+        for (int b = 0; b < kI8Bufs; ++b) mbar_init(&bar[b], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    if (blockIdx.x == 0 && tid == 0) write_wire_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
+    // thread 0: copy of the CTA's j-th position into buffer j % kI8Bufs
+    int64_t issued = 0;
+    auto issue = [&](int64_t j) {
+        const int64_t p = blockIdx.x + j * gridDim.x;
+        if (p >= seq_len) return;
+        const int b = static_cast<int>(j % kI8Bufs);
+        mbar_arrive_expect_tx(&bar[b], rb);
+        bulk_load(rows + b * rb, xb + p * rb, rb, &bar[b]);
+        issued = j + 1;
+    };
+    if (tid == 0)
+        for (int j = 0; j < kI8Bufs - 1; ++j) issue(j);
+    const int64_t stride = static_cast<int64_t>(hidden) + 8;
+    const int n4 = hidden >> 2, ng = hidden >> 3;
+    int64_t it = 0;
+    for (int64_t p = blockIdx.x; p < seq_len; p += gridDim.x, ++it) {
+        const int cur = static_cast<int>(it % kI8Bufs);
+        const uint8_t *row = rows + cur * rb;
+        const bool here = mbar_wait(&bar[cur], static_cast<uint32_t>(it / kI8Bufs) & 1, kWaitTimeoutNs);
+        // every thread is past the previous position: its buffer takes the
+        // copy kI8Bufs - 1 positions ahead
+        if (!__syncthreads_and(here)) {
+            if (tid == 0) set_err(err, LHS_ERRBIT_TIMEOUT);
+            break;
+        }
+        if (tid == 0) issue(it + kI8Bufs - 1);
+        float m = 0.0f;
+        int nonfinite = 0;
+        for (int i = tid; i < n4; i += kI8BulkThreads) {
+            float v[4];
+            if (XDT == LHS_F32) {
+                const float4 f = reinterpret_cast<const float4 *>(row)[i];
+                v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+            } else {
+                const uint2 w = reinterpret_cast<const uint2 *>(row)[i];
+                v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+                v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (!isfinite(v[j])) nonfinite = 1;
+                else m = fmaxf(m, fabsf(v[j]));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            nonfinite |= __shfl_xor_sync(0xFFFFFFFFu, nonfinite, o);
+        }
+        const int slot = static_cast<int>(it & 1);  // read by every thread before the next position's barrier
+        if (lane == 0) {
+            sm_m[slot][warp] = m;
+            sm_f[slot][warp] = nonfinite;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kI8BulkThreads / 32; ++w) {
+            m = fmaxf(m, sm_m[slot][w]);
+            nonfinite |= sm_f[slot][w];
+        }
+        const float scale = nonfinite ? 0.0f : __fdiv_rn(m, 127.0f);
+        const float rcp = __frcp_rn(scale);
+        uint8_t *pos = buf + 16 + p * stride;
+        if (tid == 0) {
+            *reinterpret_cast<uint2 *>(pos) = make_uint2(__float_as_uint(scale), 0u);
+            if (nonfinite) set_err(err, LHS_ERRBIT_NONFINITE);
+        }
+        uint2 *codes = reinterpret_cast<uint2 *>(pos + 8);
+        for (int g = tid; g < ng; g += kI8BulkThreads) {
+            float v[8];
+            if (XDT == LHS_F32) {
+                const float4 a = reinterpret_cast<const float4 *>(row)[2 * g];
+                const float4 b = reinterpret_cast<const float4 *>(row)[2 * g + 1];
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            } else {
+                const uint4 w = reinterpret_cast<const uint4 *>(row)[g];
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] = __uint_as_float(u[j] << 16);
+                    v[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+                }
+            }
+            codes[g] = i8_code8(v, scale, rcp);
+        }
+    }
+    // copies still headed for this CTA (after a timeout) land before it exits
+    if (tid == 0)
+        for (int64_t j = it; j < issued; ++j)
+            if (!mbar_wait(&bar[j % kI8Bufs], static_cast<uint32_t>(j / kI8Bufs) & 1, kWaitTimeoutNs)) break;
 }
 
 // i8 encode with 16-byte-aligned rows (hidden % 8 == 0): one warp per
@@ -286,7 +432,13 @@ __global__ void __launch_bounds__(kI8Threads)
     for (int64_t p = blockIdx.x; p < seq_len; p += gridDim.x) {
         const uint8_t *pos = buf + 16 + p * stride;
         float scale, zp;
+        uint2 pre[VEC ? kI8DecCache : 1];
         if (VEC) {
+#pragma unroll
+            for (int c = 0; c < kI8DecCache; ++c) {
+                const int g = threadIdx.x + c * kI8Threads;
+                if (g < (hidden >> 3)) pre[c] = __ldg(reinterpret_cast<const uint2 *>(pos + 8) + g);
+            }
             const uint2 h = __ldg(reinterpret_cast<const uint2 *>(pos));
             scale = __uint_as_float(h.x);
             zp = __uint_as_float(h.y);
@@ -308,7 +460,25 @@ __global__ void __launch_bounds__(kI8Threads)
         if (VEC) {
             const uint2 *codes = reinterpret_cast<const uint2 *>(pos + 8);
             float4 *o = reinterpret_cast<float4 *>(xo);
-            for (int g = threadIdx.x; g < (hidden >> 3); g += kI8Threads) {
+            const int ng = hidden >> 3;
+            // the first kI8DecCache groups of this thread were loaded with
+            // the header, before its scale is known
+#pragma unroll
+            for (int c = 0; c < kI8DecCache; ++c) {
+                const int g = threadIdx.x + c * kI8Threads;
+                if (g < ng) {
+                    const uint2 w = pre[c];
+                    float v[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        v[i] = __fmul_rn(static_cast<float>(static_cast<int8_t>(w.x >> (8 * i))), scale);
+                        v[4 + i] = __fmul_rn(static_cast<float>(static_cast<int8_t>(w.y >> (8 * i))), scale);
+                    }
+                    o[2 * g] = make_float4(v[0], v[1], v[2], v[3]);
+                    o[2 * g + 1] = make_float4(v[4], v[5], v[6], v[7]);
+                }
+            }
+            for (int g = threadIdx.x + kI8DecCache * kI8Threads; g < ng; g += kI8Threads) {
                 const uint2 w = __ldg(codes + g);
                 float v[8];
 #pragma unroll
@@ -345,6 +515,34 @@ cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_
     const int64_t n = static_cast<int64_t>(seq_len) * hidden;
     const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(buf)) % 16) == 0;
     const uint32_t s = static_cast<uint32_t>(seq_len);
+    const int64_t i8_row = static_cast<int64_t>(hidden) * (x_dtype == LHS_F32 ? 4 : 2);
+    if (fmt == LHS_WIRE_I8 && aligned && hidden % 8 == 0 && hidden > 1024 && kI8Bufs * i8_row <= kI8BulkMaxSmem) {
+        // rows staged in shared memory, kI8Bufs per CTA; as many CTAs per SM
+        // as the shared memory holds, at most 8
+        const size_t smem = static_cast<size_t>(kI8Bufs * i8_row);
+        auto kern = x_dtype == LHS_F32 ? encode_i8_bulk_kernel<LHS_F32> : encode_i8_bulk_kernel<LHS_BF16>;
+        {
+            // the largest size this kernel is launched with, once per device
+            // and instantiation (static shared memory comes on top of it)
+            static std::mutex mu;
+            static bool done[2][64] = {};
+            std::lock_guard<std::mutex> lock(mu);
+            bool &d = done[x_dtype == LHS_F32 ? 0 : 1][dev.device];
+            if (!d) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kI8BulkMaxSmem));
+                if (e != cudaSuccess) return e;
+                d = true;
+            }
+        }
+        int64_t per_sm = (200 * 1024) / static_cast<int64_t>(smem + 1024);
+        if (per_sm > 8) per_sm = 8;
+        if (per_sm < 1) per_sm = 1;
+        const int64_t cap = static_cast<int64_t>(dev.num_sms) * per_sm;
+        const int grid = static_cast<int>(seq_len < 1 ? 1 : (seq_len < cap ? seq_len : cap));
+        return launch_pdl(kern, dim3(grid), dim3(kI8BulkThreads), smem, stream, x, seq_len, hidden, layer, flags,
+                          top_k, b, err);
+    }
     if (fmt == LHS_WIRE_I8 && aligned && hidden % 8 == 0 && hidden > 1024) {
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
         const int grid = static_cast<int>(seq_len < 1 ? 1 : (seq_len < cap ? seq_len : cap));

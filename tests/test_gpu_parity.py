@@ -96,7 +96,7 @@ def _special(x):
 
 
 @pytest.mark.parametrize("shape", [(4, 256), (1, 896), (8, 5376), (3, 100), (2, 9), (0, 64), (2, 8200),
-                                   (40, 1024)])
+                                   (40, 1024), (3000, 2048), (1500, 5376), (300, 6144)])
 @pytest.mark.parametrize("xdt", [orc.F32, orc.BF16])
 @pytest.mark.parametrize("fmt", [orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8])
 def test_wire_parity(shape, xdt, fmt):
@@ -185,12 +185,12 @@ def test_embed_wire_full_size_gemma_q8():
         assert int(err.item()) == e2
 
 
+@pytest.mark.parametrize("H", [1024, 2048])   # one warp per position; rows staged per CTA
 @pytest.mark.parametrize("xdt", [orc.F32, orc.BF16])
-def test_i8_codes_at_rounding_boundaries(xdt):
+def test_i8_codes_at_rounding_boundaries(xdt, H):
     # quotients x / scale at, just below and just above every half-integer:
     # the encoder's product-with-reciprocal shortcut must fall back to the
     # correctly rounded divide exactly where rounding could differ
-    H = 1024
     rows = []
     for m in (1.0, 3.0, 1e-3, 7.5e-39):      # last: a subnormal scale
         scale = np.float32(np.float32(m) / np.float32(127.0))
@@ -213,6 +213,21 @@ def test_i8_codes_at_rounding_boundaries(xdt):
     buf, err = lhs.lhs_wire_encode(orc.WIRE_I8, xd)
     assert np.array_equal(buf.cpu().numpy(), ref)
     assert int(err.item()) == ref_err
+
+
+@pytest.mark.parametrize("H", [896, 4096])
+def test_i8_nonfinite_rows_many_positions(H):
+    # inf / NaN rows among 700 positions: those get scale 0 and zero codes
+    # and raise the flag; the rows around them are unaffected
+    g = np.random.default_rng(H)
+    x = (g.standard_normal((700, H)) * g.uniform(0.1, 9.0, (700, 1))).astype(np.float32)
+    x[3, 7] = np.inf
+    x[400, H - 1] = np.nan
+    x[699, 0] = -np.inf
+    ref, ref_err = orc.wire_encode(orc.WIRE_I8, x)
+    buf, err = lhs.lhs_wire_encode(orc.WIRE_I8, to_dev(x))
+    assert np.array_equal(buf.cpu().numpy(), ref)
+    assert int(err.item()) == ref_err == lhs.LHS_ERRBIT_NONFINITE
 
 
 def test_wire_accuracy_topk_agreement():
