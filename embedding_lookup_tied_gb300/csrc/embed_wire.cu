@@ -10,8 +10,9 @@
 //
 // f32 / f16: one warp per token, 8 elements per lane step (16-byte loads and
 // stores).  i8: one warp per token — max|x| of the scaled row, then the
-// codes from a second read of the row (the same steps, in the same binary32
-// operations, as the i8 encoder).
+// codes (the same steps, in the same binary32 operations, as the i8
+// encoder); rows up to 1024 values stay in registers between the two,
+// longer rows are read a second time.
 #include "lhs_internal.cuh"
 
 namespace lhs {
@@ -152,19 +153,59 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// i8 with rows of at most 1024 values: one warp per token, the scaled row in
+// registers between the max and the codes.
+template <int DT>
+__global__ void __launch_bounds__(128)
+    embed_wire_i8_warp4_kernel(const uint8_t *__restrict__ table, int64_t vocab, int hidden, int64_t row_bytes,
+                               const int32_t *__restrict__ ids, int64_t n, float scale, uint32_t layer,
+                               uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    pdl_trigger();
+    pdl_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        write_wire_header(buf, layer, static_cast<uint32_t>(n), flags, top_k);
+    const int lane = threadIdx.x & 31;
+    const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t stride = static_cast<int64_t>(hidden) + 8;
+    const int n4 = hidden >> 2;
+    for (int64_t p = w0; p < n; p += nw) {
+        const int32_t id = __ldg(ids + p);
+        const bool bad = bad_id(id, vocab);
+        if (bad && lane == 0) set_err(err, LHS_ERRBIT_BAD_TOKEN);
+        const uint8_t *row = table + static_cast<int64_t>(bad ? 0 : id) * row_bytes;
+        i8_position_warp4(
+            [&](int st, float (&v)[4]) {
+                if (bad) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = 0.0f;
+                } else {
+                    row_elements4<DT>(row, st, v);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(v[i], scale);
+                }
+            },
+            n4, buf + 16 + p * stride, lane, err);
+    }
+}
+
 template <int DT>
 cudaError_t launch_dt(const lhs_table &t, const int32_t *ids, int64_t n, float scale, int fmt,
                       uint32_t layer, uint32_t flags, uint32_t top_k, uint8_t *buf, int32_t *err,
-                      cudaStream_t stream, int num_sms) {
+                      cudaStream_t stream, int num_sms, int device) {
     const uint8_t *tb = static_cast<const uint8_t *>(t.data);
     // 8-element steps: rows 16-byte aligned (Q8_0: 2-byte) and hidden % 8 == 0
     bool vec = t.hidden % 8 == 0;
     if (DT != LHS_Q8_0) vec = vec && (reinterpret_cast<uintptr_t>(t.data) % 16 == 0) && (t.row_bytes % 16 == 0);
+    if (fmt == LHS_WIRE_I8 && vec && t.hidden <= 32 * kI8WarpSteps * 4) {
+        const int wps = i8_warps_per_sm(t.row_bytes);
+        const int grid = warp_kernel_grid(embed_wire_i8_warp4_kernel<DT>, n, wps, num_sms, device);
+        return launch_pdl(embed_wire_i8_warp4_kernel<DT>, dim3(grid), dim3(128), 0, stream, tb, t.vocab, t.hidden,
+                          t.row_bytes, ids, n, scale, layer, flags, top_k, buf, err);
+    }
     if (fmt == LHS_WIRE_I8 && vec) {
         const int wps = i8_warps_per_sm(t.row_bytes);
-        const int64_t cap = static_cast<int64_t>(num_sms) * wps;
-        const int64_t warps = n < cap ? n : cap;
-        const int grid = static_cast<int>(warps < 4 ? 1 : (warps + 3) / 4);
+        const int grid = warp_kernel_grid(embed_wire_i8_warp_kernel<DT>, n, wps, num_sms, device);
         return launch_pdl(embed_wire_i8_warp_kernel<DT>, dim3(grid), dim3(128), 0, stream, tb, t.vocab, t.hidden,
                           t.row_bytes, ids, n, scale, layer, flags, top_k, buf, err);
     }
@@ -195,10 +236,14 @@ cudaError_t launch_embed_wire(const lhs_table &t, const int32_t *ids, int64_t n,
     if (e != cudaSuccess) return e;
     uint8_t *b = static_cast<uint8_t *>(buf);
     switch (t.dtype) {
-    case LHS_F32: return launch_dt<LHS_F32>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream, dev.num_sms);
-    case LHS_F16: return launch_dt<LHS_F16>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream, dev.num_sms);
-    case LHS_BF16: return launch_dt<LHS_BF16>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream, dev.num_sms);
-    default: return launch_dt<LHS_Q8_0>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream, dev.num_sms);
+    case LHS_F32: return launch_dt<LHS_F32>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream,
+                                                   dev.num_sms, dev.device);
+    case LHS_F16: return launch_dt<LHS_F16>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream,
+                                                   dev.num_sms, dev.device);
+    case LHS_BF16: return launch_dt<LHS_BF16>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream,
+                                                   dev.num_sms, dev.device);
+    default: return launch_dt<LHS_Q8_0>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream,
+                                                   dev.num_sms, dev.device);
     }
 }
 

@@ -170,6 +170,31 @@ __device__ __forceinline__ void row_elements8(const uint8_t *row, int g, float (
     }
 }
 
+// Elements 4s .. 4s+3 of a row (hidden % 4 == 0; f32 rows 16-byte aligned,
+// f16/bf16 rows 8-byte aligned; Q8_0 rows 2-byte aligned).
+template <int DT>
+__device__ __forceinline__ void row_elements4(const uint8_t *row, int s, float (&v)[4]) {
+    if (DT == LHS_F32) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(row) + s);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else if (DT == LHS_F16 || DT == LHS_BF16) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(row) + s);
+        v[0] = DT == LHS_F16 ? f16_bits_to_f32(w.x & 0xFFFFu) : bf16_bits_to_f32(w.x & 0xFFFFu);
+        v[1] = DT == LHS_F16 ? f16_bits_to_f32(w.x >> 16) : bf16_bits_to_f32(w.x >> 16);
+        v[2] = DT == LHS_F16 ? f16_bits_to_f32(w.y & 0xFFFFu) : bf16_bits_to_f32(w.y & 0xFFFFu);
+        v[3] = DT == LHS_F16 ? f16_bits_to_f32(w.y >> 16) : bf16_bits_to_f32(w.y >> 16);
+    } else {
+        const unsigned short *b16 = reinterpret_cast<const unsigned short *>(row + (s >> 3) * 34);
+        const float d = f16_bits_to_f32(__ldg(b16));
+        const int q0 = 1 + (s & 7) * 2;  // codes (s & 7) * 4 .. +3, two per 16-bit word
+        const uint32_t w0 = __ldg(b16 + q0), w1 = __ldg(b16 + q0 + 1);
+        v[0] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(w0 & 0xFF)));
+        v[1] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(w0 >> 8)));
+        v[2] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(w1 & 0xFF)));
+        v[3] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(w1 >> 8)));
+    }
+}
+
 // binary16 bits of x, round to nearest even; a finite x whose rounding
 // overflows saturates to +-65504, inf stays inf, NaN becomes 0x7E00.
 __device__ __forceinline__ uint32_t f16_sat_bits(float x) {
@@ -225,12 +250,56 @@ __device__ __forceinline__ uint32_t pack_i8x4(int a, int b, int c, int d) {
     return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
+// The codes of N values, the same as i8_code's, without conversion
+// instructions on the common path: for |t| < 2^22, y = RN(t + 1.5 * 2^23)
+// lies in [2^23, 2^24], where the spacing is 1, so y is t rounded half to
+// even plus 1.5 * 2^23 — r = y - 1.5 * 2^23 (exact) is rint(t), and the
+// bits of y are 0x4B400000 + rint(t).  When |t| < 127.5 and t is not within
+// 2^-12 of a half-integer, rint(t) is the code (i8_code's argument), already
+// in [-127, 127].  The other values, rare, take the correctly rounded divide
+// in a loop over their bits that the compiler cannot turn into N divides for
+// every call.  q[i]'s low byte is the code.
+template <int N>
+__device__ __forceinline__ void i8_codes(const float (&v)[N], float scale, float rcp, int (&q)[N]) {
+    if (scale == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) q[i] = 0;
+        return;
+    }
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    uint32_t slow = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float t = __fmul_rn(v[i], rcp);
+        const float y = __fadd_rn(t, kMagic);
+        const float r = __fsub_rn(y, kMagic);
+        q[i] = static_cast<int>(__float_as_uint(y) - 0x4B400000u);
+        if (!(fabsf(t) < 127.5f && fabsf(__fsub_rn(t, r)) < 0.5f - 0x1p-12f)) slow |= 1u << i;
+    }
+    while (slow) {
+        const int i = __ffs(slow) - 1;
+        slow &= slow - 1;
+        float vi = v[0];
+#pragma unroll
+        for (int j = 1; j < N; ++j) vi = i == j ? v[j] : vi;
+        const int qi = __float2int_rn(fminf(fmaxf(rintf(__fdiv_rn(vi, scale)), -127.0f), 127.0f));
+#pragma unroll
+        for (int j = 0; j < N; ++j) q[j] = i == j ? qi : q[j];
+    }
+}
+
 // Eight codes as two little-endian words.
 __device__ __forceinline__ uint2 i8_code8(const float (&v)[8], float scale, float rcp) {
-    return make_uint2(pack_i8x4(i8_code(v[0], scale, rcp), i8_code(v[1], scale, rcp), i8_code(v[2], scale, rcp),
-                                i8_code(v[3], scale, rcp)),
-                      pack_i8x4(i8_code(v[4], scale, rcp), i8_code(v[5], scale, rcp), i8_code(v[6], scale, rcp),
-                                i8_code(v[7], scale, rcp)));
+    int q[8];
+    i8_codes<8>(v, scale, rcp, q);
+    return make_uint2(pack_i8x4(q[0], q[1], q[2], q[3]), pack_i8x4(q[4], q[5], q[6], q[7]));
+}
+
+// Four codes as one little-endian word.
+__device__ __forceinline__ uint32_t i8_code4(const float (&v)[4], float scale, float rcp) {
+    int q[4];
+    i8_codes<4>(v, scale, rcp, q);
+    return pack_i8x4(q[0], q[1], q[2], q[3]);
 }
 
 // Block-wide max of non-negative values and OR of a flag; every thread gets
@@ -294,6 +363,47 @@ __device__ __forceinline__ void i8_position_warp(const Load8 &load8, int ng, uin
     }
 }
 
+// One i8 position of at most 32 * kI8WarpSteps * 4 values by one warp, the
+// values kept in registers between the two passes: load4(s, v) yields
+// values 4s .. 4s+3 (n4 steps; lane l takes steps l, l + 32, ...; every load
+// is issued before the first value is used).  Same results as
+// i8_position_warp.  pos: [scale f32][zero point f32 = 0][codes], 4-byte
+// aligned codes.
+constexpr int kI8WarpSteps = 8;  // rows up to 1024 values
+template <typename Load4>
+__device__ __forceinline__ void i8_position_warp4(const Load4 &load4, int n4, uint8_t *pos, int lane,
+                                                  int32_t *err) {
+    float c[kI8WarpSteps][4];
+#pragma unroll
+    for (int k = 0; k < kI8WarpSteps; ++k)
+        if (lane + 32 * k < n4) load4(lane + 32 * k, c[k]);
+    // max|x| (fmaxf passes over NaN) and, in z, 0 * x summed: NaN exactly
+    // when some x is inf or NaN
+    float m = 0.0f, z = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kI8WarpSteps; ++k)
+        if (lane + 32 * k < n4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                m = fmaxf(m, fabsf(c[k][i]));
+                z = __fmaf_rn(c[k][i], 0.0f, z);
+            }
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const bool nonfinite = __any_sync(0xFFFFFFFFu, z != z);
+    const float scale = nonfinite ? 0.0f : __fdiv_rn(m, 127.0f);
+    const float rcp = __frcp_rn(scale);
+    if (lane == 0) {
+        *reinterpret_cast<uint2 *>(pos) = make_uint2(__float_as_uint(scale), 0u);
+        if (nonfinite) set_err(err, LHS_ERRBIT_NONFINITE);
+    }
+    uint32_t *codes = reinterpret_cast<uint32_t *>(pos + 8);
+#pragma unroll
+    for (int k = 0; k < kI8WarpSteps; ++k)
+        if (lane + 32 * k < n4) codes[lane + 32 * k] = i8_code4(c[k], scale, rcp);
+}
+
 // Warps per SM for the warp-per-position i8 kernels: as many as keep the
 // positions' values (the second pass re-reads them) within about 192 KB of
 // L1, between 8 and 48.
@@ -302,6 +412,21 @@ inline int i8_warps_per_sm(int64_t bytes_per_position) {
     if (w > 48) w = 48;
     if (w < 8) w = 8;
     return static_cast<int>(w);
+}
+
+// Grid of a warp-per-position kernel (4 warps per CTA) for n positions: at
+// most `wps` warps per SM and no more CTAs than stay resident at once, so
+// the grid is one wave and each warp walks its positions.
+// (The occupancy query is made once per kernel and device.)
+int resident_ctas_128(const void *kernel, int device);
+template <typename K>
+int warp_kernel_grid(K kernel, int64_t n, int wps, int num_sms, int device) {
+    const int resident = resident_ctas_128(reinterpret_cast<const void *>(kernel), device);
+    int per_sm = wps / 4 < resident ? wps / 4 : resident;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
+    const int64_t ctas = (n + 3) / 4;
+    return static_cast<int>(ctas < 1 ? 1 : (ctas < cap ? ctas : cap));
 }
 
 __device__ __forceinline__ void write_wire_header(uint8_t *buf, uint32_t layer, uint32_t seq_len,

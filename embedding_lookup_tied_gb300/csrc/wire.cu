@@ -325,8 +325,9 @@ __global__ void __launch_bounds__(kI8BulkThreads)
             break;
         }
         if (tid == 0) issue(it + kI8Bufs - 1);
-        float m = 0.0f;
-        int nonfinite = 0;
+        // max|x| (fmaxf passes over NaN) and 0 * x summed: NaN exactly when
+        // some x is inf or NaN
+        float m = 0.0f, z = 0.0f;
         for (int i = tid; i < n4; i += kI8BulkThreads) {
             float v[4];
             if (XDT == LHS_F32) {
@@ -339,10 +340,11 @@ __global__ void __launch_bounds__(kI8BulkThreads)
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (!isfinite(v[j])) nonfinite = 1;
-                else m = fmaxf(m, fabsf(v[j]));
+                m = fmaxf(m, fabsf(v[j]));
+                z = __fmaf_rn(v[j], 0.0f, z);
             }
         }
+        int nonfinite = z != z;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -406,13 +408,21 @@ __global__ void __launch_bounds__(128)
     const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
-    const int ng = hidden >> 3;
+    const int n4 = hidden >> 2;  // hidden <= 32 * kI8WarpSteps * 4
     for (int64_t p = w0; p < seq_len; p += nw) {
         const int64_t xrow = p * static_cast<int64_t>(hidden);
-        const void *xp = XDT == LHS_F32 ? static_cast<const void *>(static_cast<const float *>(x) + xrow)
-                                        : static_cast<const void *>(static_cast<const unsigned short *>(x) + xrow);
-        i8_position_warp([&](int g, float (&v)[8]) { load_x8<XDT>(xp, g, v); }, ng, buf + 16 + p * stride,
-                         lane, err);
+        i8_position_warp4(
+            [&](int st, float (&v)[4]) {
+                if (XDT == LHS_F32) {
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + xrow) + st);
+                    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                } else {
+                    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(static_cast<const unsigned short *>(x) + xrow) + st);
+                    v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+                    v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+                }
+            },
+            n4, buf + 16 + p * stride, lane, err);
     }
 }
 
@@ -505,6 +515,28 @@ int ew_grid(int64_t work_items, int num_sms) {
 
 }  // namespace
 
+// CTAs of 128 threads (no dynamic shared memory) of `kernel` resident on one
+// SM, cached per kernel and device.
+int resident_ctas_128(const void *kernel, int device) {
+    struct Entry {
+        const void *k;
+        int device, n;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int used = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].k == kernel && cache[i].device == device) return cache[i].n;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 128, 0) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    if (used < 64) cache[used++] = Entry{kernel, device, n};
+    return n;
+}
+
 cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_len,
                                int32_t hidden, uint32_t layer, uint32_t flags, uint32_t top_k,
                                void *buf, int32_t *err, cudaStream_t stream) {
@@ -552,10 +584,8 @@ cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_
     }
     if (fmt == LHS_WIRE_I8 && aligned && hidden % 8 == 0) {
         const int wps = i8_warps_per_sm(static_cast<int64_t>(hidden) * (x_dtype == LHS_F32 ? 4 : 2));
-        const int64_t warps = seq_len < static_cast<int64_t>(dev.num_sms) * wps ? seq_len
-                                                                                  : static_cast<int64_t>(dev.num_sms) * wps;
-        const int grid = static_cast<int>(warps < 4 ? 1 : (warps + 3) / 4);
         auto kern = x_dtype == LHS_F32 ? encode_i8_warp_kernel<LHS_F32> : encode_i8_warp_kernel<LHS_BF16>;
+        const int grid = warp_kernel_grid(kern, seq_len, wps, dev.num_sms, dev.device);
         return launch_pdl(kern, dim3(grid), dim3(128), 0, stream, x, seq_len, hidden, layer, flags, top_k, b,
                           err);
     }
