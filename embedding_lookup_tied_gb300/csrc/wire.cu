@@ -27,7 +27,7 @@ namespace {
 constexpr int kEwThreads = 256;
 constexpr int kI8Threads = 128;
 constexpr int kI8Cache = 6;     // 8-value groups a thread keeps in registers (CTA path)
-constexpr int kI8DecCache = 6;  // 8-value code groups a decoding thread loads with the header
+constexpr int kI8DecCache = 12;  // 4-code units a decoding thread loads with the header
 
 template <int XDT>
 __device__ __forceinline__ float load_x(const void *x, int64_t i) {
@@ -102,56 +102,43 @@ __global__ void __launch_bounds__(kEwThreads)
         return;
     }
     const uint8_t *pay = buf + 16;
-    const int64_t ng = VEC ? n / 8 : 0;
-    // kDecUnroll groups of 8 values per thread step, every load issued
-    // before the first store
+    // 4 values per unit: a warp's unit loads and stores are contiguous (512
+    // bytes written per instruction, whole 32-byte sectors); kDecUnroll units
+    // per thread step, every load issued before the first store
+    const int64_t ng = VEC ? n / 4 : 0;
     constexpr int kDecUnroll = 4;
     for (int64_t g0 = tid; g0 < ng; g0 += kDecUnroll * nth) {
         if (FMT == LHS_WIRE_F16) {
-            uint4 w[kDecUnroll];
+            uint2 w[kDecUnroll];
 #pragma unroll
             for (int u = 0; u < kDecUnroll; ++u) {
                 const int64_t g = g0 + u * nth;
-                if (g < ng) w[u] = __ldg(reinterpret_cast<const uint4 *>(pay) + g);
+                if (g < ng) w[u] = __ldg(reinterpret_cast<const uint2 *>(pay) + g);
             }
 #pragma unroll
             for (int u = 0; u < kDecUnroll; ++u) {
                 const int64_t g = g0 + u * nth;
                 if (g >= ng) break;
-                const uint32_t q[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-                float v[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&q[i]));
-                    v[2 * i] = f.x;
-                    v[2 * i + 1] = f.y;
-                }
-                float4 *o = reinterpret_cast<float4 *>(x) + 2 * g;
-                o[0] = make_float4(v[0], v[1], v[2], v[3]);
-                o[1] = make_float4(v[4], v[5], v[6], v[7]);
+                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w[u].x));
+                const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w[u].y));
+                reinterpret_cast<float4 *>(x)[g] = make_float4(a.x, a.y, b.x, b.y);
             }
         } else {
-            float4 w[2 * kDecUnroll];
+            float4 w[kDecUnroll];
 #pragma unroll
             for (int u = 0; u < kDecUnroll; ++u) {
                 const int64_t g = g0 + u * nth;
-                if (g < ng) {
-                    const float4 *p = reinterpret_cast<const float4 *>(pay) + 2 * g;
-                    w[2 * u] = __ldg(p);
-                    w[2 * u + 1] = __ldg(p + 1);
-                }
+                if (g < ng) w[u] = __ldg(reinterpret_cast<const float4 *>(pay) + g);
             }
 #pragma unroll
             for (int u = 0; u < kDecUnroll; ++u) {
                 const int64_t g = g0 + u * nth;
                 if (g >= ng) break;
-                float4 *o = reinterpret_cast<float4 *>(x) + 2 * g;
-                o[0] = w[2 * u];
-                o[1] = w[2 * u + 1];
+                reinterpret_cast<float4 *>(x)[g] = w[u];
             }
         }
     }
-    for (int64_t i = ng * 8 + tid; i < n; i += nth) {
+    for (int64_t i = ng * 4 + tid; i < n; i += nth) {
         if (FMT == LHS_WIRE_F16)
             x[i] = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(pay) + i)));
         else
@@ -442,12 +429,12 @@ __global__ void __launch_bounds__(kI8Threads)
     for (int64_t p = blockIdx.x; p < seq_len; p += gridDim.x) {
         const uint8_t *pos = buf + 16 + p * stride;
         float scale, zp;
-        uint2 pre[VEC ? kI8DecCache : 1];
+        uint32_t pre[VEC ? kI8DecCache : 1];
         if (VEC) {
 #pragma unroll
             for (int c = 0; c < kI8DecCache; ++c) {
                 const int g = threadIdx.x + c * kI8Threads;
-                if (g < (hidden >> 3)) pre[c] = __ldg(reinterpret_cast<const uint2 *>(pos + 8) + g);
+                if (g < (hidden >> 2)) pre[c] = __ldg(reinterpret_cast<const uint32_t *>(pos + 8) + g);
             }
             const uint2 h = __ldg(reinterpret_cast<const uint2 *>(pos));
             scale = __uint_as_float(h.x);
@@ -468,37 +455,25 @@ __global__ void __launch_bounds__(kI8Threads)
         }
         float *xo = x + p * static_cast<int64_t>(hidden);
         if (VEC) {
-            const uint2 *codes = reinterpret_cast<const uint2 *>(pos + 8);
+            // 4 codes -> 4 values per unit: a warp's stores are 512
+            // contiguous bytes (whole 32-byte sectors)
+            const uint32_t *codes = reinterpret_cast<const uint32_t *>(pos + 8);
             float4 *o = reinterpret_cast<float4 *>(xo);
-            const int ng = hidden >> 3;
-            // the first kI8DecCache groups of this thread were loaded with
+            const int ng = hidden >> 2;
+            auto put = [&](int g, uint32_t w) {
+                o[g] = make_float4(__fmul_rn(static_cast<float>(static_cast<int8_t>(w)), scale),
+                                   __fmul_rn(static_cast<float>(static_cast<int8_t>(w >> 8)), scale),
+                                   __fmul_rn(static_cast<float>(static_cast<int8_t>(w >> 16)), scale),
+                                   __fmul_rn(static_cast<float>(static_cast<int8_t>(w >> 24)), scale));
+            };
+            // the first kI8DecCache units of this thread were loaded with
             // the header, before its scale is known
 #pragma unroll
             for (int c = 0; c < kI8DecCache; ++c) {
                 const int g = threadIdx.x + c * kI8Threads;
-                if (g < ng) {
-                    const uint2 w = pre[c];
-                    float v[8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        v[i] = __fmul_rn(static_cast<float>(static_cast<int8_t>(w.x >> (8 * i))), scale);
-                        v[4 + i] = __fmul_rn(static_cast<float>(static_cast<int8_t>(w.y >> (8 * i))), scale);
-                    }
-                    o[2 * g] = make_float4(v[0], v[1], v[2], v[3]);
-                    o[2 * g + 1] = make_float4(v[4], v[5], v[6], v[7]);
-                }
+                if (g < ng) put(g, pre[c]);
             }
-            for (int g = threadIdx.x + kI8DecCache * kI8Threads; g < ng; g += kI8Threads) {
-                const uint2 w = __ldg(codes + g);
-                float v[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[i] = __fmul_rn(static_cast<float>(static_cast<int8_t>(w.x >> (8 * i))), scale);
-                    v[4 + i] = __fmul_rn(static_cast<float>(static_cast<int8_t>(w.y >> (8 * i))), scale);
-                }
-                o[2 * g] = make_float4(v[0], v[1], v[2], v[3]);
-                o[2 * g + 1] = make_float4(v[4], v[5], v[6], v[7]);
-            }
+            for (int g = threadIdx.x + kI8DecCache * kI8Threads; g < ng; g += kI8Threads) put(g, __ldg(codes + g));
         } else {
             for (int j = threadIdx.x; j < hidden; j += kI8Threads)
                 xo[j] = __fmul_rn(static_cast<float>(static_cast<int8_t>(__ldg(pos + 8 + j))), scale);
@@ -626,7 +601,7 @@ cudaError_t launch_wire_decode(int fmt, const void *buf, int32_t seq_len, int32_
         return launch_pdl(vec ? decode_i8_kernel<true> : decode_i8_kernel<false>, dim3(grid),
                           dim3(kI8Threads), 0, stream, b, seq_len, hidden, x, err);
     }
-    const int grid = ew_grid(aligned ? (n + 7) / 8 : n, dev.num_sms);
+    const int grid = ew_grid(aligned ? (n + 3) / 4 : n, dev.num_sms);
     const uint32_t s = static_cast<uint32_t>(seq_len);
     void (*kern)(const uint8_t *, int64_t, uint32_t, float *, int32_t *);
     if (fmt == LHS_WIRE_F16) kern = aligned ? decode_ew_kernel<LHS_WIRE_F16, true> : decode_ew_kernel<LHS_WIRE_F16, false>;
