@@ -43,7 +43,22 @@ __global__ void __launch_bounds__(kWarps * 32)
         const bool bad = bad_id(id, vocab);
         if (bad && lane == 0) set_err(err, LHS_ERRBIT_BAD_TOKEN);
         const uint8_t *row = table + static_cast<int64_t>(bad ? 0 : id) * row_bytes;
-        if (VEC) {
+        if (VEC && FMT == LHS_WIRE_F32) {
+            // 4 values per lane step: a warp's stores are whole 32-byte sectors
+            const int n4 = hidden >> 2;
+            for (int s4 = lane; s4 < n4; s4 += 32) {
+                float v[4];
+                if (bad) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = 0.0f;
+                } else {
+                    row_elements4<DT>(row, s4, v);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(v[i], scale);
+                }
+                reinterpret_cast<float4 *>(pay)[t * n4 + s4] = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        } else if (VEC) {
             const int ng = hidden >> 3;
             for (int g = lane; g < ng; g += 32) {
                 float v[8];
@@ -55,13 +70,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], scale);
                 }
-                if (FMT == LHS_WIRE_F32) {
-                    float4 *o = reinterpret_cast<float4 *>(pay) + (t * ng + g) * 2;
-                    o[0] = make_float4(v[0], v[1], v[2], v[3]);
-                    o[1] = make_float4(v[4], v[5], v[6], v[7]);
-                } else {
-                    reinterpret_cast<uint4 *>(pay)[t * ng + g] = pack_f16x8(v);
-                }
+                reinterpret_cast<uint4 *>(pay)[t * ng + g] = pack_f16x8(v);
             }
         } else {
             for (int j = lane; j < hidden; j += 32) {

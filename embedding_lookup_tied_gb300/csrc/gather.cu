@@ -65,25 +65,26 @@ __global__ void __launch_bounds__(kWarps * 32)
                 o4[c] = scale4(v.x, v.y, v.z, v.w, scale);
             }
         } else if (DT == LHS_F16 || DT == LHS_BF16) {
-            const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
-            const int nv = hidden >> 3;
+            // four values per lane step: a warp's 16-byte stores are 512
+            // contiguous bytes (whole 32-byte sectors)
+            const uint2 *r2 = reinterpret_cast<const uint2 *>(row);
+            const int nv = hidden >> 2;
 #pragma unroll 4
             for (int c = lane; c < nv; c += 32) {
-                const uint4 v = __ldg(r4 + c);
-                float e[8];
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (DT == LHS_F16) {
-                        e[2 * i] = f16_bits_to_f32(w[i] & 0xFFFFu);
-                        e[2 * i + 1] = f16_bits_to_f32(w[i] >> 16);
-                    } else {
-                        e[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-                        e[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-                    }
+                const uint2 v = __ldg(r2 + c);
+                float e[4];
+                if (DT == LHS_F16) {
+                    e[0] = f16_bits_to_f32(v.x & 0xFFFFu);
+                    e[1] = f16_bits_to_f32(v.x >> 16);
+                    e[2] = f16_bits_to_f32(v.y & 0xFFFFu);
+                    e[3] = f16_bits_to_f32(v.y >> 16);
+                } else {
+                    e[0] = bf16_bits_to_f32(v.x & 0xFFFFu);
+                    e[1] = bf16_bits_to_f32(v.x >> 16);
+                    e[2] = bf16_bits_to_f32(v.y & 0xFFFFu);
+                    e[3] = bf16_bits_to_f32(v.y >> 16);
                 }
-                o4[2 * c] = scale4(e[0], e[1], e[2], e[3], scale);
-                o4[2 * c + 1] = scale4(e[4], e[5], e[6], e[7], scale);
+                o4[c] = scale4(e[0], e[1], e[2], e[3], scale);
             }
         } else {
             // Q8_0: four outputs j..j+3 (same block) per step; the block's

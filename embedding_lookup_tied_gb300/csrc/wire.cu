@@ -66,19 +66,25 @@ __global__ void __launch_bounds__(kEwThreads)
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (tid == 0) write_wire_header(buf, layer, seq_len, flags, top_k);
     uint8_t *pay = buf + 16;
-    const int64_t ng = VEC ? n / 8 : 0;
+    // f16: 8 values per step (a 16-byte store each); f32: 4 values per step
+    // (a warp's stores are whole 32-byte sectors)
+    const int per = FMT == LHS_WIRE_F16 ? 8 : 4;
+    const int64_t ng = VEC ? n / per : 0;
     for (int64_t g = tid; g < ng; g += nth) {
-        float v[8];
-        load_x8<XDT>(x, g, v);
         if (FMT == LHS_WIRE_F16) {
+            float v[8];
+            load_x8<XDT>(x, g, v);
             reinterpret_cast<uint4 *>(pay)[g] = pack_f16x8(v);
+        } else if (XDT == LHS_F32) {
+            reinterpret_cast<float4 *>(pay)[g] = __ldg(static_cast<const float4 *>(x) + g);
         } else {
-            float4 *p = reinterpret_cast<float4 *>(pay) + 2 * g;
-            p[0] = make_float4(v[0], v[1], v[2], v[3]);
-            p[1] = make_float4(v[4], v[5], v[6], v[7]);
+            const uint2 w = __ldg(static_cast<const uint2 *>(x) + g);
+            reinterpret_cast<float4 *>(pay)[g] =
+                make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                            __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
         }
     }
-    for (int64_t i = ng * 8 + tid; i < n; i += nth) {
+    for (int64_t i = ng * per + tid; i < n; i += nth) {
         const float v = load_x<XDT>(x, i);
         if (FMT == LHS_WIRE_F16)
             reinterpret_cast<unsigned short *>(pay)[i] = static_cast<unsigned short>(f16_sat_bits(v));
