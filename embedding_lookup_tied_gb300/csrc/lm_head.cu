@@ -705,6 +705,30 @@ __device__ __forceinline__ void cta_rows(int64_t V, int G, int c, int64_t &r0, i
     if (r0 > V) r0 = V;
 }
 
+// Blocks of CTA c in the tensor-core GEMV, interleaved over the table: the
+// full 128-row blocks c, c + G, c + 2G, ... of the first q = V / (G * BM)
+// rounds, then CTA c's even share (16-row units) of the rows after them.
+// Every CTA streams the same number of rows give or take 16, drawn from all
+// over the table.
+__device__ __forceinline__ int tc_blocks(int64_t V, int G, int c) {
+    const int64_t q = V / (static_cast<int64_t>(G) * BM);
+    int64_t s0, s1;
+    cta_rows(V - q * G * BM, G, c, s0, s1);
+    return static_cast<int>(q) + (s1 > s0 ? 1 : 0);
+}
+__device__ __forceinline__ void tc_block(int64_t V, int G, int c, int blk, int64_t &row0, int &rows) {
+    const int64_t q = V / (static_cast<int64_t>(G) * BM);
+    if (blk < q) {
+        row0 = (c + static_cast<int64_t>(blk) * G) * BM;
+        rows = BM;
+    } else {
+        int64_t s0, s1;
+        cta_rows(V - q * G * BM, G, c, s0, s1);
+        row0 = q * G * BM + s0;
+        rows = static_cast<int>(s1 - s0);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // residual operand prep: x[b][k] (f32 or bf16) -> 16 x Kp rows of the
 // table's 16-bit type: rows 0..7 = hi, rows 8..15 = lo (zero padded)
@@ -820,9 +844,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     while (q < p.Bc) q <<= 1;
     const int cap = kCandTotal / q;  // candidate slots per residual
 
-    int64_t r0, r1;
-    cta_rows(p.V, gridDim.x, blockIdx.x, r0, r1);
-    const int nblk = static_cast<int>((r1 - r0 + BM - 1) / BM);
+    const int nblk = tc_blocks(p.V, gridDim.x, blockIdx.x);
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -843,13 +865,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_prefetch_map(&tm_x);
             const uint32_t total = static_cast<uint32_t>(nblk) * p.nk;
             auto block_rows = [&](int blk) {
-                const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
-                return static_cast<int>((r1 - row0) < BM ? (r1 - row0) : BM);
+                int64_t row0;
+                int rows;
+                tc_block(p.V, gridDim.x, blockIdx.x, blk, row0, rows);
+                return rows;
             };
             auto issue_a = [&](uint32_t j) {
                 const int blk = j / p.nk, kc = j % p.nk, s = j % kStages;
-                const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
-                const int rows = block_rows(blk);
+                int64_t row0;
+                int rows;
+                tc_block(p.V, gridDim.x, blockIdx.x, blk, row0, rows);
                 if (rows == BM) {
                     tma_load_2d(sm.a[s], &tm_a, &sm.full[s], kc * BK, static_cast<int32_t>(row0));
                 } else {
@@ -950,8 +975,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     uint32_t it = 0;
     for (int blk = 0; blk < nblk; ++blk) {
-        const int64_t row0 = r0 + static_cast<int64_t>(blk) * BM;
-        const int rows = static_cast<int>((r1 - row0) < BM ? (r1 - row0) : BM);
+        int64_t row0;
+        int rows;
+        tc_block(p.V, gridDim.x, blockIdx.x, blk, row0, rows);
         const bool active = warp * 16 < rows;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int kc = 0; kc < p.nk; ++kc, ++it) {
@@ -986,7 +1012,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int64_t v = row0 + warp * 16 + g + 8 * r;
-                if (v < r1) {
+                if (v < row0 + rows) {
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const int b = 2 * t + c;
