@@ -458,6 +458,7 @@ __device__ void merge_column(const uint64_t *part_keys, const float2 *part_ms, i
 // in L2 instead (merge_extract_warp): slower, same result.
 // ---------------------------------------------------------------------------
 constexpr int kMergeThreads = 256;             // >= G
+static_assert(kMergeThreads == 256, "one histogram bin per merge thread");
 constexpr int kMergeR = 16;                    // most entries staged per list
 constexpr int kMergeSet = 2 * kMergeThreads;   // G*m <= G + k - 1 < 512
 constexpr int kMergeCand = 1024;
@@ -465,8 +466,10 @@ constexpr int kMergeCand = 1024;
 struct MergeWork {
     uint64_t cand[kMergeCand];
     uint32_t set[kMergeSet];
+    unsigned hist[256];  // the sampled keys' histogram (zeroed with lo / hi before the merge)
     float ssum[kMergeThreads / 32];
     uint32_t bound;
+    uint32_t lo, hi;     // range of the nonzero sampled keys
     int total;
     float2 msf;
 };
@@ -587,9 +590,24 @@ __device__ void merge_column_sorted(const uint64_t *lists, int R, const float2 *
         w.bound = 0u;
         w.total = 0;
     }
+    unsigned vlo = 0xFFFFFFFFu, vhi = 0u;
     for (int i = tid; i < na4; i += kMergeThreads) {
         const int gi = m == 1 ? i : i / m;
-        w.set[i] = i < na ? static_cast<uint32_t>(lists[gi * R + (i - gi * m)] >> 32) : 0u;
+        const uint32_t v = i < na ? static_cast<uint32_t>(lists[gi * R + (i - gi * m)] >> 32) : 0u;
+        w.set[i] = v;
+        if (v != 0u) {
+            vlo = min(vlo, v);
+            vhi = max(vhi, v);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        vlo = min(vlo, __shfl_xor_sync(0xFFFFFFFFu, vlo, o));
+        vhi = max(vhi, __shfl_xor_sync(0xFFFFFFFFu, vhi, o));
+    }
+    if (lane == 0 && vlo <= vhi) {
+        atomicMin(&w.lo, vlo);
+        atomicMax(&w.hi, vhi);
     }
     named_bar_sync(bar_id, kMergeThreads);
     // (max, sum) over the lists, max first: the G rescalings are then
@@ -601,21 +619,44 @@ __device__ void merge_column_sorted(const uint64_t *lists, int R, const float2 *
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
         if (lane == 0) w.msf.x = mx;
     }
-    // 2. the bound: the k-th largest sampled order key (ties allowed); the
-    //    ms warp joins only when the sample needs every thread
-    const uint4 *set4 = reinterpret_cast<const uint4 *>(w.set);
-    const int nw4 = na4 / 4;
+    // 2. the bound: the lower edge of the bin, in a 256-bin histogram of the
+    //    nonzero sampled order keys over their range, that holds the k-th
+    //    largest — at least k sampled keys (so at least k keys) are >= it.
+    //    Fewer than k nonzero samples leave the bound at 0.
     {
+        const uint32_t lo = w.lo, range = w.hi - lo;
+        const int sh = w.lo > w.hi ? 0 : (range < 256u ? 0 : 24 - __clz(range));  // (range >> sh) < 256
         for (int i = tid; i < na; i += kMergeThreads) {
-            const uint32_t x = w.set[i];
-            int gt = 0, ge = 0;
-#pragma unroll 4
-            for (int q = 0; q < nw4; ++q) {
-                const uint4 y = set4[q];
-                gt += (y.x > x) + (y.y > x) + (y.z > x) + (y.w > x);
-                ge += (y.x >= x) + (y.y >= x) + (y.z >= x) + (y.w >= x);
+            const uint32_t v = w.set[i];
+            if (v != 0u) atomicAdd(&w.hist[(v - lo) >> sh], 1u);
+        }
+        named_bar_sync(bar_id, kMergeThreads);
+        if (warp == 0) {  // lane L owns bins 255-8L ... 248-8L, highest first
+            unsigned c[8];
+            unsigned lsum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c[i] = w.hist[255 - 8 * lane - i];
+                lsum += c[i];
             }
-            if (gt < k && ge >= k) w.bound = x;
+            unsigned incl = lsum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const unsigned excl = incl - lsum;
+            if (excl < static_cast<unsigned>(k) && static_cast<unsigned>(k) <= incl) {
+                unsigned run = excl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (run + c[i] >= static_cast<unsigned>(k)) {
+                        w.bound = lo + (static_cast<uint32_t>(255 - 8 * lane - i) << sh);
+                        break;
+                    }
+                    run += c[i];
+                }
+            }
         }
     }
     named_bar_sync(bar_id, kMergeThreads);
@@ -1660,6 +1701,11 @@ __global__ void __launch_bounds__(kMergeThreads)
     extern __shared__ uint64_t lists[];  // [G][R], then G float2
     float2 *sms = reinterpret_cast<float2 *>(lists + G * R);
     pdl_trigger();
+    w.hist[threadIdx.x] = 0u;  // kMergeThreads == 256 bins
+    if (threadIdx.x == 0) {
+        w.lo = 0xFFFFFFFFu;
+        w.hi = 0u;
+    }
     pdl_wait();
     stage_sorted_lists(part_keys, part_ms, G, k, R, batch_total, blockIdx.x, lists, sms, threadIdx.x,
                        kMergeThreads);
