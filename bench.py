@@ -415,47 +415,70 @@ def time_device(c, steps, warmup, world):
 
 def time_e2e(c, steps):
     """Same step through the public binding with HOST buffers: each step
-    copies its inputs from pinned host memory and reads its results back."""
+    copies its inputs from pinned host memory and reads its results back.
+    The step's inputs and outputs share one device buffer (and one pinned
+    host mirror) laid out [ids | residuals | error word | lm_head outputs |
+    wire message | embeddings], so a step is one host-to-device copy (ids,
+    residuals and the zeroed error word), the calls, and one device-to-host
+    copy (the error word and every output), all on the stream of the calls.
+    (Copying the embeddings on a second stream, overlapped with the
+    lm_head, measured slower: the per-step cross-stream waits cost more.)"""
     import torch
     lhs = c.lhs
-    h_ids = torch.from_numpy(c.ids_host.copy()).pin_memory()
+    dev = c.ids.device
+    rd_t = torch.bfloat16 if c.w.resid_dtype == wl.BF16 else torch.float32
+    relt = 2 if c.w.resid_dtype == wl.BF16 else 4
+    H = c.w.hidden
+    parts = [("ids", c.n_ids * 4), ("res", c.B * H * relt), ("err", 4)]
+    if c.raw:
+        parts.append(("raw", c.B * c.w.vocab * 4))
+    else:
+        parts += [("tid", c.B * c.k * 4), ("tlg", c.B * c.k * 4), ("tpr", c.B * c.k * 4)]
+    parts += [("buf", c.wire_bytes), ("emb", c.n_ids * H * 4)]
+    off, pos = {}, 0
+    for name, nb in parts:
+        off[name] = pos
+        pos = (pos + nb + 255) // 256 * 256
+    total = pos
+    d_io = torch.empty(total, dtype=torch.uint8, device=dev)
+    h_io = torch.empty(total, dtype=torch.uint8).pin_memory()
+
+    def view(t, name, nb, dtype, shape):
+        return t[off[name]:off[name] + nb].view(dtype).view(shape)
+
+    # inputs and the zeroed error word, in the host mirror
+    view(h_io, "ids", c.n_ids * 4, torch.int32, (c.n_ids,)).copy_(torch.from_numpy(c.ids_host.copy()))
     rh = c.R_host.view(np.int16) if c.R_host.dtype == np.uint16 else c.R_host
-    h_res = torch.from_numpy(np.ascontiguousarray(rh)).pin_memory()
-    if c.w.resid_dtype == wl.BF16:
-        h_res = h_res.view(torch.bfloat16)
-    h_emb = torch.empty(c.emb_out.shape, dtype=torch.float32).pin_memory()
-    h_raw = torch.empty(c.raw_out.shape, dtype=torch.float32).pin_memory() if c.raw else None
-    h_tid = torch.empty(c.top_ids.shape, dtype=torch.int32).pin_memory()
-    h_tlg = torch.empty(c.top_logits.shape, dtype=torch.float32).pin_memory()
-    h_tpr = torch.empty(c.top_probs.shape, dtype=torch.float32).pin_memory()
-    h_buf = torch.empty(c.wire_buf.shape, dtype=torch.uint8).pin_memory()
-    h_err = torch.empty(1, dtype=torch.int32).pin_memory()
-    d_ids = torch.empty_like(c.ids)
-    d_res = torch.empty_like(c.resid)
-    h2d = h_ids.numel() * 4 + h_res.numel() * h_res.element_size()
-    lm_out = h_raw.numel() * 4 if c.raw else h_tid.numel() * 4 + h_tlg.numel() * 4 + h_tpr.numel() * 4
-    d2h = h_emb.numel() * 4 + lm_out + h_buf.numel() + 4
+    hr = torch.from_numpy(np.ascontiguousarray(rh))
+    view(h_io, "res", c.B * H * relt, hr.dtype, (c.B, H)).copy_(hr)
+    view(h_io, "err", 4, torch.int32, (1,)).zero_()
+    d_ids = view(d_io, "ids", c.n_ids * 4, torch.int32, (c.n_ids,))
+    d_res = view(d_io, "res", c.B * H * relt, rd_t, (c.B, H))
+    d_err = view(d_io, "err", 4, torch.int32, (1,))
+    d_emb = view(d_io, "emb", c.n_ids * H * 4, torch.float32, (c.n_ids, H))
+    d_buf = view(d_io, "buf", c.wire_bytes, torch.uint8, (c.wire_bytes,))
+    if c.raw:
+        d_raw = view(d_io, "raw", c.B * c.w.vocab * 4, torch.float32, (c.B, c.w.vocab))
+    else:
+        d_tid = view(d_io, "tid", c.B * c.k * 4, torch.int32, (c.B, c.k))
+        d_tlg = view(d_io, "tlg", c.B * c.k * 4, torch.float32, (c.B, c.k))
+        d_tpr = view(d_io, "tpr", c.B * c.k * 4, torch.float32, (c.B, c.k))
+    in_end = off["err"] + 4              # ids, residuals, error word
+    out0 = off["err"]                    # error word and every output
+    out1 = off["emb"] + c.n_ids * H * 4
+    h2d = in_end
+    d2h = out1 - out0
 
     def one():
-        d_ids.copy_(h_ids, non_blocking=True)
-        d_res.copy_(h_res, non_blocking=True)
-        c.err.zero_()
-        lhs.lhs_embed(c.table, d_ids, c.scale, out=c.emb_out, err=c.err)
+        d_io[:in_end].copy_(h_io[:in_end], non_blocking=True)
+        lhs.lhs_embed(c.table, d_ids, c.scale, out=d_emb, err=d_err)
         if c.raw:
-            lhs.lhs_logits(c.lm_table, d_res, out=c.raw_out, ws=c.ws, err=c.err)
+            lhs.lhs_logits(c.lm_table, d_res, out=d_raw, ws=c.ws, err=d_err)
         else:
-            lhs.lhs_logits_topk(c.lm_table, d_res, c.k, 1.0, ws=c.ws, ids=c.top_ids,
-                                logits=c.top_logits, probs=c.top_probs, err=c.err)
-        lhs.lhs_wire_encode(c.fmt, d_res, 0, 0, c.k, buf=c.wire_buf, err=c.err)
-        h_emb.copy_(c.emb_out, non_blocking=True)
-        if c.raw:
-            h_raw.copy_(c.raw_out, non_blocking=True)
-        else:
-            h_tid.copy_(c.top_ids, non_blocking=True)
-            h_tlg.copy_(c.top_logits, non_blocking=True)
-            h_tpr.copy_(c.top_probs, non_blocking=True)
-        h_buf.copy_(c.wire_buf, non_blocking=True)
-        h_err.copy_(c.err, non_blocking=True)
+            lhs.lhs_logits_topk(c.lm_table, d_res, c.k, 1.0, ws=c.ws, ids=d_tid, logits=d_tlg, probs=d_tpr,
+                                err=d_err)
+        lhs.lhs_wire_encode(c.fmt, d_res, 0, 0, c.k, buf=d_buf, err=d_err)
+        h_io[out0:out1].copy_(d_io[out0:out1], non_blocking=True)
 
     for _ in range(5):
         one()
@@ -467,7 +490,7 @@ def time_e2e(c, steps):
         one()
     e1.record(c.stream)
     e1.synchronize()
-    if int(h_err.item()) != 0:
+    if int(view(h_io, "err", 4, torch.int32, (1,)).item()) != 0:
         raise RuntimeError("error word set in the end-to-end loop")
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
