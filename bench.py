@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--untied", action="store_true",
                     help="lm_head on a second table of the same shape (an untied lm_head)")
+    ap.add_argument("--e2e-eager", action="store_true",
+                    help="time the end-to-end step as eager calls instead of replaying it as a CUDA graph")
     ap.add_argument("--raw-logits", action="store_true",
                     help="the step's lm_head call returns the full logits (raw-logits mode)")
     ap.add_argument("--wire-accuracy", action="store_true",
@@ -413,7 +415,7 @@ def time_device(c, steps, warmup, world):
     return ms, lm_ms, ck
 
 
-def time_e2e(c, steps):
+def time_e2e(c, steps, graph=False):
     """Same step through the public binding with HOST buffers: each step
     copies its inputs from pinned host memory and reads its results back.
     The step's inputs and outputs share one device buffer (and one pinned
@@ -422,7 +424,9 @@ def time_e2e(c, steps):
     residuals and the zeroed error word), the calls, and one device-to-host
     copy (the error word and every output), all on the stream of the calls.
     (Copying the embeddings on a second stream, overlapped with the
-    lm_head, measured slower: the per-step cross-stream waits cost more.)"""
+    lm_head, measured slower: the per-step cross-stream waits cost more.)
+    graph=True captures one step — copies and calls — in a CUDA graph and
+    replays it, so the host's per-call launch cost leaves the loop."""
     import torch
     lhs = c.lhs
     dev = c.ids.device
@@ -483,11 +487,21 @@ def time_e2e(c, steps):
     for _ in range(5):
         one()
     torch.cuda.synchronize()
+    step = one
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one()
+        torch.cuda.synchronize()
+        step = g.replay
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(c.stream)
     for _ in range(steps):
-        one()
+        step()
     e1.record(c.stream)
     e1.synchronize()
     if int(view(h_io, "err", 4, torch.int32, (1,)).item()) != 0:
@@ -738,7 +752,8 @@ def main():
     ms, lm_ms, clocks = time_device(c, steps, max(3, args.warmup), world)
     ms = max_over_ranks(ms, world, dev)
     e2e_steps = max(20, min(steps // 10, 2000))
-    e2e_ms, h2d, d2h = time_e2e(c, e2e_steps)
+    e2e_graph = not args.e2e_eager
+    e2e_ms, h2d, d2h = time_e2e(c, e2e_steps, graph=e2e_graph)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     peak, peak_kind, _ = load_peaks()
     value = world * c.B / (ms / 1e3)
@@ -765,7 +780,9 @@ def main():
         "clocks": clocks,
         "e2e": {"value": world * c.B / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms,
+                "launch": ("one CUDA graph per step (the copies and the calls, captured once)" if e2e_graph
+                           else "eager calls")},
     }
     if c.gemm:
         # a dense contraction near the ridge point: its tensor-core fraction too
