@@ -42,14 +42,14 @@ namespace {
 // ---------------------------------------------------------------------------
 constexpr int BM = 128;                   // table rows per block
 constexpr int BK = 64;                    // k per stage: 128 bytes of 16-bit values
-constexpr int kStages = 8;
+constexpr int kStages = 10;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kTcThreads = kConsumers + 32;  // + one producer warp
 constexpr int kAStageBytes = BM * BK * 2;    // 16 KB
 constexpr int kXStageBytes = 16 * BK * 2;    // 2 KB: 8 hi rows + 8 lo rows
 constexpr int kBoxRowsSmall = 16;            // TMA box for the ragged last block
-constexpr int kCandTotal = 4096;             // candidate keys per CTA (all residuals)
+constexpr int kCandTotal = 2048;             // candidate keys per CTA (all residuals)
 constexpr int kBatchChunk = 8;               // residuals per projection pass
 constexpr int kBarAll = 15;                  // named barrier: all consumers (groups use 1..8)
 constexpr int kMaxConsumerWarps = 16;        // largest consumer group of the top-k state
