@@ -510,6 +510,7 @@ struct LmHeadPlan {
     int key_stride;    // entries between consecutive partial lists
     bool sample;       // GEMM: run the sample pass
     bool xres;         // tensor-core GEMV: residual operand resident in shared memory (no prep kernel)
+    int nst;           // tensor-core GEMV: TMA ring stages
     size_t bytes;      // total workspace
 };
 int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dtype,

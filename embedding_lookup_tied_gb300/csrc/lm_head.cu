@@ -42,7 +42,12 @@ namespace {
 // ---------------------------------------------------------------------------
 constexpr int BM = 128;                   // table rows per block
 constexpr int BK = 64;                    // k per stage: 128 bytes of 16-bit values
-constexpr int kStages = 10;
+// TMA ring depth of the tensor-core GEMV: as deep as shared memory allows
+// next to the residual operand (a consumer stall stops the refills; stages
+// in flight beyond the bandwidth-delay product absorb it)
+constexpr int kStagesRing = 11;       // residual tiles streamed beside the table tiles
+constexpr int kStagesResident = 10;   // all 16 residual rows resident
+constexpr int kStagesCompact = 12;    // at most 3 residuals: 2 Bc + 1 rows resident
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kTcThreads = kConsumers + 32;  // + one producer warp
@@ -60,10 +65,15 @@ constexpr int kSimtThreads = 256;
 // ---------------------------------------------------------------------------
 struct TopkShared {
     uint64_t cand[kCandTotal];
-    uint64_t scratch[kBatchChunk][kMaxK];
+    // Column c's radix-select histogram and its scratch keys share bytes:
+    // the select has finished with hist[c] (behind a group barrier) before
+    // scratch[c] is written, and nothing reads hist[c] after that.
+    union {
+        uint64_t scratch[kBatchChunk][kMaxK];
+        unsigned hist[kBatchChunk][256];
+    };
     uint64_t tau[kBatchChunk];
     uint64_t tmin[kBatchChunk];
-    unsigned hist[kBatchChunk][256];
     float2 ms_warp[kMaxConsumerWarps][kBatchChunk];
     int cnt[kBatchChunk];
     int nsel[kBatchChunk];
@@ -72,6 +82,8 @@ struct TopkShared {
     int need_compact;
     int abort_flag;
 };
+
+static_assert(sizeof(uint64_t) * kMaxK == sizeof(unsigned) * 256, "a column's hist and scratch coincide");
 
 __device__ __forceinline__ int ld_volatile(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
 
@@ -829,20 +841,36 @@ struct TcParams {
     int32_t *err;
 };
 
-// Shared memory of the tensor-core GEMV: the table-tile ring, barriers and
-// top-k state, then (at the next 1 KB boundary) the residual operand: a ring
-// of TMA tiles [kStages][16 x 64], or — when it fits — the whole operand
-// [Kpad / 64][16 x 64] resident, written by the consumers themselves.  Both
-// use the TMA 128-byte swizzle: within a 16 x 128-byte tile, row r's 16-byte
-// chunk c sits at r * 128 + ((c ^ (r & 7)) << 4).
-struct TcSmem {
-    uint8_t a[kStages][kAStageBytes];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+// Shared memory of the tensor-core GEMV: the table-tile ring of NST stages,
+// barriers and top-k state, then (at the next 1 KB boundary) the residual
+// operand: a ring of TMA tiles [NST][16 x 64], or — when it fits — the whole
+// operand resident, Kpad / 64 tiles of xres_rows(Bc) rows x 128 bytes,
+// written by the consumers themselves.  Both use the TMA 128-byte swizzle:
+// within a tile, row r's 16-byte chunk c sits at r * 128 + ((c ^ (r & 7)) << 4).
+// The mma reads 16 operand rows per tile, the hi rows of the 8 batch slots
+// and then their lo rows.  With at most 3 residuals the resident operand
+// keeps only the used ones (hi rows 0 .. Bc-1, lo rows Bc .. 2Bc-1) and one
+// zero row, 2 Bc, that every unused slot reads: the rows one 8-row ldmatrix
+// reads then have distinct residues mod 8, so no bank conflicts.  From 4
+// residuals on it keeps all 16 rows (zeros beyond Bc).
+template <int NST>
+struct TcSmemT {
+    uint8_t a[NST][kAStageBytes];
+    uint64_t full[NST];
+    uint64_t empty[NST];
     TopkShared tk;
 };
-constexpr size_t kTcXOffset = (sizeof(TcSmem) + 1023) & ~size_t(1023);
-constexpr size_t kTcXRingBytes = static_cast<size_t>(kStages) * kXStageBytes;
+template <int NST>
+__host__ __device__ constexpr size_t tc_x_offset() { return (sizeof(TcSmemT<NST>) + 1023) & ~size_t(1023); }
+
+__host__ __device__ __forceinline__ int xres_rows(int Bc) { return Bc <= 3 ? 2 * Bc + 1 : 16; }
+// resident row of operand row r (r < 8: hi row of batch slot r; else the lo
+// row of slot r - 8)
+__device__ __forceinline__ int xres_row(int r, int Bc) {
+    if (Bc > 3) return r;
+    const int b = r & 7;
+    return b < Bc ? (r < 8 ? b : Bc + b) : 2 * Bc;
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
@@ -871,14 +899,14 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 // XRES: the residual operand is resident in shared memory, built by the
 // consumers from the residuals (what prep_kernel does otherwise), so the pass
 // is one launch and the producer never waits for an earlier kernel.
-template <bool BF16T, bool RAW, bool XRES>
+template <bool BF16T, bool RAW, bool XRES, int NST>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a16,
                    const __grid_constant__ CUtensorMap tm_x, const TcParams p) {
     extern __shared__ uint8_t dyn_smem[];
-    TcSmem &sm = *reinterpret_cast<TcSmem *>(
+    TcSmemT<NST> &sm = *reinterpret_cast<TcSmemT<NST> *>(
         (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *xsm = reinterpret_cast<uint8_t *>(&sm) + kTcXOffset;
+    uint8_t *xsm = reinterpret_cast<uint8_t *>(&sm) + tc_x_offset<NST>();
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     int q = 1;
@@ -888,7 +916,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nblk = tc_blocks(p.V, gridDim.x, blockIdx.x);
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kConsumerWarps);
         }
@@ -912,7 +940,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 return rows;
             };
             auto issue_a = [&](uint32_t j) {
-                const int blk = j / p.nk, kc = j % p.nk, s = j % kStages;
+                const int blk = j / p.nk, kc = j % p.nk, s = j % NST;
                 int64_t row0;
                 int rows;
                 tc_block(p.V, gridDim.x, blockIdx.x, blk, row0, rows);
@@ -934,7 +962,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // The table is never written by an earlier kernel, so the first
             // ring's worth of table tiles is requested before waiting for the
             // residual operand the preceding kernel prepares.
-            const uint32_t pre = total < kStages ? total : kStages;
+            const uint32_t pre = total < NST ? total : NST;
             for (uint32_t j = 0; j < pre; ++j) {
                 mbar_arrive_expect_tx(&sm.full[j], stage_bytes(j));
                 issue_a(j);
@@ -946,8 +974,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             uint32_t it = pre;
             for (; it < total; ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
+                const int s = it % NST;
+                const uint32_t ph = (it / NST) & 1;
                 if (!mbar_wait(&sm.empty[s], ph ^ 1, kWaitTimeoutNs)) {
                     // consumers stopped releasing slots; they record their
                     // own timeout and leave together
@@ -961,9 +989,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // drain: every issued stage must land before the CTA exits
             const uint32_t issued = it;
-            for (uint32_t j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
-                const int s = j % kStages;
-                if (!mbar_wait(&sm.full[s], (j / kStages) & 1, kWaitTimeoutNs)) {
+            for (uint32_t j = (issued > NST ? issued - NST : 0); j < issued; ++j) {
+                const int s = j % NST;
+                if (!mbar_wait(&sm.full[s], (j / NST) & 1, kWaitTimeoutNs)) {
                     set_err(p.err, LHS_ERRBIT_TIMEOUT);
                     break;
                 }
@@ -976,16 +1004,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int g = lane >> 2, t = lane & 3;
     const int a_row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int a_csel = lane >> 4;
-    const int x_row = (lane & 7) + ((lane >> 4) << 3);
+    const int x_row = XRES ? xres_row((lane & 7) + ((lane >> 4) << 3), p.Bc) : (lane & 7) + ((lane >> 4) << 3);
     const int x_csel = (lane >> 3) & 1;
+    const uint32_t x_tile = XRES ? static_cast<uint32_t>(xres_rows(p.Bc)) * 128u : static_cast<uint32_t>(kXStageBytes);
     float m_st[2] = {-INFINITY, -INFINITY}, s_st[2] = {0.0f, 0.0f};
     if (XRES) {
         // the residuals may come from the previous kernel, and the partial
         // lists written below may still be read by it
         pdl_wait();
         const int Kp = p.nk * BK;
+        const bool compact = p.Bc <= 3;
+        const int xtile = xres_rows(p.Bc) * 128;
         int bad = 0;
-        for (int b = 0; b < 8; ++b) {
+        for (int b = 0; b < (compact ? p.Bc : 8); ++b) {
+            const int rh = b, rl = compact ? p.Bc + b : 8 + b;  // resident rows of slot b (hi, lo)
             for (int kk = tid; kk < Kp; kk += kConsumers) {
                 float v = 0.0f;
                 if (b < p.Bc && kk < p.K) {
@@ -1004,12 +1036,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     hi = __half_as_ushort(h);
                     lo = __half_as_ushort(__float2half_rn(v - __half2float(h)));
                 }
-                // rows b (hi) and 8 + b (lo) of tile kk / 64; both rows have r & 7 == b
+                // rows rh and rl of tile kk / 64
                 const int e = kk & (BK - 1);
-                uint8_t *cell = xsm + (kk / BK) * kXStageBytes + ((((e >> 3) ^ b) << 4) | ((e & 7) * 2));
-                *reinterpret_cast<uint16_t *>(cell + b * 128) = hi;
-                *reinterpret_cast<uint16_t *>(cell + (8 + b) * 128) = lo;
+                uint8_t *tile = xsm + (kk / BK) * xtile;
+                *reinterpret_cast<uint16_t *>(tile + rh * 128 + ((((e >> 3) ^ (rh & 7)) << 4) | ((e & 7) * 2))) = hi;
+                *reinterpret_cast<uint16_t *>(tile + rl * 128 + ((((e >> 3) ^ (rl & 7)) << 4) | ((e & 7) * 2))) = lo;
             }
+        }
+        if (compact) {
+            // the zero row that the unused batch slots read
+            for (int i = tid; i < p.nk * 8; i += kConsumers)
+                *reinterpret_cast<uint4 *>(xsm + (i >> 3) * xtile + 2 * p.Bc * 128 + (i & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
         }
         if (bad && p.Bc > 0) set_err(p.err, LHS_ERRBIT_NONFINITE);
         named_bar_sync(kBarAll, kConsumers);
@@ -1022,8 +1060,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool active = warp * 16 < rows;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int kc = 0; kc < p.nk; ++kc, ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (it / kStages) & 1;
+            const int s = it % NST;
+            const uint32_t ph = (it / NST) & 1;
             if (!ld_volatile(&sm.tk.abort_flag)) {
                 if (!mbar_wait(&sm.full[s], ph, kWaitTimeoutNs)) {
                     if (lane == 0) {
@@ -1032,7 +1070,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 } else if (active) {
                     const uint32_t abase = smem_u32(sm.a[s]);
-                    const uint32_t xbase = smem_u32(xsm + (XRES ? kc : s) * kXStageBytes);
+                    const uint32_t xbase = smem_u32(xsm) + static_cast<uint32_t>(XRES ? kc : s) * x_tile;
 #pragma unroll
                     for (int ks = 0; ks < BK / 16; ++ks) {
                         const int ca = 2 * ks + a_csel;
@@ -1752,9 +1790,14 @@ bool make_tma_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint6
 
 namespace {
 
-// dynamic shared memory of the tensor-core GEMV: alignment slack + layout
-size_t tc_smem_bytes(bool xres, int kpad) {
-    return 1024 + kTcXOffset + (xres ? static_cast<size_t>(kpad) * 32 : kTcXRingBytes);
+// dynamic shared memory of the tensor-core GEMV with nst stages and passes
+// of up to bc residuals: alignment slack + layout
+size_t tc_smem_bytes(bool xres, int kpad, int nst, int bc) {
+    const size_t x_off = nst == kStagesCompact ? tc_x_offset<kStagesCompact>()
+                         : nst == kStagesRing  ? tc_x_offset<kStagesRing>()
+                                               : tc_x_offset<kStagesResident>();
+    return 1024 + x_off +
+           (xres ? static_cast<size_t>(kpad / BK) * xres_rows(bc) * 128 : static_cast<size_t>(nst) * kXStageBytes);
 }
 constexpr size_t kSimtXBytesMax = 96 * 1024;
 
@@ -1812,8 +1855,19 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
         p.batch_chunk = kBatchChunk;
     } else if (tc) {
         p.batch_chunk = kBatchChunk;
-        p.xres = tc_smem_bytes(true, p.kpad) <= static_cast<size_t>(dev.max_smem_optin);
-        if (tc_smem_bytes(p.xres, p.kpad) > static_cast<size_t>(dev.max_smem_optin)) return LHS_ERR_UNSUPPORTED;
+        // the deepest ring that fits: the resident operand (compact for up
+        // to 3 residuals) if it fits beside 10 stages or more, else the
+        // operand streamed beside the table
+        const int bc = batch < 1 ? 1 : (batch < kBatchChunk ? batch : kBatchChunk);
+        const size_t lim = static_cast<size_t>(dev.max_smem_optin);
+        p.xres = true;
+        p.nst = xres_rows(bc) < 16 ? kStagesCompact : kStagesResident;
+        if (tc_smem_bytes(true, p.kpad, p.nst, bc) > lim) p.nst = kStagesResident;
+        if (tc_smem_bytes(true, p.kpad, p.nst, bc) > lim) {
+            p.xres = false;
+            p.nst = kStagesRing;
+        }
+        if (tc_smem_bytes(p.xres, p.kpad, p.nst, bc) > lim) return LHS_ERR_UNSUPPORTED;
     } else {
         int bc = static_cast<int>(kSimtXBytesMax / (static_cast<size_t>(t.hidden) * 4));
         if (bc > kBatchChunk) bc = kBatchChunk;
@@ -1909,18 +1963,23 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             !make_tma_map_16bit(&tm_x, xs, plan.kpad, 16, static_cast<uint64_t>(plan.kpad) * 2, BK, 16, bf16))
             return cudaErrorInvalidValue;
         using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams);
-        static const TcKernel kTable[2][2][2] = {
-            {{gemv_tc_kernel<false, false, false>, gemv_tc_kernel<false, false, true>},
-             {gemv_tc_kernel<false, true, false>, gemv_tc_kernel<false, true, true>}},
-            {{gemv_tc_kernel<true, false, false>, gemv_tc_kernel<true, false, true>},
-             {gemv_tc_kernel<true, true, false>, gemv_tc_kernel<true, true, true>}}};
-        const TcKernel kern = kTable[bf16][raw][plan.xres];
-        const size_t smem = tc_smem_bytes(plan.xres, plan.kpad);
+        // variants: operand streamed (kStagesRing), resident (kStagesResident
+        // or, compact, kStagesCompact)
+#define LHS_TC(BF, R)                                                                              \
+    {gemv_tc_kernel<BF, R, false, kStagesRing>, gemv_tc_kernel<BF, R, true, kStagesResident>, \
+     gemv_tc_kernel<BF, R, true, kStagesCompact>}
+        static const TcKernel kTable[2][2][3] = {{LHS_TC(false, false), LHS_TC(false, true)},
+                                                 {LHS_TC(true, false), LHS_TC(true, true)}};
+#undef LHS_TC
+        const int variant = !plan.xres ? 0 : (plan.nst == kStagesCompact ? 2 : 1);
+        const TcKernel kern = kTable[bf16][raw][variant];
+        const size_t smem = tc_smem_bytes(plan.xres, plan.kpad, plan.nst,
+                                          batch < plan.batch_chunk ? batch : plan.batch_chunk);
         {
             // one attribute flag per instantiation: the largest size this device allows
             static std::mutex mu;
-            static bool done[8][64] = {};
-            const int which = (bf16 ? 4 : 0) + (raw ? 2 : 0) + (plan.xres ? 1 : 0);
+            static bool done[12][64] = {};
+            const int which = (bf16 ? 6 : 0) + (raw ? 3 : 0) + variant;
             std::lock_guard<std::mutex> lock(mu);
             if (!done[which][dev.device]) {
                 e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);

@@ -280,8 +280,10 @@ LM_CASES = [
     (orc.BF16, 5000, 128, 2, 128, orc.F32),   # k = kMax over every SM: lists deeper than staged
     (orc.BF16, 20000, 64, 8, 50, orc.F32),    # one full pass, 8 residuals
     (orc.F16, 20000, 64, 12, 50, orc.F32),    # two passes
-    (orc.F16, 3000, 2048, 3, 10, orc.F32),    # operand too large to keep resident: prep + TMA tiles
-    (orc.BF16, 2000, 1504, 2, 7, orc.BF16),   # largest resident operand, hidden % 64 != 0
+    (orc.F16, 3000, 2048, 3, 10, orc.F32),    # 3 residuals: only their rows (+ a zero row) resident
+    (orc.F16, 3000, 2048, 4, 10, orc.F32),    # 16 operand rows too large to keep resident: prep + TMA tiles
+    (orc.BF16, 2000, 1504, 2, 7, orc.BF16),   # compact resident operand, hidden % 64 != 0
+    (orc.BF16, 2000, 1272, 5, 7, orc.BF16),   # largest 16-row resident operand, hidden % 64 != 0
     (orc.BF16, 128, 64, 2, 1, orc.F32),       # one block, k = 1
     (orc.F32, 1000, 256, 4, 5, orc.F32),      # bulk-stream CUDA-core path (1 KB rows)
     (orc.Q8_0, 700, 128, 2, 10, orc.F32),     # CUDA-core path (136-byte rows)
@@ -374,10 +376,12 @@ def test_launch_count_follows_the_plan():
     assert n(8, 128, lhs.LHS_BF16) == 2
     assert n(9, 10, lhs.LHS_F32) == 3                      # two passes + merge
     assert n(3, 0, lhs.LHS_F32) == 1                       # raw logits: no merge
-    # hidden 4096: operand tiles streamed by TMA after a prep kernel
+    # hidden 4096: up to 3 residuals keep only their rows resident; from 4 on
+    # the operand tiles are streamed by TMA after a prep kernel
     T4 = wl.make_table(orc.F16, 512, 4096, 0.02, cid=252, threads=4)
     tab4 = upload_table(T4, orc.F16, 512, 4096)
-    assert lhs.lhs_logits_topk_launches(tab4, 1, 10, lhs.LHS_F32) == 3
+    assert lhs.lhs_logits_topk_launches(tab4, 1, 10, lhs.LHS_F32) == 2
+    assert lhs.lhs_logits_topk_launches(tab4, 4, 10, lhs.LHS_F32) == 3
     assert n(64, 10, lhs.LHS_BF16) in (2, 4)               # GEMM (+ sample pass and its merge)
     assert n(64, 0, lhs.LHS_BF16) == 1
     T32 = wl.make_table(orc.F32, 1000, 64, 0.02, cid=251, threads=4)
