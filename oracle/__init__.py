@@ -31,8 +31,11 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "lhs_oracle.c")
-_LIB = os.path.join(_HERE, "liblhs_oracle.so")
+# LHS_ORACLE_SRC names another C source to build the oracle from; only the
+# mutation test sets it, to check that the pins fail on planted mistakes.
+_SRC = os.environ.get("LHS_ORACLE_SRC") or os.path.join(_HERE, "lhs_oracle.c")
+_LIB = (os.path.splitext(_SRC)[0] + ".so" if os.environ.get("LHS_ORACLE_SRC")
+        else os.path.join(_HERE, "liblhs_oracle.so"))
 _CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
            "-Wall", "-Wextra"]
 
