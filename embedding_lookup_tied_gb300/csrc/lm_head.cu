@@ -46,7 +46,8 @@ constexpr int BK = 64;                    // k per stage: 128 bytes of 16-bit va
 // next to the residual operand (a consumer stall stops the refills; stages
 // in flight beyond the bandwidth-delay product absorb it)
 constexpr int kStagesRing = 11;       // residual tiles streamed beside the table tiles
-constexpr int kStagesResident = 10;   // all 16 residual rows resident
+constexpr int kStagesResident = 10;   // resident operand: all 16 rows, or the compact
+                                      // layout when it is too wide for kStagesCompact
 constexpr int kStagesCompact = 12;    // at most 3 residuals: 2 Bc + 1 rows resident
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
