@@ -11,7 +11,7 @@ namespace lhs {
 
 static thread_local int g_last_cuda_error = 0;
 
-static int cuda_status(cudaError_t e) {
+int cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return LHS_OK;
     g_last_cuda_error = static_cast<int>(e);
     return LHS_ERR_CUDA;

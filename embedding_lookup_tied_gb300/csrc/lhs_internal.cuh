@@ -469,6 +469,10 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo *out);
 
+// LHS_OK for cudaSuccess; otherwise records `e` for lhs_last_cuda_error()
+// (per host thread) and returns LHS_ERR_CUDA.
+int cuda_status(cudaError_t e);
+
 // ---------------------------------------------------------------------------
 // launchers (host side); each returns cudaSuccess or the launch error
 // ---------------------------------------------------------------------------

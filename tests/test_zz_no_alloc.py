@@ -19,8 +19,6 @@ import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-PROB_RTOL = 1e-5
-
 
 def _dev(a):
     a = np.ascontiguousarray(a)
@@ -45,40 +43,63 @@ def _noalloc(table, resid, k, temperature):
     return ids, logits, probs, err
 
 
-def test_noalloc_matches_workspace_call_twice_in_a_row():
+def _resid(seed, B, H, dtype):
+    r = wl.residuals(seed, B, H, (0.5, 8.0), dtype)
+    t = _dev(r)
+    return t.view(torch.bfloat16) if dtype == wl.BF16 else t
+
+
+def test_noalloc_matches_workspace_call_three_in_a_row():
+    # The same kernels on the same inputs: the results must be identical to
+    # the workspace call's, bit for bit, whatever the array held before.
     cases = [
-        # call 1: tensor-core path (bf16 table), 3 residuals, k 12
-        (wl.BF16, 20000, 512, 3, 12, 1.0, 31),
-        # call 2: CUDA-core path (f32 table), 8 residuals, k 40, other inputs
-        (wl.F32, 9000, 256, 8, 40, 0.8, 32),
+        # call 1: tensor-core GEMV (bf16 table), 3 residuals, k 12
+        (wl.BF16, 20000, 512, 3, 12, 1.0, 31, wl.F32),
+        # call 2: CUDA-core GEMV (f32 table), 8 residuals, k 40, other inputs
+        (wl.F32, 9000, 256, 8, 40, 0.8, 32, wl.F32),
+        # call 3: tcgen05 GEMM (bf16 table, 16 bf16 residuals), k 8; a vocab
+        # below two tiles per cluster, so no sampling pass (that pass keeps
+        # 256 KB of logits per cluster, more than the array holds)
+        (wl.BF16, 30000, 256, 16, 8, 1.3, 33, wl.BF16),
     ]
-    for dtype, V, H, B, k, T, seed in cases:
+    for dtype, V, H, B, k, T, seed, rdt in cases:
         table_np = wl.make_table(dtype, V, H, 0.02, cid=seed, threads=4)
         table = lhs.lhs_table_init(_dev(table_np), V, H, dtype)
-        resid = _dev(wl.residuals(seed, B, H, (0.5, 8.0)))
+        resid = _resid(seed, B, H, rdt)
+        assert lhs.lhs_logits_topk_workspace(table, B, k, lhs.LHS_F32 if rdt == wl.F32 else lhs.LHS_BF16) \
+            <= lhs.LHS_NOALLOC_SCRATCH_BYTES
         ref_ids, ref_logits, ref_probs, ref_err = lhs.lhs_logits_topk(table, resid, k, T)
         ids, logits, probs, err = _noalloc(table, resid, k, T)
         torch.cuda.synchronize()
         assert int(err.item()) == int(ref_err.item()) == 0
         assert torch.equal(ids, ref_ids)
         assert torch.equal(logits, ref_logits)
-        rp = ref_probs.double()
-        assert torch.all((probs.double() - rp).abs() <= PROB_RTOL * rp)
+        assert torch.equal(probs, ref_probs)
 
 
-def test_noalloc_rejects_requests_beyond_its_scratch():
-    V, H = 262144, 64
+@pytest.mark.parametrize("case", ["gemv", "gemm_with_sampling_pass"])
+def test_noalloc_rejects_requests_beyond_its_scratch(case):
+    if case == "gemv":
+        V, H, B, k, rdt = 262144, 64, 64, 128, lhs.LHS_F32   # partial lists alone > 4 MiB
+    else:
+        V, H, B, k, rdt = 100000, 64, 16, 8, lhs.LHS_BF16    # the sampled tiles' logits > 4 MiB
     table = lhs.lhs_table_init(torch.zeros((V, H), dtype=torch.bfloat16, device="cuda"), V, H,
                                lhs.LHS_BF16)
-    B, k = 64, 128            # partial lists alone: SMs x 64 x 128 x 8 bytes > 4 MiB
-    need = lhs.lhs_logits_topk_workspace(table, B, k, lhs.LHS_F32)
+    need = lhs.lhs_logits_topk_workspace(table, B, k, rdt)
     assert need > lhs.LHS_NOALLOC_SCRATCH_BYTES
-    resid = torch.zeros((B, H), dtype=torch.float32, device="cuda")
-    out = torch.empty((B, k), dtype=torch.int32, device="cuda")
-    vals = torch.empty((B, k), dtype=torch.float32, device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tdt = torch.float32 if rdt == lhs.LHS_F32 else torch.bfloat16
+    resid = torch.zeros((B, H), dtype=tdt, device="cuda")
+    # sentinels: a rejected call enqueues nothing, so none of them may change
+    out = torch.full((B, k), -7, dtype=torch.int32, device="cuda")
+    vals = torch.full((B, k), -7.0, dtype=torch.float32, device="cuda")
+    probs = torch.full((B, k), -7.0, dtype=torch.float32, device="cuda")
+    err = torch.full((1,), 0x3C, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
     rc = lhs.lib().lhs_logits_topk_noalloc(
-        ctypes.byref(table.c), resid.data_ptr(), lhs.LHS_F32, B, k, ctypes.c_float(1.0),
-        out.data_ptr(), vals.data_ptr(), None, err.data_ptr(),
+        ctypes.byref(table.c), resid.data_ptr(), rdt, B, k, ctypes.c_float(1.0),
+        out.data_ptr(), vals.data_ptr(), probs.data_ptr(), err.data_ptr(),
         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
     assert rc == lhs.LHS_ERR_BUFFER_TOO_SMALL
+    assert torch.all(out == -7) and torch.all(vals == -7.0) and torch.all(probs == -7.0)
+    assert int(err.item()) == 0x3C
