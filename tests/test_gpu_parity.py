@@ -230,23 +230,82 @@ def test_i8_nonfinite_rows_many_positions(H):
     assert int(err.item()) == ref_err == lhs.LHS_ERRBIT_NONFINITE
 
 
-def test_wire_accuracy_topk_agreement():
-    # ADR-0009 Validation on a synthetic C4-shaped case: logits from
-    # wire-decoded residuals keep the top-5 (f16) and the top-1 (i8).  The
-    # tables are Gaussian, whose top logits sit closer together than a trained
-    # model's; the bounds below follow from the codecs' error against those
-    # spacings (f16: relative 2^-11 per value -> swaps a few in 10^3; i8: noise
-    # about 0.02 sigma on a logit difference against a top-1 margin of about
-    # 0.3 sigma -> a few in 10^2).
+def _decided_topk(L64, dev, k):
+    """fp64 top-k ids per residual, and whether a GPU whose logits lie
+    within dev[b] of L64[b] (every vocab row) must return the same ordered
+    top-k: every gap between consecutive values among the k+1 largest
+    exceeds 2 dev[b]."""
+    ids = np.empty((L64.shape[0], k), np.int32)
+    decided = np.empty(L64.shape[0], bool)
+    for b in range(L64.shape[0]):
+        i, v = orc.topk_f64(L64[b], k + 1)
+        ids[b] = i[:k]
+        decided[b] = bool(np.all(v[:-1] - v[1:] > 2.0 * dev[b]))
+    return ids, decided
+
+
+# ADR-0009 Validation: top-5 agreement of logits from f16-decoded residuals
+# with the originals, top-1 for i8.  The shapes of the 31B decode and of the
+# batched workload (hidden, table type, residual distribution) on 16,384
+# vocab rows, so that the oracle's binary64 logits of every residual finish
+# in seconds.
+WIRE_ACC_CASES = [("gemma31b", 64, 710), ("batched", 128, 720)]
+
+
+@pytest.mark.parametrize("name,B,cid", WIRE_ACC_CASES, ids=[c[0] for c in WIRE_ACC_CASES])
+def test_wire_accuracy_topk_agreement_matches_oracle(name, B, cid):
+    import os
+
     import bench
-    V, H, B = 16384, 5376, 64
-    T = wl.make_table(orc.F16, V, H, 0.02, cid=700, threads=8)
-    tab = upload_table(T, orc.F16, V, H)
-    x = to_dev(wl.residuals(701, B, H, (0.5, 8.0)))
-    ordered, same_set = bench.wire_agreement(lhs, tab, x, 5, orc.WIRE_F16)
-    assert same_set >= 0.95 and ordered >= 0.9
-    ordered, _ = bench.wire_agreement(lhs, tab, x, 1, orc.WIRE_I8)
-    assert ordered >= 0.85
+    w = wl.WORKLOADS[name]
+    V, H = 16384, w.hidden
+    T = wl.make_table(w.dtype, V, H, 0.02, cid=cid, threads=8)
+    tab = upload_table(T, w.dtype, V, H)
+    R = wl.residuals(cid + 1, B, H, w.resid_scale_range, w.resid_dtype)
+    xv = np.ascontiguousarray(resid_values(R, w.resid_dtype))   # the residual values, f32
+    x = to_dev(xv)
+    rtol = RTOL[w.dtype]
+    threads = os.cpu_count() or 1
+    L64, S64 = orc.logits(T, w.dtype, V, H, xv, threads=threads, with_sumabs=True)
+    raw, e = lhs.lhs_logits(tab, x)
+    assert int(e.item()) == 0
+    dev_x = np.abs(raw.cpu().numpy().astype(np.float64) - L64)
+    assert np.all(dev_x <= rtol * S64 + 1e-30)
+    for fmt, k in ((orc.WIRE_F16, 5), (orc.WIRE_I8, 1)):
+        # oracle: its own codec round trip, binary64 logits of both
+        buf, e = orc.wire_encode(fmt, xv)
+        assert e == 0
+        xh, e = orc.wire_decode(fmt, buf, B, H)
+        assert e == 0
+        Lh64, Sh64 = orc.logits(T, w.dtype, V, H, xh, threads=threads, with_sumabs=True)
+        # the GPU's logits of the same decoded residuals (its codec is
+        # byte-exact against the oracle's, checked here too)
+        gbuf, e1 = lhs.lhs_wire_encode(fmt, x)
+        gxh, e2 = lhs.lhs_wire_decode(fmt, gbuf, B, H)
+        assert int(e1.item()) == 0 and int(e2.item()) == 0
+        assert np.array_equal(gxh.cpu().numpy().view(np.uint32), xh.view(np.uint32))
+        rawh, e = lhs.lhs_logits(tab, gxh)
+        assert int(e.item()) == 0
+        dev_h = np.abs(rawh.cpu().numpy().astype(np.float64) - Lh64)
+        assert np.all(dev_h <= rtol * Sh64 + 1e-30)
+        ref_ids, dec_ref = _decided_topk(L64, dev_x.max(axis=1), k)
+        got_ids, dec_got = _decided_topk(Lh64, dev_h.max(axis=1), k)
+        oracle_agree = np.all(ref_ids == got_ids, axis=1)
+        decided = dec_ref & dec_got
+        # the GPU's verdict (its fused top-k of x and of the decoded x)
+        gpu_agree, _ = bench.wire_agreement(lhs, tab, x, k, fmt)
+        # where the GPU's logit error cannot reorder the binary64 top-k, the
+        # verdicts must be equal
+        assert decided.mean() >= 0.95, (fmt, decided.mean())
+        bad = np.flatnonzero(gpu_agree[decided] != oracle_agree[decided])
+        assert bad.size == 0, (fmt, bad)
+        # the page expects identical top-5 for f16 and top-1 for i8; on
+        # Gaussian tables (top logits closer together than a trained
+        # model's) the oracle's own verdicts bound what the codecs keep
+        if fmt == orc.WIRE_F16:
+            assert oracle_agree.mean() >= 0.95
+        else:
+            assert oracle_agree.mean() >= 0.85
 
 
 def test_wire_decode_malformed():
@@ -632,10 +691,12 @@ def test_lm_head_workloads_full_size(name, batch):
     raw, rerr = lhs.lhs_logits(tab, rd)
     assert int(err.item()) == 0 and int(rerr.item()) == 0
     ids, vals, probs = ids.cpu().numpy(), vals.cpu().numpy(), probs.cpu().numpy()
-    # sampled residuals: the oracle computes their full logit rows one by one
+    # every residual's top-k against the oracle's selection over the GPU's
+    # own logits; a sample of them against binary64 logits, row by row
     sample = list(range(batch)) if batch <= 8 else [0, 1, 77, 128, 200, 255]
-    for b in sample:
-        Lg = raw[b].cpu().numpy()
+    raw_h = raw.cpu().numpy()
+    for b in range(batch):
+        Lg = raw_h[b]
         rid, rv = orc.topk_f32(Lg, w.k)
         assert np.array_equal(ids[b], rid), b
         assert np.array_equal(vals[b].view(np.uint32), rv.view(np.uint32)), b
@@ -644,7 +705,7 @@ def test_lm_head_workloads_full_size(name, batch):
     for b in sample[:4]:
         L64, S64 = orc.logits(T, w.dtype, w.vocab, w.hidden, xv[b:b + 1], threads=16,
                               with_sumabs=True)
-        Lg = raw[b].cpu().numpy().astype(np.float64)
+        Lg = raw_h[b].astype(np.float64)
         assert np.all(np.abs(Lg - L64[0]) <= RTOL[w.dtype] * S64[0] + 1e-30), b
         check_topk_against_fp64(ids[b], vals[b], L64[0], S64[0], w.k, RTOL[w.dtype])
 
