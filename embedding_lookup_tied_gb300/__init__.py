@@ -208,7 +208,8 @@ def lhs_embed_wire(table: Table, ids: torch.Tensor, scale: float, fmt: int, laye
     return buf, err
 
 
-def lhs_unique_ids(ids: torch.Tensor, vocab: int, ws=None, err=None, stream=None):
+def lhs_unique_ids(ids: torch.Tensor, vocab: int, ws=None, err=None, stream=None, unique=None,
+                   inverse=None, count=None):
     """Distinct ids in [0, vocab), ascending, and each position's index into
     them (-1 for a bad id).  Returns (unique, inverse, count tensor, err word);
     unique holds min(n, vocab) entries, the first `count` of them valid."""
@@ -220,9 +221,14 @@ def lhs_unique_ids(ids: torch.Tensor, vocab: int, ws=None, err=None, stream=None
     if need < 0:
         raise ValueError("bad vocab")
     ws = torch.empty(need, dtype=torch.uint8, device=dev) if ws is None else ws
-    unique = torch.empty(max(1, min(n, vocab)), dtype=torch.int32, device=dev)
-    inverse = torch.empty(max(1, n), dtype=torch.int32, device=dev)
-    count = torch.empty(1, dtype=torch.int32, device=dev)
+    if unique is None:
+        unique = torch.empty(max(1, min(n, vocab)), dtype=torch.int32, device=dev)
+    if inverse is None:
+        inverse = torch.empty(max(1, n), dtype=torch.int32, device=dev)
+    if count is None:
+        count = torch.empty(1, dtype=torch.int32, device=dev)
+    if unique.numel() < min(n, vocab) or inverse.numel() < n or count.numel() < 1:
+        raise ValueError("output tensors too small")
     err = _err_word(err, dev)
     _check(lib().lhs_unique_ids(vocab, _dev(ids, "ids") if n else None, n, _dev(unique, "unique"),
                                 _dev(inverse, "inverse"), _dev(count, "count"), _dev(ws, "ws"),

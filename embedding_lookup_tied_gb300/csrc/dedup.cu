@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(256)
     bool bad = false;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int32_t id = __ldg(ids + i);
+        const int32_t id = ld_dep(ids + i);
         if (id < 0 || static_cast<int64_t>(id) >= vocab) bad = true;
         else flags[id] = 1u;  // every writer stores the same value
     }
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kScanThreads)
     __shared__ uint32_t ws[33];
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kTile + threadIdx.x;
     uint32_t excl;
-    const uint32_t total = block_exclusive_scan(i < vocab ? flags[i] : 0u, excl, ws);
+    const uint32_t total = block_exclusive_scan(i < vocab ? ld_dep(flags + i) : 0u, excl, ws);
     if (threadIdx.x == 0) tile_sums[blockIdx.x] = total;
 }
 
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kScanThreads)
     uint32_t excl;
     block_exclusive_scan(f, excl, ws);
     if (f) {
-        const uint32_t r = tile_offs[blockIdx.x] + excl;
+        const uint32_t r = ld_dep(tile_offs + blockIdx.x) + excl;
         flags[i] = r;  // the flag array becomes the rank array
         unique[r] = static_cast<int32_t>(i);
     }
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(256)
     pdl_wait();
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int32_t id = __ldg(ids + i);
-        inverse[i] = (id < 0 || static_cast<int64_t>(id) >= vocab) ? -1 : static_cast<int32_t>(rank[id]);
+        const int32_t id = ld_dep(ids + i);
+        inverse[i] = (id < 0 || static_cast<int64_t>(id) >= vocab) ? -1 : static_cast<int32_t>(ld_dep(rank + id));
     }
 }
 
@@ -139,9 +139,9 @@ __global__ void __launch_bounds__(256)
     const int lane = threadIdx.x & 31;
     const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t nu = __ldg(count);
+    const int64_t nu = ld_dep(count);
     for (int64_t u = w0; u < nu; u += nw) {
-        const uint8_t *row = table + static_cast<int64_t>(__ldg(unique + u)) * row_bytes;
+        const uint8_t *row = table + static_cast<int64_t>(ld_dep(unique + u)) * row_bytes;
         float *o = rows + u * hidden;
         for (int j = lane; j < hidden; j += 32) o[j] = __fmul_rn(row_element<DT>(row, j), scale);
     }
@@ -157,15 +157,15 @@ __global__ void __launch_bounds__(256)
     const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t i = w0; i < n; i += nw) {
-        const int32_t u = __ldg(inverse + i);
+        const int32_t u = ld_dep(inverse + i);
         float *o = out + i * hidden;
         if (vec) {
             float4 *o4 = reinterpret_cast<float4 *>(o);
             const float4 *r4 = reinterpret_cast<const float4 *>(rows + static_cast<int64_t>(u < 0 ? 0 : u) * hidden);
-            for (int c = lane; c < hidden / 4; c += 32) o4[c] = u < 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(r4 + c);
+            for (int c = lane; c < hidden / 4; c += 32) o4[c] = u < 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_dep(r4 + c);
         } else {
             const float *r = rows + static_cast<int64_t>(u < 0 ? 0 : u) * hidden;
-            for (int j = lane; j < hidden; j += 32) o[j] = u < 0 ? 0.0f : __ldg(r + j);
+            for (int j = lane; j < hidden; j += 32) o[j] = u < 0 ? 0.0f : ld_dep(r + j);
         }
     }
 }

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     uint8_t *pay = buf + 16;
     for (int64_t t = warp0; t < n; t += nwarps) {
-        const int32_t id = __ldg(ids + t);
+        const int32_t id = ld_dep(ids + t);
         const bool bad = bad_id(id, vocab);
         if (bad && lane == 0) set_err(err, LHS_ERRBIT_BAD_TOKEN);
         const uint8_t *row = table + static_cast<int64_t>(bad ? 0 : id) * row_bytes;
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kI8Threads)
         write_wire_header(buf, layer, static_cast<uint32_t>(n), flags, top_k);
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
     for (int64_t p = blockIdx.x; p < n; p += gridDim.x) {
-        const int32_t id = __ldg(ids + p);
+        const int32_t id = ld_dep(ids + p);
         const bool bad = bad_id(id, vocab);  // uniform over the block
         if (bad && threadIdx.x == 0) set_err(err, LHS_ERRBIT_BAD_TOKEN);
         const uint8_t *row = table + static_cast<int64_t>(bad ? 0 : id) * row_bytes;
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(128)
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
     const int ng = hidden >> 3;
     for (int64_t p = w0; p < n; p += nw) {
-        const int32_t id = __ldg(ids + p);
+        const int32_t id = ld_dep(ids + p);
         const bool bad = bad_id(id, vocab);
         if (bad && lane == 0) set_err(err, LHS_ERRBIT_BAD_TOKEN);
         const uint8_t *row = table + static_cast<int64_t>(bad ? 0 : id) * row_bytes;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(128)
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
     const int n4 = hidden >> 2;
     for (int64_t p = w0; p < n; p += nw) {
-        const int32_t id = __ldg(ids + p);
+        const int32_t id = ld_dep(ids + p);
         const bool bad = bad_id(id, vocab);
         if (bad && lane == 0) set_err(err, LHS_ERRBIT_BAD_TOKEN);
         const uint8_t *row = table + static_cast<int64_t>(bad ? 0 : id) * row_bytes;

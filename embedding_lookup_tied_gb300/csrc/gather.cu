@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t t = warp0; t < n; t += nwarps) {
-        const int32_t id = __ldg(ids + t);
+        const int32_t id = ld_dep(ids + t);
         float *o = out + t * hidden;
         if (id < 0 || static_cast<int64_t>(id) >= vocab) {
             if (VEC) {

@@ -306,8 +306,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                    const GemmParams p) {
     constexpr int S = kStagesG;
     extern __shared__ uint8_t dyn_smem[];
-    GemmSmem &sm = *reinterpret_cast<GemmSmem *>(
-        (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+    GemmSmem &sm = *reinterpret_cast<GemmSmem *>(smem_align<1024>(dyn_smem));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();          // residual half
     const int cl = blockIdx.x >> 1;                   // cluster index
@@ -494,7 +493,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int cnt = 0;
             uint64_t tau = 0ull;       // exact key every kept entry beats (after a cut)
             float tau_val = -INFINITY; // the logit below which nothing can be kept
-            if (valid && p.sample_logits) tau_val = p.sample_logits[static_cast<size_t>(b) * p.k + p.k - 1];
+            if (valid && p.sample_logits) tau_val = ld_dep(p.sample_logits + static_cast<size_t>(b) * p.k + p.k - 1);
             const float l2e_invT = 1.4426950408889634f * p.invT;
             uint64_t *cand = p.keys + (static_cast<size_t>(cl) * p.B + (valid ? b : 0)) * p.cap;
             uint64_t *cand_lane0 =

@@ -48,6 +48,17 @@ __device__ __forceinline__ int32_t key_id(uint64_t key) {
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// `p` (a pointer into shared memory) advanced to the next multiple of ALIGN
+// bytes of the shared window.  The offset is added to p itself, so the
+// compiler still knows that the result points into shared memory and emits
+// shared loads, stores and atomics through it; a round trip through an
+// integer would leave a generic pointer, whose accesses take the slower
+// generic path.
+template <unsigned ALIGN>
+__device__ __forceinline__ uint8_t *smem_align(uint8_t *p) {
+    static_assert((ALIGN & (ALIGN - 1)) == 0, "a power of two");
+    return p + ((ALIGN - (smem_u32(p) & (ALIGN - 1))) & (ALIGN - 1));
+}
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
@@ -432,6 +443,20 @@ int warp_kernel_grid(K kernel, int64_t n, int wps, int num_sms, int device) {
 __device__ __forceinline__ void write_wire_header(uint8_t *buf, uint32_t layer, uint32_t seq_len,
                                                   uint32_t flags, uint32_t top_k) {
     *reinterpret_cast<uint4 *>(buf) = make_uint4(layer, seq_len, flags, top_k);
+}
+
+// Load of data that the preceding kernel in the stream may have written
+// (residuals, token ids, wire messages, intermediate buffers).  A kernel
+// launched as a programmatic dependent starts before its predecessor has
+// finished; a non-coherent read-only load (ld.global.nc, as __ldg or a
+// const __restrict__ pointer produce) counts on its bytes staying fixed for
+// the whole kernel, so it may be scheduled ahead of pdl_wait() and return
+// the bytes from before the predecessor wrote them.  These loads take the
+// coherent L2 path (ld.global.cg), which stays behind the wait.  Only the
+// tables, which no kernel writes between calls, are read with __ldg.
+template <typename T>
+__device__ __forceinline__ T ld_dep(const T *p) {
+    return __ldcg(p);
 }
 
 // Programmatic dependent launch.  pdl_wait(): block until the preceding

@@ -112,7 +112,7 @@ __device__ __forceinline__ Group make_group(int tid, int nthreads, int ncols) {
 // Radix select over 8-bit digits of 64-bit keys: find the kk-th largest of
 // keys[0..cnt) (keys unique) and return (prefix, mask) such that exactly kk
 // keys satisfy (key & mask) >= prefix.  Executed by the T threads of a group.
-__device__ void group_radix_select(const uint64_t *keys, int cnt, int kk, unsigned *hist,
+__device__ __forceinline__ void group_radix_select(const uint64_t *keys, int cnt, int kk, unsigned *hist,
                                    int *sel_digit, int *sel_above, const Group &g,
                                    uint64_t &prefix_out, uint64_t &mask_out) {
     uint64_t prefix = 0, mask = 0;
@@ -185,7 +185,7 @@ __device__ void group_radix_select(const uint64_t *keys, int cnt, int kk, unsign
 // its place), one pass instead of the radix select's digit passes.
 constexpr int kDirectWork = 512;
 
-__device__ void group_compact(uint64_t *keys, int *cnt, uint64_t *tau, int kk, TopkShared &sm,
+__device__ __forceinline__ void group_compact(uint64_t *keys, int *cnt, uint64_t *tau, int kk, TopkShared &sm,
                               const Group &g) {
     const int n = *cnt;
     if (n <= kk) return;  // uniform across the group
@@ -292,7 +292,7 @@ __device__ __forceinline__ void topk_offer(TopkShared &sm, int col, int cap, flo
 // early and later rounds offer few candidates), and always before they could
 // overflow.  The cut runs while the producer keeps the TMA ring full, so it
 // costs no HBM time while it is shorter than the ring.  All consumers call.
-__device__ void topk_round_end(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
+__device__ __forceinline__ void topk_round_end(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
                                int round_max) {
     named_bar_sync(kBarAll, nthreads);
     if (tid == 0) {
@@ -317,7 +317,7 @@ __device__ void topk_round_end(TopkShared &sm, int tid, int nthreads, int ncols,
 // first cuts each column to k.
 constexpr int kRankWork = 512;  // comparisons per thread for the direct ranking
 
-__device__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
+__device__ __forceinline__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
                             int b_off, int batch_total, uint64_t *part_keys, float2 *part_ms,
                             float invT) {
     named_bar_sync(kBarAll, nthreads);
@@ -802,8 +802,8 @@ __global__ void __launch_bounds__(256)
         float v = 0.0f;
         if (b < Bc && kk < K) {
             const int64_t src = static_cast<int64_t>(b) * K + kk;
-            if (XDT == LHS_F32) v = __ldg(static_cast<const float *>(resid) + src);
-            else v = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(resid) + src)) << 16);
+            if (XDT == LHS_F32) v = ld_dep(static_cast<const float *>(resid) + src);
+            else v = __uint_as_float(static_cast<uint32_t>(ld_dep(static_cast<const unsigned short *>(resid) + src)) << 16);
         }
         uint16_t hi, lo;
         if (BF16T) {
@@ -905,8 +905,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a16,
                    const __grid_constant__ CUtensorMap tm_x, const TcParams p) {
     extern __shared__ uint8_t dyn_smem[];
-    TcSmemT<NST> &sm = *reinterpret_cast<TcSmemT<NST> *>(
-        (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+    TcSmemT<NST> &sm = *reinterpret_cast<TcSmemT<NST> *>(smem_align<1024>(dyn_smem));
     uint8_t *xsm = reinterpret_cast<uint8_t *>(&sm) + tc_x_offset<NST>();
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -1023,8 +1022,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float v = 0.0f;
                 if (b < p.Bc && kk < p.K) {
                     const int64_t src = static_cast<int64_t>(b) * p.K + kk;
-                    if (p.resid_f32) v = __ldg(static_cast<const float *>(p.resid) + src);
-                    else v = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(p.resid) + src)) << 16);
+                    if (p.resid_f32) v = ld_dep(static_cast<const float *>(p.resid) + src);
+                    else v = __uint_as_float(static_cast<uint32_t>(ld_dep(static_cast<const unsigned short *>(p.resid) + src)) << 16);
                 }
                 uint16_t hi, lo;
                 if (BF16T) {
@@ -1205,8 +1204,8 @@ __global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtPa
 
     for (int64_t i = tid; i < static_cast<int64_t>(p.Bc) * p.K; i += kSimtThreads) {
         float v;
-        if (p.resid_dtype == LHS_F32) v = __ldg(static_cast<const float *>(p.resid) + i);
-        else v = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(p.resid) + i)) << 16);
+        if (p.resid_dtype == LHS_F32) v = ld_dep(static_cast<const float *>(p.resid) + i);
+        else v = __uint_as_float(static_cast<uint32_t>(ld_dep(static_cast<const unsigned short *>(p.resid) + i)) << 16);
         xs[i] = v;
     }
     topk_init(tk, tid, kSimtThreads);
@@ -1347,7 +1346,7 @@ __host__ __device__ __forceinline__ size_t bulk_xs_offset(int64_t row_bytes) {
 template <int DT, bool RAW, int BC>
 __global__ void __launch_bounds__(kBulkThreads, 1) gemv_bulk_kernel(const BulkParams p) {
     extern __shared__ uint8_t dyn_smem[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 127) & ~uintptr_t(127));
+    uint8_t *base = smem_align<128>(dyn_smem);
     uint8_t *ring = base;
     uint64_t *full = reinterpret_cast<uint64_t *>(base + bulk_ring_bytes(p.row_bytes));
     uint64_t *empty = full + kBulkStages;
@@ -1411,8 +1410,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) gemv_bulk_kernel(const BulkPa
     pdl_wait();  // residuals may come from the previous kernel; partial lists may still be read by it
     for (int64_t i = tid; i < static_cast<int64_t>(p.Bc) * p.K; i += kBulkConsumers) {
         float v;
-        if (p.resid_dtype == LHS_F32) v = __ldg(static_cast<const float *>(p.resid) + i);
-        else v = __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(p.resid) + i)) << 16);
+        if (p.resid_dtype == LHS_F32) v = ld_dep(static_cast<const float *>(p.resid) + i);
+        else v = __uint_as_float(static_cast<uint32_t>(ld_dep(static_cast<const unsigned short *>(p.resid) + i)) << 16);
         xs[i] = v;
     }
     named_bar_sync(kBarAll, kBulkConsumers);

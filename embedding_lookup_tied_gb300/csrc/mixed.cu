@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(256)
     const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t t = w0; t < n; t += nw) {
-        const int32_t id = __ldg(ids + t);
+        const int32_t id = ld_dep(ids + t);
         float *o = out + t * hidden;
         if (id < 0 || static_cast<int64_t>(id) >= vocab) {
             for (int j = lane; j < hidden; j += 32) o[j] = 0.0f;

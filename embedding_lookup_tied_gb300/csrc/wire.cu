@@ -31,8 +31,8 @@ constexpr int kI8DecCache = 12;  // 4-code units a decoding thread loads with th
 
 template <int XDT>
 __device__ __forceinline__ float load_x(const void *x, int64_t i) {
-    if (XDT == LHS_F32) return __ldg(static_cast<const float *>(x) + i);
-    return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(x) + i))
+    if (XDT == LHS_F32) return ld_dep(static_cast<const float *>(x) + i);
+    return __uint_as_float(static_cast<uint32_t>(ld_dep(static_cast<const unsigned short *>(x) + i))
                            << 16);
 }
 
@@ -41,11 +41,11 @@ template <int XDT>
 __device__ __forceinline__ void load_x8(const void *x, int64_t g, float (&v)[8]) {
     if (XDT == LHS_F32) {
         const float4 *p = static_cast<const float4 *>(x) + 2 * g;
-        const float4 a = __ldg(p), b = __ldg(p + 1);
+        const float4 a = ld_dep(p), b = ld_dep(p + 1);
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else {
-        const uint4 w = __ldg(static_cast<const uint4 *>(x) + g);
+        const uint4 w = ld_dep(static_cast<const uint4 *>(x) + g);
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -76,9 +76,9 @@ __global__ void __launch_bounds__(kEwThreads)
             load_x8<XDT>(x, g, v);
             reinterpret_cast<uint4 *>(pay)[g] = pack_f16x8(v);
         } else if (XDT == LHS_F32) {
-            reinterpret_cast<float4 *>(pay)[g] = __ldg(static_cast<const float4 *>(x) + g);
+            reinterpret_cast<float4 *>(pay)[g] = ld_dep(static_cast<const float4 *>(x) + g);
         } else {
-            const uint2 w = __ldg(static_cast<const uint2 *>(x) + g);
+            const uint2 w = ld_dep(static_cast<const uint2 *>(x) + g);
             reinterpret_cast<float4 *>(pay)[g] =
                 make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
                             __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kEwThreads)
     pdl_wait();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const uint32_t hdr_seq = __ldg(reinterpret_cast<const uint32_t *>(buf) + 1);
+    const uint32_t hdr_seq = ld_dep(reinterpret_cast<const uint32_t *>(buf) + 1);
     if (hdr_seq != seq_len) {
         if (tid == 0) set_err(err, LHS_ERRBIT_MALFORMED);
         return;
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kEwThreads)
 #pragma unroll
             for (int u = 0; u < kDecUnroll; ++u) {
                 const int64_t g = g0 + u * nth;
-                if (g < ng) w[u] = __ldg(reinterpret_cast<const uint2 *>(pay) + g);
+                if (g < ng) w[u] = ld_dep(reinterpret_cast<const uint2 *>(pay) + g);
             }
 #pragma unroll
             for (int u = 0; u < kDecUnroll; ++u) {
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kEwThreads)
 #pragma unroll
             for (int u = 0; u < kDecUnroll; ++u) {
                 const int64_t g = g0 + u * nth;
-                if (g < ng) w[u] = __ldg(reinterpret_cast<const float4 *>(pay) + g);
+                if (g < ng) w[u] = ld_dep(reinterpret_cast<const float4 *>(pay) + g);
             }
 #pragma unroll
             for (int u = 0; u < kDecUnroll; ++u) {
@@ -146,9 +146,9 @@ __global__ void __launch_bounds__(kEwThreads)
     }
     for (int64_t i = ng * 4 + tid; i < n; i += nth) {
         if (FMT == LHS_WIRE_F16)
-            x[i] = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short *>(pay) + i)));
+            x[i] = __half2float(__ushort_as_half(ld_dep(reinterpret_cast<const unsigned short *>(pay) + i)));
         else
-            x[i] = __ldg(reinterpret_cast<const float *>(pay) + i);
+            x[i] = ld_dep(reinterpret_cast<const float *>(pay) + i);
     }
 }
 
@@ -407,10 +407,10 @@ __global__ void __launch_bounds__(128)
         i8_position_warp4(
             [&](int st, float (&v)[4]) {
                 if (XDT == LHS_F32) {
-                    const float4 a = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + xrow) + st);
+                    const float4 a = ld_dep(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + xrow) + st);
                     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
                 } else {
-                    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(static_cast<const unsigned short *>(x) + xrow) + st);
+                    const uint2 w = ld_dep(reinterpret_cast<const uint2 *>(static_cast<const unsigned short *>(x) + xrow) + st);
                     v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xFFFF0000u);
                     v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xFFFF0000u);
                 }
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kI8Threads)
                      float *__restrict__ x, int32_t *err) {
     pdl_trigger();
     pdl_wait();
-    const uint32_t hdr_seq = __ldg(reinterpret_cast<const uint32_t *>(buf) + 1);
+    const uint32_t hdr_seq = ld_dep(reinterpret_cast<const uint32_t *>(buf) + 1);
     if (hdr_seq != static_cast<uint32_t>(seq_len)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) set_err(err, LHS_ERRBIT_MALFORMED);
         return;
@@ -440,17 +440,17 @@ __global__ void __launch_bounds__(kI8Threads)
 #pragma unroll
             for (int c = 0; c < kI8DecCache; ++c) {
                 const int g = threadIdx.x + c * kI8Threads;
-                if (g < (hidden >> 2)) pre[c] = __ldg(reinterpret_cast<const uint32_t *>(pos + 8) + g);
+                if (g < (hidden >> 2)) pre[c] = ld_dep(reinterpret_cast<const uint32_t *>(pos + 8) + g);
             }
-            const uint2 h = __ldg(reinterpret_cast<const uint2 *>(pos));
+            const uint2 h = ld_dep(reinterpret_cast<const uint2 *>(pos));
             scale = __uint_as_float(h.x);
             zp = __uint_as_float(h.y);
         } else {
             uint32_t s = 0, z = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                s |= static_cast<uint32_t>(__ldg(pos + i)) << (8 * i);
-                z |= static_cast<uint32_t>(__ldg(pos + 4 + i)) << (8 * i);
+                s |= static_cast<uint32_t>(ld_dep(pos + i)) << (8 * i);
+                z |= static_cast<uint32_t>(ld_dep(pos + 4 + i)) << (8 * i);
             }
             scale = __uint_as_float(s);
             zp = __uint_as_float(z);
@@ -479,10 +479,10 @@ __global__ void __launch_bounds__(kI8Threads)
                 const int g = threadIdx.x + c * kI8Threads;
                 if (g < ng) put(g, pre[c]);
             }
-            for (int g = threadIdx.x + kI8DecCache * kI8Threads; g < ng; g += kI8Threads) put(g, __ldg(codes + g));
+            for (int g = threadIdx.x + kI8DecCache * kI8Threads; g < ng; g += kI8Threads) put(g, ld_dep(codes + g));
         } else {
             for (int j = threadIdx.x; j < hidden; j += kI8Threads)
-                xo[j] = __fmul_rn(static_cast<float>(static_cast<int8_t>(__ldg(pos + 8 + j))), scale);
+                xo[j] = __fmul_rn(static_cast<float>(static_cast<int8_t>(ld_dep(pos + 8 + j))), scale);
         }
     }
 }
