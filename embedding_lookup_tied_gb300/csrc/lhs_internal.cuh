@@ -527,7 +527,8 @@ struct LmHeadPlan {
     int path;          // 0 = tensor-core streaming GEMV (f16/bf16 table, batch <= 8 per pass)
                        // 1 = CUDA-core GEMV (any table dtype)
                        // 2 = tcgen05 GEMM (bf16 table, bf16 residuals, batch > 8)
-                       // 3 = bulk-stream CUDA-core GEMV (f32 / Q8_0, rows of 16..1024 bytes)
+                       // 3 = bulk-stream CUDA-core GEMV (f32, rows of 16..1024 bytes)
+                       // 4 = Q8_0 tensor-core GEMV (hidden % 256 == 0, batch <= 8 per pass)
     int grid;          // CTAs of the projection kernel (= partial top-k lists)
     int batch_chunk;   // residuals per pass of the projection
     int kpad;          // hidden rounded up for the tensor-core operand
@@ -539,7 +540,7 @@ struct LmHeadPlan {
     int key_stride;    // entries between consecutive partial lists
     bool sample;       // GEMM: run the sample pass
     bool xres;         // tensor-core GEMV: residual operand resident in shared memory (no prep kernel)
-    int nst;           // tensor-core GEMV: TMA ring stages
+    int nst;           // tensor-core GEMVs: TMA ring stages
     size_t bytes;      // total workspace
 };
 int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dtype,
@@ -558,6 +559,20 @@ cudaError_t launch_selftest_wait(int32_t *err, int64_t timeout_ns, cudaStream_t 
 // row pitch; box = box_cols x box_rows, 128-byte swizzle, zero fill outside.
 bool make_tma_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
                         uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, bool bf16);
+
+// 2-D map over a row-major [rows x cols] matrix of 16-bit units (any bytes:
+// the Q8_0 GEMV reads its rows' blocks through it) with the given row pitch;
+// box = box_cols x box_rows, no swizzle, zero fill outside.
+bool make_tma_map_u16_plain(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                            uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows);
+
+// Q8_0 lm_head on the tensor cores (see gemv_q8.cu): ring stages that fit
+// for passes of up to bc residuals (0: the kernel does not fit), and the
+// projection passes of one call (partial lists per CTA, or raw logits).
+int gemv_q8_stages(int K, int bc, int max_smem);
+cudaError_t launch_gemv_q8(const lhs_table &t, int nst, const void *resid, int32_t resid_dtype, int32_t batch,
+                           int32_t k, float invT, float *raw, uint64_t *part_keys, float2 *part_ms,
+                           int32_t *err, int grid, const DeviceInfo &dev, cudaStream_t stream);
 
 // Merge of per-CTA partial lists (stride entries apart, the first len of
 // each used) into the sorted top-k per residual, with probabilities when

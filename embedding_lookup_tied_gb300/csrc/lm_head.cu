@@ -16,8 +16,12 @@
 //    on 16 vocab rows.  The residuals enter as two 16-bit rows each
 //    (hi = rn16(x), lo = rn16(x - hi)), so the product keeps ~16 (bf16) or
 //    ~22 (f16) bits of every f32 residual.
-//  * Other tables (f32, Q8_0, ragged hidden): CUDA-core GEMV, one warp per
-//    row, residuals in shared memory as f32.
+//  * Q8_0 tables, hidden % 256 == 0: the tensor-core GEMV of gemv_q8.cu
+//    (codes turned into exact f16 in registers, the per-block scale applied
+//    in f32 after each block's MMAs).
+//  * Other tables (f32, other Q8_0, ragged hidden): CUDA-core GEMV, one warp
+//    per row (f32 rows up to 1 KB: a bulk-copy ring of whole rows),
+//    residuals in shared memory as f32.
 //  * Fused top-k: every logit is offered to a per-CTA candidate list per
 //    residual if it beats that list's current k-th best key; lists are cut
 //    back to k by a radix select when they fill.  An online (max, sum exp)
@@ -33,6 +37,7 @@
 #include <mutex>
 
 #include "lhs_internal.cuh"
+#include "lm_topk.cuh"
 
 namespace lhs {
 namespace {
@@ -40,7 +45,6 @@ namespace {
 // ---------------------------------------------------------------------------
 // tile geometry
 // ---------------------------------------------------------------------------
-constexpr int BM = 128;                   // table rows per block
 constexpr int BK = 64;                    // k per stage: 128 bytes of 16-bit values
 // TMA ring depth of the tensor-core GEMV: as deep as shared memory allows
 // next to the residual operand (a consumer stall stops the refills; stages
@@ -55,309 +59,7 @@ constexpr int kTcThreads = kConsumers + 32;  // + one producer warp
 constexpr int kAStageBytes = BM * BK * 2;    // 16 KB
 constexpr int kXStageBytes = 16 * BK * 2;    // 2 KB: 8 hi rows + 8 lo rows
 constexpr int kBoxRowsSmall = 16;            // TMA box for the ragged last block
-constexpr int kCandTotal = 2048;             // candidate keys per CTA (all residuals)
-constexpr int kBatchChunk = 8;               // residuals per projection pass
-constexpr int kBarAll = 15;                  // named barrier: all consumers (groups use 1..8)
-constexpr int kMaxConsumerWarps = 16;        // largest consumer group of the top-k state
 constexpr int kSimtThreads = 256;
-
-// ---------------------------------------------------------------------------
-// shared top-k state (both GEMV kernels)
-// ---------------------------------------------------------------------------
-struct TopkShared {
-    uint64_t cand[kCandTotal];
-    // Column c's radix-select histogram and its scratch keys share bytes:
-    // the select has finished with hist[c] (behind a group barrier) before
-    // scratch[c] is written, and nothing reads hist[c] after that.
-    union {
-        uint64_t scratch[kBatchChunk][kMaxK];
-        unsigned hist[kBatchChunk][256];
-    };
-    uint64_t tau[kBatchChunk];
-    uint64_t tmin[kBatchChunk];
-    float2 ms_warp[kMaxConsumerWarps][kBatchChunk];
-    int cnt[kBatchChunk];
-    int nsel[kBatchChunk];
-    int sel_digit[kBatchChunk];
-    int sel_above[kBatchChunk];
-    int need_compact;
-    int abort_flag;
-};
-
-static_assert(sizeof(uint64_t) * kMaxK == sizeof(unsigned) * 256, "a column's hist and scratch coincide");
-
-__device__ __forceinline__ int ld_volatile(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
-
-struct Group {  // the threads that own one residual column during selection
-    int gtid, T, bar_id, col;
-};
-
-__device__ __forceinline__ void group_sync(const Group &g) {
-    if (g.T == 32) __syncwarp();
-    else named_bar_sync(g.bar_id, g.T);
-}
-
-// Split `nthreads` consumer threads into pow2(ncols) groups.
-__device__ __forceinline__ Group make_group(int tid, int nthreads, int ncols) {
-    int p = 1;
-    while (p < ncols) p <<= 1;
-    Group g;
-    g.T = nthreads / p;
-    g.col = tid / g.T;
-    g.gtid = tid % g.T;
-    g.bar_id = 1 + g.col;  // ids 1..4 (only used when T > 32, i.e. p <= 4)
-    return g;
-}
-
-// Radix select over 8-bit digits of 64-bit keys: find the kk-th largest of
-// keys[0..cnt) (keys unique) and return (prefix, mask) such that exactly kk
-// keys satisfy (key & mask) >= prefix.  Executed by the T threads of a group.
-__device__ __forceinline__ void group_radix_select(const uint64_t *keys, int cnt, int kk, unsigned *hist,
-                                   int *sel_digit, int *sel_above, const Group &g,
-                                   uint64_t &prefix_out, uint64_t &mask_out) {
-    uint64_t prefix = 0, mask = 0;
-    int need = kk;
-    const int lane = g.gtid & 31;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int i = g.gtid; i < 256; i += g.T) hist[i] = 0;
-        group_sync(g);
-        // histogram of the digit, one atomic per distinct digit per warp
-        // (keys that share a prefix mostly share the next digit too)
-        for (int base = 0; base < cnt; base += g.T) {
-            const int i = base + g.gtid;
-            uint32_t digit = 0xFFFFFFFFu;
-            if (i < cnt) {
-                const uint64_t key = keys[i];
-                if ((key & mask) == prefix) digit = static_cast<uint32_t>(key >> shift) & 255u;
-            }
-            const unsigned peers = __match_any_sync(0xFFFFFFFFu, digit);
-            if (digit != 0xFFFFFFFFu && __ffs(peers) - 1 == lane)
-                atomicAdd(&hist[digit], static_cast<unsigned>(__popc(peers)));
-        }
-        group_sync(g);
-        if (g.gtid < 32) {
-            // lane L owns digits 255-8L ... 248-8L (descending)
-            unsigned c[8];
-            unsigned lsum = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                c[i] = hist[255 - 8 * lane - i];
-                lsum += c[i];
-            }
-            unsigned incl = lsum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            const unsigned excl = incl - lsum;
-            if (excl < static_cast<unsigned>(need) && static_cast<unsigned>(need) <= incl) {
-                unsigned run = excl;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (run + c[i] >= static_cast<unsigned>(need)) {
-                        *sel_digit = 255 - 8 * lane - i;
-                        *sel_above = static_cast<int>(run);
-                        break;
-                    }
-                    run += c[i];
-                }
-            }
-        }
-        group_sync(g);
-        const int d = *sel_digit;
-        const int above = *sel_above;
-        const int bin = static_cast<int>(hist[d]);
-        need -= above;
-        prefix |= static_cast<uint64_t>(d) << shift;
-        mask |= 0xFFull << shift;
-        group_sync(g);  // everyone has read hist / sel_* before they change
-        if (bin == need) break;
-    }
-    prefix_out = prefix;
-    mask_out = mask;
-}
-
-// Cut keys[0..*cnt) down to its kk best (kk <= kMaxK), in place; *tau
-// becomes the kk-th best key.  Group-collective.
-// Short lists (n^2 / group size <= kDirectWork compares per thread) are cut
-// by ranking every key against all the others (keys are unique: its rank is
-// its place), one pass instead of the radix select's digit passes.
-constexpr int kDirectWork = 512;
-
-__device__ __forceinline__ void group_compact(uint64_t *keys, int *cnt, uint64_t *tau, int kk, TopkShared &sm,
-                              const Group &g) {
-    const int n = *cnt;
-    if (n <= kk) return;  // uniform across the group
-    if (n <= kMaxK * 2 + 128 && n * n <= g.T * kDirectWork) {
-        for (int i = g.gtid; i < n; i += g.T) {
-            const uint64_t key = keys[i];
-            int rank = 0;
-#pragma unroll 4
-            for (int q = 0; q < n; ++q) rank += keys[q] > key;
-            if (rank < kk) sm.scratch[g.col][rank] = key;
-        }
-        group_sync(g);
-        for (int i = g.gtid; i < kk; i += g.T) keys[i] = sm.scratch[g.col][i];
-        if (g.gtid == 0) {
-            *cnt = kk;
-            *tau = sm.scratch[g.col][kk - 1];
-        }
-        group_sync(g);
-        return;
-    }
-    uint64_t prefix, mask;
-    group_radix_select(keys, n, kk, sm.hist[g.col], &sm.sel_digit[g.col], &sm.sel_above[g.col], g,
-                       prefix, mask);
-    if (g.gtid == 0) {
-        sm.nsel[g.col] = 0;
-        sm.tmin[g.col] = ~0ull;
-    }
-    group_sync(g);
-    uint64_t kmin = ~0ull;
-    for (int i = g.gtid; i < n; i += g.T) {
-        const uint64_t key = keys[i];
-        if ((key & mask) >= prefix) {
-            const int pos = atomicAdd(&sm.nsel[g.col], 1);
-            sm.scratch[g.col][pos] = key;
-            kmin = key < kmin ? key : kmin;
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, kmin, o);
-        kmin = other < kmin ? other : kmin;
-    }
-    if ((g.gtid & 31) == 0 && kmin != ~0ull)
-        atomicMin(reinterpret_cast<unsigned long long *>(&sm.tmin[g.col]),
-                  static_cast<unsigned long long>(kmin));
-    group_sync(g);
-    for (int i = g.gtid; i < kk; i += g.T) keys[i] = sm.scratch[g.col][i];
-    if (g.gtid == 0) {
-        *cnt = kk;
-        *tau = sm.tmin[g.col];
-    }
-    group_sync(g);
-}
-
-// Online softmax state (m, s): s = sum exp((v - m) / T) over the values
-// seen, m their max.  Of the two rescalings exp((m - m') / T) and
-// exp((v - m') / T) one has a zero argument, i.e. is exactly 1, so only the
-// other is evaluated.
-__device__ __forceinline__ void ms_update(float &m, float &s, float v, float invT) {
-    const float mn = fmaxf(m, v);
-    if (mn == -INFINITY) return;
-    if (m >= v) {
-        s = s + expf((v - mn) * invT);
-    } else {
-        s = s * expf((m - mn) * invT) + 1.0f;
-        m = mn;
-    }
-}
-// s * exp((m - M) / T), the sum of a partial (m, s) rescaled to a max M >= m
-// (exactly s when m == M, including the empty partial m = M = -inf).
-__device__ __forceinline__ float ms_rescaled(float m, float s, float M, float invT) {
-    return m == M ? s : (m == -INFINITY ? 0.0f : s * expf((m - M) * invT));
-}
-
-__device__ __forceinline__ float2 ms_combine(float2 a, float2 b, float invT) {
-    const float mn = fmaxf(a.x, b.x);
-    if (mn == -INFINITY) return make_float2(-INFINITY, 0.0f);
-    if (a.x >= b.x) return make_float2(a.x, a.y + b.y * expf((b.x - a.x) * invT));
-    return make_float2(b.x, b.y + a.y * expf((a.x - b.x) * invT));
-}
-
-__device__ __forceinline__ void topk_init(TopkShared &sm, int tid, int nthreads) {
-    for (int b = tid; b < kBatchChunk; b += nthreads) {
-        sm.cnt[b] = 0;
-        sm.tau[b] = 0ull;
-    }
-    if (tid == 0) {
-        sm.need_compact = 0;
-        sm.abort_flag = 0;
-    }
-}
-
-// Offer one logit: appended when it beats the column's current k-th best.
-__device__ __forceinline__ void topk_offer(TopkShared &sm, int col, int cap, float v, int32_t id) {
-    const uint64_t key = topk_key(v, id);
-    if (key > sm.tau[col]) {
-        const int pos = atomicAdd(&sm.cnt[col], 1);
-        sm.cand[col * cap + pos] = key;
-    }
-}
-
-// After a round that could add up to `round_max` candidates per column:
-// cut lists back to k once they hold 2k+64 entries (so the threshold rises
-// early and later rounds offer few candidates), and always before they could
-// overflow.  The cut runs while the producer keeps the TMA ring full, so it
-// costs no HBM time while it is shorter than the ring.  All consumers call.
-__device__ __forceinline__ void topk_round_end(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
-                               int round_max) {
-    named_bar_sync(kBarAll, nthreads);
-    if (tid == 0) {
-        const int limit = min(cap - round_max, 2 * k + 64);
-        int need = 0;
-        for (int b = 0; b < ncols; ++b) need |= (sm.cnt[b] > limit);
-        sm.need_compact = need;
-    }
-    named_bar_sync(kBarAll, nthreads);
-    if (sm.need_compact) {
-        const Group g = make_group(tid, nthreads, ncols);
-        if (g.col < ncols) group_compact(sm.cand + g.col * cap, &sm.cnt[g.col], &sm.tau[g.col], k, sm, g);
-        named_bar_sync(kBarAll, nthreads);
-    }
-}
-
-// Final cut to k and write the CTA's partial list and (m, s) per column.
-// Each list is written sorted, largest key first, and padded with 0 (below
-// every key).  A candidate's place is the number of larger candidates in its
-// column (keys are unique), so when the lists are short every candidate is
-// ranked directly — one pass, no selection rounds; otherwise a radix select
-// first cuts each column to k.
-constexpr int kRankWork = 512;  // comparisons per thread for the direct ranking
-
-__device__ __forceinline__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
-                            int b_off, int batch_total, uint64_t *part_keys, float2 *part_ms,
-                            float invT) {
-    named_bar_sync(kBarAll, nthreads);
-    int work = 0;
-    for (int b = 0; b < ncols; ++b) work += sm.cnt[b] * sm.cnt[b];
-    if (work > nthreads * kRankWork) {  // uniform: every thread read the same counts
-        const Group g = make_group(tid, nthreads, ncols);
-        if (g.col < ncols) group_compact(sm.cand + g.col * cap, &sm.cnt[g.col], &sm.tau[g.col], k, sm, g);
-        named_bar_sync(kBarAll, nthreads);
-    }
-    int total = 0;
-    for (int b = 0; b < ncols; ++b) total += sm.cnt[b];
-    for (int i = tid; i < total; i += nthreads) {
-        int b = 0, j = i;
-        while (j >= sm.cnt[b]) j -= sm.cnt[b++];
-        const int n = sm.cnt[b];
-        const uint64_t *src = sm.cand + b * cap;
-        const uint64_t key = src[j];
-        int rank = 0;
-#pragma unroll 4
-        for (int q = 0; q < n; ++q) rank += src[q] > key;
-        if (rank < k)
-            part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + rank] = key;
-    }
-    for (int i = tid; i < ncols * k; i += nthreads) {
-        const int b = i / k, j = i % k;
-        if (j >= sm.cnt[b])
-            part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + j] = 0ull;
-    }
-    if (tid < ncols) {
-        // the warps' (m, s): max first, then the rescaled sums (independent exps)
-        const int nw = nthreads / 32;
-        float M = -INFINITY;
-        for (int w = 0; w < nw; ++w) M = fmaxf(M, sm.ms_warp[w][tid].x);
-        float S = 0.0f;
-#pragma unroll 4
-        for (int w = 0; w < nw; ++w) S += ms_rescaled(sm.ms_warp[w][tid].x, sm.ms_warp[w][tid].y, M, invT);
-        part_ms[static_cast<size_t>(blockIdx.x) * batch_total + b_off + tid] = make_float2(M, S);
-    }
-}
 
 // ---------------------------------------------------------------------------
 // merge: global top-k of one residual from G partial lists, sorted, + probs.
@@ -750,38 +452,6 @@ __device__ void merge_column_sorted(const uint64_t *lists, int R, const float2 *
     named_bar_sync(bar_id, kMergeThreads);  // w is free for the next residual
 }
 
-// Row range of CTA c: 16-row units split evenly.
-__device__ __forceinline__ void cta_rows(int64_t V, int G, int c, int64_t &r0, int64_t &r1) {
-    const int64_t units = (V + 15) / 16;
-    r0 = (units * c / G) * 16;
-    r1 = (units * (c + 1) / G) * 16;
-    if (r1 > V) r1 = V;
-    if (r0 > V) r0 = V;
-}
-
-// Blocks of CTA c in the tensor-core GEMV, interleaved over the table: the
-// full 128-row blocks c, c + G, c + 2G, ... of the first q = V / (G * BM)
-// rounds, then CTA c's even share (16-row units) of the rows after them.
-// Every CTA streams the same number of rows give or take 16, drawn from all
-// over the table.
-__device__ __forceinline__ int tc_blocks(int64_t V, int G, int c) {
-    const int64_t q = V / (static_cast<int64_t>(G) * BM);
-    int64_t s0, s1;
-    cta_rows(V - q * G * BM, G, c, s0, s1);
-    return static_cast<int>(q) + (s1 > s0 ? 1 : 0);
-}
-__device__ __forceinline__ void tc_block(int64_t V, int G, int c, int blk, int64_t &row0, int &rows) {
-    const int64_t q = V / (static_cast<int64_t>(G) * BM);
-    if (blk < q) {
-        row0 = (c + static_cast<int64_t>(blk) * G) * BM;
-        rows = BM;
-    } else {
-        int64_t s0, s1;
-        cta_rows(V - q * G * BM, G, c, s0, s1);
-        row0 = q * G * BM + s0;
-        rows = static_cast<int>(s1 - s0);
-    }
-}
 
 // ---------------------------------------------------------------------------
 // residual operand prep: x[b][k] (f32 or bf16) -> 16 x Kp rows of the
@@ -1274,7 +944,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) gemv_simt_kernel(const SimtPa
 }
 
 // ---------------------------------------------------------------------------
-// Bulk-stream CUDA-core GEMV (f32 and Q8_0 tables, rows a multiple of 16
+// Bulk-stream CUDA-core GEMV (f32 tables, rows a multiple of 16
 // bytes and at most kBulkRowBytesMax): a producer warp copies 32 whole rows
 // per stage — one contiguous cp.async.bulk — into a 4-stage ring (one top-k
 // round of 128 rows in flight); each of 16 consumer warps multiplies two
@@ -1290,30 +960,14 @@ constexpr int kBulkThreads = kBulkConsumers + 32;  // + the producer warp
 constexpr int kBulkRowsPerWarp = kBulkRows / kBulkWarps;
 constexpr int kBulkRowBytesMax = 1024;  // ring: 4 x 32 rows <= 128 KB
 
-// Elements 8g .. 8g+7 of a row held in shared memory.
+// Elements 8g .. 8g+7 of an f32 row held in shared memory.
 template <int DT>
 __device__ __forceinline__ void smem_row8(const uint8_t *row, int g, float (&v)[8]) {
-    if (DT == LHS_F32) {
-        const float4 a = *reinterpret_cast<const float4 *>(row + 32 * g);
-        const float4 b = *reinterpret_cast<const float4 *>(row + 32 * g + 16);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {  // Q8_0: block g / 4, codes (g % 4) * 8 .. +7
-        const unsigned short *b16 = reinterpret_cast<const unsigned short *>(row + (g >> 2) * 34);
-        const float d = f16_bits_to_f32(b16[0]);
-        const int q0 = 1 + (g & 3) * 4;
-        // int8 -> binary32 without a conversion instruction: with u = q + 128
-        // (the code's bits with the top bit flipped), the bits 0x4B000000 | u
-        // are the float 2^23 + u, so subtracting 2^23 + 128 leaves q exactly
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t w = static_cast<uint32_t>(b16[q0 + i]) ^ 0x8080u;
-            const float f0 = __int_as_float(static_cast<int>(__byte_perm(w, 0x4B000000u, 0x7540))) - 8388736.0f;
-            const float f1 = __int_as_float(static_cast<int>(__byte_perm(w, 0x4B000000u, 0x7541))) - 8388736.0f;
-            v[2 * i] = __fmul_rn(d, f0);
-            v[2 * i + 1] = __fmul_rn(d, f1);
-        }
-    }
+    static_assert(DT == LHS_F32, "the bulk-stream GEMV serves f32 tables");
+    const float4 a = *reinterpret_cast<const float4 *>(row + 32 * g);
+    const float4 b = *reinterpret_cast<const float4 *>(row + 32 * g + 16);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 struct BulkParams {
@@ -1788,6 +1442,20 @@ bool make_tma_map_16bit(CUtensorMap *map, const void *base, uint64_t cols, uint6
     return r == CUDA_SUCCESS;
 }
 
+bool make_tma_map_u16_plain(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                            uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 // dynamic shared memory of the tensor-core GEMV with nst stages and passes
@@ -1836,23 +1504,37 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
         const int64_t tiles = (t.vocab + 255) / 256;
         if ((tiles + clusters - 1) / clusters * 256 > 65535) gemm = false;
     }
-    // f32 / Q8_0 tables with short 16-byte-multiple rows: bulk-stream GEMV
-    const bool bulk = !tc && (t.dtype == LHS_F32 || t.dtype == LHS_Q8_0) && t.hidden % 8 == 0 &&
+    // Q8_0 tables whose rows are whole 256-value stages (272-byte multiples,
+    // a TMA pitch), 16-byte aligned, with a ring of at least two stages
+    const int bc1 = batch < 1 ? 1 : (batch < kBatchChunk ? batch : kBatchChunk);
+    const int q8_nst = (t.dtype == LHS_Q8_0 && t.hidden % 256 == 0 && t.vocab >= BM &&
+                        reinterpret_cast<uintptr_t>(t.data) % 16 == 0)
+                           ? gemv_q8_stages(t.hidden, bc1, dev.max_smem_optin)
+                           : 0;
+    // f32 tables with short 16-byte-multiple rows: bulk-stream GEMV
+    const bool bulk = !tc && t.dtype == LHS_F32 && t.hidden % 8 == 0 &&
                       t.row_bytes % 16 == 0 && t.row_bytes <= kBulkRowBytesMax &&
                       bulk_smem_bytes(t.row_bytes, kBatchChunk, t.hidden) <= static_cast<size_t>(dev.max_smem_optin);
-    p.path = gemm ? 2 : (tc ? 0 : (bulk ? 3 : 1));
+    p.path = gemm ? 2 : (tc ? 0 : (q8_nst ? 4 : (bulk ? 3 : 1)));
     if (gemm) {
         p.grid = clusters;  // partial lists: one per cluster
         // a cluster covers 2 x 128 residuals (one TMEM lane each): larger
         // batches run as successive passes of that many
         p.batch_chunk = batch < gemm_lm_head_max_batch() ? batch : gemm_lm_head_max_batch();
     } else {
-        p.grid = static_cast<int>(units < dev.num_sms ? units : dev.num_sms);
+        // with top-k, one SM stays free for the merge kernel: it cannot share
+        // an SM with a GEMV CTA (shared memory), so it runs there while the
+        // next call's CTAs already stream on the others
+        const int ctas = (k > 0 && dev.num_sms > 1) ? dev.num_sms - 1 : dev.num_sms;
+        p.grid = static_cast<int>(units < ctas ? units : ctas);
     }
     if (gemm) {
         // nothing else to size: the GEMM reads the residuals in place
     } else if (p.path == 3) {
         p.batch_chunk = kBatchChunk;
+    } else if (p.path == 4) {
+        p.batch_chunk = kBatchChunk;
+        p.nst = q8_nst;
     } else if (tc) {
         p.batch_chunk = kBatchChunk;
         // the deepest ring that fits: the resident operand (compact for up
@@ -2016,32 +1698,35 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
             e = launch_pdl(kern, dim3(plan.grid), dim3(kTcThreads), smem, stream, tm_a, tm_a16, tm_x, p);
             if (e != cudaSuccess) return e;
         }
+    } else if (plan.path == 4) {
+        e = launch_gemv_q8(t, plan.nst, resid, resid_dtype, batch, k, invT, raw_logits, part_keys, part_ms, err,
+                           plan.grid, dev, stream);
+        if (e != cudaSuccess) return e;
     } else if (plan.path == 3) {
         using BulkKernel = void (*)(const BulkParams);
-#define LHS_BULK(DT, R) {gemv_bulk_kernel<DT, R, 1>, gemv_bulk_kernel<DT, R, 2>, gemv_bulk_kernel<DT, R, 4>, \
-                         gemv_bulk_kernel<DT, R, 8>}
-        static const BulkKernel kTable[2][2][4] = {{LHS_BULK(LHS_Q8_0, false), LHS_BULK(LHS_Q8_0, true)},
-                                                   {LHS_BULK(LHS_F32, false), LHS_BULK(LHS_F32, true)}};
-#undef LHS_BULK
+        static const BulkKernel kTable[2][4] = {
+            {gemv_bulk_kernel<LHS_F32, false, 1>, gemv_bulk_kernel<LHS_F32, false, 2>,
+             gemv_bulk_kernel<LHS_F32, false, 4>, gemv_bulk_kernel<LHS_F32, false, 8>},
+            {gemv_bulk_kernel<LHS_F32, true, 1>, gemv_bulk_kernel<LHS_F32, true, 2>,
+             gemv_bulk_kernel<LHS_F32, true, 4>, gemv_bulk_kernel<LHS_F32, true, 8>}};
         {
             static std::mutex mu;
-            static bool done[16][64] = {};
+            static bool done[8][64] = {};
             std::lock_guard<std::mutex> lock(mu);
-            for (int d = 0; d < 2; ++d)
-                for (int r = 0; r < 2; ++r)
-                    for (int c = 0; c < 4; ++c) {
-                        const int which = d * 8 + r * 4 + c;
-                        if (!done[which][dev.device]) {
-                            e = cudaFuncSetAttribute(kTable[d][r][c], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     dev.max_smem_optin);
-                            if (e != cudaSuccess) return e;
-                            done[which][dev.device] = true;
-                        }
+            for (int r = 0; r < 2; ++r)
+                for (int c = 0; c < 4; ++c) {
+                    const int which = r * 4 + c;
+                    if (!done[which][dev.device]) {
+                        e = cudaFuncSetAttribute(kTable[r][c], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 dev.max_smem_optin);
+                        if (e != cudaSuccess) return e;
+                        done[which][dev.device] = true;
                     }
+                }
         }
         for (int c0 = 0; c0 < batch; c0 += plan.batch_chunk) {
             const int Bc = batch - c0 < plan.batch_chunk ? batch - c0 : plan.batch_chunk;
-            const BulkKernel kern = kTable[t.dtype == LHS_F32][raw][Bc <= 1 ? 0 : (Bc <= 2 ? 1 : (Bc <= 4 ? 2 : 3))];
+            const BulkKernel kern = kTable[raw][Bc <= 1 ? 0 : (Bc <= 2 ? 1 : (Bc <= 4 ? 2 : 3))];
             BulkParams p;
             p.table = static_cast<const uint8_t *>(t.data);
             p.V = t.vocab;

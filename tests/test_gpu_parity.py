@@ -346,8 +346,12 @@ LM_CASES = [
     (orc.BF16, 128, 64, 2, 1, orc.F32),       # one block, k = 1
     (orc.F32, 1000, 256, 4, 5, orc.F32),      # bulk-stream CUDA-core path (1 KB rows)
     (orc.Q8_0, 700, 128, 2, 10, orc.F32),     # CUDA-core path (136-byte rows)
-    (orc.Q8_0, 5000, 768, 3, 10, orc.F32),    # bulk-stream path, 816-byte rows, ragged last stage
-    (orc.Q8_0, 2100, 256, 11, 7, orc.BF16),   # bulk-stream path, two passes, bf16 residuals
+    (orc.Q8_0, 5000, 768, 3, 10, orc.F32),    # Q8_0 tensor-core path, 816-byte rows, ragged last block
+    (orc.Q8_0, 2100, 256, 11, 7, orc.BF16),   # Q8_0 tensor-core path: passes of 8 and 3 (two and
+                                              # one column groups), bf16 residuals
+    (orc.Q8_0, 40000, 512, 8, 50, orc.F32),   # Q8_0 tensor-core path, several blocks on every SM
+    (orc.Q8_0, 3001, 2560, 5, 16, orc.F32),   # Q8_0 tensor-core path, 10 stages per block, ragged
+    (orc.Q8_0, 100, 256, 3, 20, orc.F32),     # vocab < 128 -> CUDA-core path
     (orc.F32, 3001, 64, 8, 64, orc.F32),      # bulk-stream path, 256-byte rows, ragged vocab
     (orc.F32, 900, 36, 2, 5, orc.F32),        # hidden % 8 != 0: CUDA-core path
     (orc.F16, 1000, 72, 2, 6, orc.F32),       # hidden % 64 != 0, tensor-core path
@@ -402,6 +406,62 @@ def test_lm_head_parity(case):
         check_topk_against_fp64(ids[b], vals[b], L64[b], S64[b], k, rtol)
 
 
+def test_q8_lm_head_residual_range():
+    # The Q8_0 tensor-core path scales each residual by a power of two and
+    # splits it into two levels of f16 halves: residuals far outside the f16
+    # range, deep in the f32 subnormals, or with values 2^33 apart stay within
+    # the f32-table tolerance -- also on rows whose code at the outlier is 0,
+    # where the logit comes from the small values alone.
+    V, H, k = 3000, 768, 12
+    T = wl.make_table(orc.Q8_0, V, H, 0.02, cid=290, threads=4)
+    tab = upload_table(T, orc.Q8_0, V, H)
+    code17 = T.view(np.uint8).reshape(V, -1)[:, 2 + 17].view(np.int8)
+    assert np.count_nonzero(code17 == 0) >= 3
+    base = wl.residuals(291, 6, H)
+    X = np.empty_like(base)
+    X[0] = base[0] * np.float32(1e-30)
+    X[1] = base[1] * np.float32(1e30)
+    X[2] = base[2]
+    X[2, 17] = np.float32(1e10)            # one value 2^33 above the rest
+    X[3] = base[3] * np.float32(1e-41)     # f32 subnormals
+    X[4] = 0.0
+    X[5] = base[5] * np.float32(70000.0)   # beyond the f16 range
+    L64, S64 = orc.logits(T, orc.Q8_0, V, H, X, threads=8, with_sumabs=True)
+    raw, err = lhs.lhs_logits(tab, to_dev(X))
+    assert int(err.item()) == 0
+    Lg = raw.cpu().numpy()
+    assert np.all(np.isfinite(Lg))
+    assert np.all(np.abs(Lg.astype(np.float64) - L64) <= RTOL[orc.Q8_0] * S64 + 1e-300)
+    assert np.all(Lg[4] == 0.0)
+    ids, vals, _, err = lhs.lhs_logits_topk(tab, to_dev(X), k)
+    assert int(err.item()) == 0
+    for b in range(X.shape[0]):
+        rid, rv = orc.topk_f32(Lg[b], k)
+        assert np.array_equal(ids.cpu().numpy()[b], rid), b
+        assert np.array_equal(vals.cpu().numpy()[b].view(np.uint32), rv.view(np.uint32)), b
+
+
+def test_q8_lm_head_nonfinite_residuals():
+    # inf / NaN residual values: every logit is what binary64 gives (+-inf, or
+    # NaN where an inf meets a zero code or inf meets -inf)
+    V, H = 1000, 256
+    T = wl.make_table(orc.Q8_0, V, H, 0.02, cid=292, threads=4)
+    tab = upload_table(T, orc.Q8_0, V, H)
+    X = wl.residuals(293, 3, H)
+    X[0, 5] = np.inf
+    X[1, 7] = np.nan
+    X[2, 3] = -np.inf
+    X[2, 200] = np.inf
+    L64 = orc.logits(T, orc.Q8_0, V, H, X, threads=8)
+    raw, err = lhs.lhs_logits(tab, to_dev(X))
+    assert int(err.item()) == 0
+    Lg = raw.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isnan(Lg), np.isnan(L64))
+    fin = ~np.isnan(L64)
+    assert np.array_equal(Lg[fin], L64[fin])   # +-inf on both sides
+    assert np.isnan(L64[1]).all() and (~np.isnan(L64[0])).any()
+
+
 @pytest.mark.parametrize("lm_dtype", [orc.BF16, orc.Q8_0, orc.F32])
 def test_untied_lm_head_on_embedded_rows(lm_dtype):
     # untied: rows gathered from one table, projected on another
@@ -443,6 +503,10 @@ def test_launch_count_follows_the_plan():
     assert lhs.lhs_logits_topk_launches(tab4, 4, 10, lhs.LHS_F32) == 3
     assert n(64, 10, lhs.LHS_BF16) in (2, 4)               # GEMM (+ sample pass and its merge)
     assert n(64, 0, lhs.LHS_BF16) == 1
+    Tq = wl.make_table(orc.Q8_0, 1000, 512, 0.02, cid=253, threads=4)
+    tabq = upload_table(Tq, orc.Q8_0, 1000, 512)
+    assert lhs.lhs_logits_topk_launches(tabq, 1, 10, lhs.LHS_F32) == 2    # Q8_0 GEMV + merge
+    assert lhs.lhs_logits_topk_launches(tabq, 12, 10, lhs.LHS_BF16) == 3  # two passes + merge
     T32 = wl.make_table(orc.F32, 1000, 64, 0.02, cid=251, threads=4)
     tab32 = upload_table(T32, orc.F32, 1000, 64)
     assert lhs.lhs_logits_topk_launches(tab32, 4, 5, lhs.LHS_F32) == 2   # GEMV + merge
@@ -638,8 +702,9 @@ def test_topk_clustered_in_one_cta_range():
 
 def test_topk_many_keys_above_the_merge_bound():
     # 32-row CTA ranges, each with 4 high logits and k = 5: every CTA's k-th
-    # key is a low one, so the bound admits all 4 x 152 high keys
-    G = 152
+    # key is a low one, so the bound admits all 4 x G high keys (a top-k
+    # GEMV runs one CTA per SM but one, which it leaves to the merge)
+    G = torch.cuda.get_device_properties(0).multi_processor_count - 1
     V, H, k = 32 * G, 64, 5
     T = wl.make_table(orc.BF16, V, H, 0.02, cid=264, threads=4)
     rows = np.arange(V)
