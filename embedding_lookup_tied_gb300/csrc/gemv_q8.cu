@@ -32,8 +32,9 @@
 // A non-finite residual value enters level 0's hi unscaled (inf or NaN,
 // lo = 0), so such logits are inf or NaN as the products dictate.
 //
-// Layout: one CTA per SM, 8 consumer warps of 16 vocab rows each + one
-// producer warp.  The producer keeps a ring of TMA tiles in flight: 128
+// Layout: one CTA per SM, 8 consumer warps of 16 vocab rows each, one
+// producer warp and one selection warp (lm_topk.cuh: the consumers only stage
+// each block's logits; the selection warp keeps the top-k lists).  The producer keeps a ring of TMA tiles in flight: 128
 // table rows x 8 Q8_0 blocks (256 values, 272 bytes, no swizzle); the CTA's
 // 128-row blocks are those of the tensor-core GEMV (interleaved over the
 // table, then an even share of the rest).  The residual operand is built by
@@ -60,7 +61,7 @@ constexpr int kQStageBytes = BM * kQChunkBytes;           // 34,816 = 34 KB
 constexpr int kQBoxRowsSmall = 16;                        // box of the ragged last block
 constexpr int kQWarps = 8;
 constexpr int kQConsumers = kQWarps * 32;
-constexpr int kQThreads = kQConsumers + 32;  // + the producer warp
+constexpr int kQThreads = kQConsumers + 64;  // + the producer warp and the selection warp
 constexpr int kQMaxStages = 8;
 constexpr int kQFragBytes = 32 * 16;  // one B fragment set: 32 lanes x 4 registers
 
@@ -179,9 +180,8 @@ __device__ __forceinline__ void q8_block_a(const Q8Words<ODD> &q, uint32_t (&a)[
 
 // NB: column groups of 8: residuals 2 nb and 2 nb + 1, each as columns
 // (hi, lo) of level 0 then (hi, lo) of level 1.  RAW: write the logits
-// instead of the top-k lists.  WL: per-warp candidate lists (no CTA-wide
-// barrier between blocks), else the CTA's shared lists.
-template <bool RAW, int NB, bool WL>
+// instead of the top-k lists (the selection warp then has nothing to do).
+template <bool RAW, int NB>
 __global__ void __launch_bounds__(kQThreads, 1)
     gemv_q8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a16,
                    const Q8Params p) {
@@ -192,10 +192,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     TopkShared &tk = hd.tk;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    int qq = 1;
-    while (qq < p.Bc) qq <<= 1;
-    const int cap = kCandTotal / qq;  // candidate slots per residual (CTA lists)
-    const int cap_w = warp_list_cap(p.Bc);  // per-warp lists
     const int nblk = tc_blocks(p.V, gridDim.x, blockIdx.x);
     const int nst = p.nst;
 
@@ -204,6 +200,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             mbar_init(&hd.full[s], 1);
             mbar_init(&hd.empty[s], kQWarps);
         }
+        sel_init(tk, kQWarps);
         fence_mbar_init();
     }
     if (tid < kQConsumers) topk_init(tk, tid, kQConsumers);
@@ -257,6 +254,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     break;
                 }
         }
+        return;
+    }
+    if (warp == kQWarps + 1) {
+        // ---------------- selection: the CTA's top-k lists and (m, s)
+        if (RAW) return;
+        pdl_wait();  // the partial lists may still be read by the previous kernel
+        sel_run(tk, nblk, [&](int blk, int64_t &row0, int &rows) { tc_block(p.V, gridDim.x, blockIdx.x, blk, row0, rows); },
+                p.Bc, p.k, p.invT, p.b_off, p.batch_total, p.part_ms, p.err, lane);
+        named_bar_sync(kBarFinal, kQConsumers + 32);
         return;
     }
 
@@ -379,12 +385,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     named_bar_sync(kBarAll, kQConsumers);
 
-    float m_st[NB], s_st[NB];
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        m_st[nb] = -INFINITY;
-        s_st[nb] = 0.0f;
-    }
     int s = 0;
     uint32_t ph = 0;
     const uint4 *frag_l = frag + lane;
@@ -446,8 +446,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // epilogue: thread holds rows (g, g+8) x columns (2c, 2c+1), the hi
         // and lo of residual 2 nb + c / 2 at level c % 2.  Both threads of a
         // pair form the logit, level-0 part + level-1 part (the same sum in
-        // either order); the even one takes row g, the odd one row g+8.
-        if (active && !ld_volatile(&tk.abort_flag)) {
+        // either order); the even one takes row g, the odd one row g+8.  The
+        // logits are written out (raw) or staged for the selection warp.
+        bool staged = RAW;
+        if (!RAW && active && !ld_volatile(&tk.abort_flag)) {
+            if (!sel_acquire(tk, blk)) {
+                if (lane == 0) {
+                    set_err(p.err, LHS_ERRBIT_TIMEOUT);
+                    tk.abort_flag = 1;
+                }
+            } else {
+                staged = true;
+            }
+        }
+        if (active && staged) {
+            float *st = RAW ? nullptr : sel_slot(tk, blk);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
                 float val[2];
@@ -457,52 +470,32 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     val[r] = part + __shfl_xor_sync(0xFFFFFFFFu, part, 1);
                 }
                 const int r = c & 1;
+                const float vr = r ? val[1] : val[0];  // a select: no indexed local array
                 const int b = 2 * nb + (c >> 1);
-                const int64_t v = row0 + warp * 16 + g + 8 * r;
-                if (b < p.Bc && v < row0 + rows) {
+                const int rr = warp * 16 + g + 8 * r;  // row within the block
+                if (b < p.Bc) {
                     if (RAW) {
-                        p.raw[static_cast<int64_t>(p.b_off + b) * p.V + v] = val[r];
+                        if (rr < rows) p.raw[static_cast<int64_t>(p.b_off + b) * p.V + row0 + rr] = vr;
                     } else {
-                        ms_update(m_st[nb], s_st[nb], val[r], p.invT);
-                        if (WL) wl_offer(tk, warp, b, cap_w, val[r], static_cast<int32_t>(v));
-                        else topk_offer(tk, b, cap, val[r], static_cast<int32_t>(v));
+                        st[b * BM + rr] = vr;
                     }
                 }
             }
         }
-        if (RAW) {
-            named_bar_sync(kBarAll, kQConsumers);
-        } else if (WL) {
-            // the warp's own lists: no wait for the other warps
-            wl_round_end(tk, warp, p.Bc, p.k, lane);
-        } else {
-            topk_round_end(tk, tid, kQConsumers, p.Bc, p.k, cap, BM);
-        }
-        // the flag only changes inside the stage loop: every consumer reads
-        // the same value here after a CTA barrier, every lane of a warp after
-        // the warp's own round end
+        if (RAW) named_bar_sync(kBarAll, kQConsumers);
+        else sel_publish(tk, blk, lane);
+        // the flag only changes inside the stage loop or just above: every
+        // consumer reads the same value here after the CTA barrier (raw), and
+        // every lane of a warp after the warp barrier of sel_publish
         if (ld_volatile(&tk.abort_flag)) break;
     }
-    if (WL) named_bar_sync(kBarAll, kQConsumers);  // the warps leave the loop at different times
-    if (RAW || ld_volatile(&tk.abort_flag)) return;
-    // per-warp (m, s) of residual 2 nb + c / 2 over the lanes that share c / 2
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-        float M = m_st[nb];
-        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 1));
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-        float S = ms_rescaled(m_st[nb], s_st[nb], M, p.invT);
-        S += __shfl_xor_sync(0xFFFFFFFFu, S, 1);
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
-        if (g == 0 && (c & 1) == 0) tk.ms_warp[warp][2 * nb + (c >> 1)] = make_float2(M, S);
-    }
-    if (WL)
-        wl_finish(tk, tid, kQConsumers, p.Bc, p.k, p.b_off, p.batch_total, p.part_keys, p.part_ms, p.invT);
-    else
-        topk_finish(tk, tid, kQConsumers, p.Bc, p.k, cap, p.b_off, p.batch_total, p.part_keys, p.part_ms,
-                    p.invT);
+    if (RAW) return;
+    // the CTA's partial lists, written by the consumers once the selection
+    // warp has taken every block
+    named_bar_sync(kBarFinal, kQConsumers + 32);
+    if (ld_volatile(&tk.abort_flag)) return;
+    topk_write_lists(tk, tid, kQConsumers, p.Bc, p.k, kCandTotal / pow2_at_least(p.Bc), p.b_off, p.batch_total,
+                     p.part_keys);
 }
 
 }  // namespace
@@ -525,21 +518,17 @@ cudaError_t launch_gemv_q8(const lhs_table &t, int nst, const void *resid, int32
         !make_tma_map_u16_plain(&tm_a16, t.data, cols, t.vocab, t.row_bytes, kQChunkU16, kQBoxRowsSmall))
         return cudaErrorInvalidValue;
     using Kern = void (*)(const CUtensorMap, const CUtensorMap, const Q8Params);
-    // [mode: CTA lists, per-warp lists, raw][column groups - 1]
-    static const Kern kTable[3][4] = {
-        {gemv_q8_kernel<false, 1, false>, gemv_q8_kernel<false, 2, false>, gemv_q8_kernel<false, 3, false>,
-         gemv_q8_kernel<false, 4, false>},
-        {gemv_q8_kernel<false, 1, true>, gemv_q8_kernel<false, 2, true>, gemv_q8_kernel<false, 3, true>,
-         gemv_q8_kernel<false, 4, true>},
-        {gemv_q8_kernel<true, 1, false>, gemv_q8_kernel<true, 2, false>, gemv_q8_kernel<true, 3, false>,
-         gemv_q8_kernel<true, 4, false>}};
+    // [raw][column groups - 1]
+    static const Kern kTable[2][4] = {
+        {gemv_q8_kernel<false, 1>, gemv_q8_kernel<false, 2>, gemv_q8_kernel<false, 3>, gemv_q8_kernel<false, 4>},
+        {gemv_q8_kernel<true, 1>, gemv_q8_kernel<true, 2>, gemv_q8_kernel<true, 3>, gemv_q8_kernel<true, 4>}};
     const bool is_raw = raw != nullptr;
     {
         // one attribute flag per instantiation: the largest size this device allows
         static std::mutex mu;
-        static bool done[12][64] = {};
+        static bool done[8][64] = {};
         std::lock_guard<std::mutex> lock(mu);
-        for (int r = 0; r < 3; ++r)
+        for (int r = 0; r < 2; ++r)
             for (int n = 0; n < 4; ++n)
                 if (!done[r * 4 + n][dev.device]) {
                     const cudaError_t e = cudaFuncSetAttribute(kTable[r][n], cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -568,8 +557,7 @@ cudaError_t launch_gemv_q8(const lhs_table &t, int nst, const void *resid, int32
         p.resid = static_cast<const uint8_t *>(resid) + static_cast<size_t>(c0) * t.hidden * relt;
         p.resid_f32 = resid_dtype == LHS_F32;
         p.err = err;
-        const int mode = is_raw ? 2 : (warp_lists_fit(Bc, k) ? 1 : 0);
-        const cudaError_t e = launch_pdl(kTable[mode][NB - 1], dim3(grid), dim3(kQThreads),
+        const cudaError_t e = launch_pdl(kTable[is_raw][NB - 1], dim3(grid), dim3(kQThreads),
                                          q8_smem_bytes(nst, t.hidden, NB), stream, tm_a, tm_a16, p);
         if (e != cudaSuccess) return e;
     }

@@ -16,9 +16,6 @@ constexpr int kCandTotal = 2048;             // candidate keys per CTA (all resi
 constexpr int kBatchChunk = 8;               // residuals per projection pass
 constexpr int kBarAll = 15;                  // named barrier: all consumers (groups use 1..8)
 constexpr int kMaxConsumerWarps = 16;        // largest consumer group of the top-k state
-constexpr int kWarpLists = 8;                // warps with lists of their own (per-warp mode)
-constexpr int kWarpListSlots = kCandTotal / kWarpLists;  // 256 keys per warp, all columns
-constexpr int kWarpRowsPerRound = 16;        // rows a warp offers between two of its cuts
 
 // ---------------------------------------------------------------------------
 // shared top-k state (both GEMV kernels)
@@ -41,9 +38,10 @@ struct TopkShared {
     int sel_above[kBatchChunk];
     int need_compact;
     int abort_flag;
-    // per-warp lists (warp_lists_fit): counts and k-th best keys, warp x column
-    int wcnt[kWarpLists][kBatchChunk];
-    uint64_t wtau[kWarpLists][kBatchChunk];
+    // selection-warp mode: the two staging slots of block logits (in the
+    // bytes of scratch / hist, unused in that mode) and their barriers
+    uint64_t sel_full[2];
+    uint64_t sel_empty[2];
 };
 
 static_assert(sizeof(uint64_t) * kMaxK == sizeof(unsigned) * 256, "a column's hist and scratch coincide");
@@ -204,21 +202,18 @@ __device__ __forceinline__ void group_compact(uint64_t *keys, int *cnt, uint64_t
 
 // Online softmax state (m, s): s = sum exp((v - m) / T) over the values
 // seen, m their max.  Of the two rescalings exp((m - m') / T) and
-// exp((v - m') / T) one has a zero argument, i.e. is exactly 1, so only the
-// other is evaluated.  The common case, a term below the running max, uses
-// the hardware exponential (__expf: a few ulp where the terms matter, i.e.
-// near the max; the far terms it rounds worse are smaller by e^-|x|), which
-// keeps the sum within ~1e-6 of the exact one; the rare new-max rescaling of
-// the whole sum uses the accurate expf.
+// exp((v - m') / T) one has a zero argument, i.e. is exactly 1, so one
+// exponential of (min(m, v) - m') / T serves both cases, without a branch:
+// s' = s + t when v does not raise the max, s' = s t + 1 when it does.  It
+// is the hardware exponential (__expf: a few ulp where the terms matter,
+// i.e. near the max; the far terms it rounds worse are smaller by e^-|x|),
+// which keeps the sum within ~1e-6 of the exact one.
 __device__ __forceinline__ void ms_update(float &m, float &s, float v, float invT) {
     const float mn = fmaxf(m, v);
     if (mn == -INFINITY) return;
-    if (m >= v) {
-        s = s + __expf((v - mn) * invT);
-    } else {
-        s = s * expf((m - mn) * invT) + 1.0f;
-        m = mn;
-    }
+    const float t = __expf((fminf(m, v) - mn) * invT);
+    s = v > m ? fmaf(s, t, 1.0f) : s + t;
+    m = mn;
 }
 // s * exp((m - M) / T), the sum of a partial (m, s) rescaled to a max M >= m
 // (exactly s when m == M, including the empty partial m = M = -inf).
@@ -238,10 +233,7 @@ __device__ __forceinline__ void topk_init(TopkShared &sm, int tid, int nthreads)
         sm.cnt[b] = 0;
         sm.tau[b] = 0ull;
     }
-    for (int i = tid; i < kWarpLists * kBatchChunk; i += nthreads) {
-        sm.wcnt[i / kBatchChunk][i % kBatchChunk] = 0;
-        sm.wtau[i / kBatchChunk][i % kBatchChunk] = 0ull;
-    }
+
     if (tid == 0) {
         sm.need_compact = 0;
         sm.abort_flag = 0;
@@ -287,9 +279,8 @@ __device__ __forceinline__ void topk_round_end(TopkShared &sm, int tid, int nthr
 // first cuts each column to k.
 constexpr int kRankWork = 512;  // comparisons per thread for the direct ranking
 
-__device__ __forceinline__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
-                            int b_off, int batch_total, uint64_t *part_keys, float2 *part_ms,
-                            float invT) {
+__device__ __forceinline__ void topk_write_lists(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
+                                                 int b_off, int batch_total, uint64_t *part_keys) {
     named_bar_sync(kBarAll, nthreads);
     int work = 0;
     for (int b = 0; b < ncols; ++b) work += sm.cnt[b] * sm.cnt[b];
@@ -317,6 +308,12 @@ __device__ __forceinline__ void topk_finish(TopkShared &sm, int tid, int nthread
         if (j >= sm.cnt[b])
             part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + j] = 0ull;
     }
+}
+
+__device__ __forceinline__ void topk_finish(TopkShared &sm, int tid, int nthreads, int ncols, int k, int cap,
+                            int b_off, int batch_total, uint64_t *part_keys, float2 *part_ms,
+                            float invT) {
+    topk_write_lists(sm, tid, nthreads, ncols, k, cap, b_off, batch_total, part_keys);
     if (tid < ncols) {
         // the warps' (m, s): max first, then the rescaled sums (independent exps)
         const int nw = nthreads / 32;
@@ -329,126 +326,239 @@ __device__ __forceinline__ void topk_finish(TopkShared &sm, int tid, int nthread
     }
 }
 
-// ---------------------------------------------------------------------------
-// Per-warp candidate lists.  Each of kWarpLists consumer warps keeps its own
-// list per residual column in its kWarpListSlots slots of cand (column b at
-// b * cap_w, cap_w = kWarpListSlots / pow2(ncols)) and cuts it alone, so the
-// stream has no CTA-wide barrier: a warp cuts its list back to k (sorted,
-// largest first; the k-th key becomes its threshold) once it could not take
-// another kWarpRowsPerRound offers, or holds 2k + 32 keys.  At the end every
-// warp sorts what it holds, and the CTA ranks each key among the union of
-// the sorted lists by binary search.  Used when a column's list holds k plus
-// one round of offers (warp_lists_fit).
-// ---------------------------------------------------------------------------
 __host__ __device__ __forceinline__ int pow2_at_least(int n) {
     int q = 1;
     while (q < n) q <<= 1;
     return q;
 }
-__host__ __device__ __forceinline__ int warp_list_cap(int ncols) { return kWarpListSlots / pow2_at_least(ncols); }
-__host__ __device__ __forceinline__ bool warp_lists_fit(int ncols, int k) {
-    return k >= 1 && k + kWarpRowsPerRound <= warp_list_cap(ncols);
-}
-__device__ __forceinline__ int warp_list_limit(int ncols, int k) {
-    const int a = warp_list_cap(ncols) - kWarpRowsPerRound, b = 2 * k + 32;
-    return a < b ? a : b;
-}
 
-// Offer one logit to warp w's list for column b (any subset of the warp's
-// lanes, one logit each).
-__device__ __forceinline__ void wl_offer(TopkShared &sm, int w, int b, int cap_w, float v, int32_t id) {
-    const uint64_t key = topk_key(v, id);
-    if (key > sm.wtau[w][b]) {
-        const int pos = atomicAdd(&sm.wcnt[w][b], 1);
-        sm.cand[w * kWarpListSlots + b * cap_w + pos] = key;
+// Bitonic sort, largest first, of the warp's 32 * KPL keys: lane l holds
+// elements l, 32 + l, 64 + l, ...  Partners 32 or more apart sit in the same
+// lane; nearer ones in lane l ^ t, exchanged by shuffles.
+template <int KPL>
+__device__ __forceinline__ void warp_sort_desc(uint64_t (&x)[KPL], int lane) {
+    constexpr int N = 32 * KPL;
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+        for (int t = size >> 1; t > 0; t >>= 1) {
+            if (t >= 32) {
+                const int tq = t >> 5;
+#pragma unroll
+                for (int q = 0; q < KPL; ++q) {
+                    const int pq = q ^ tq;
+                    if (pq > q) {  // element i = 32 q + l, partner i + t
+                        const int i = 32 * q + lane;
+                        const bool desc = (i & size) == 0;  // this run sorts largest first
+                        const uint64_t a = x[q], c = x[pq];
+                        const bool swap = desc ? (a < c) : (a > c);
+                        x[q] = swap ? c : a;
+                        x[pq] = swap ? a : c;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < KPL; ++q) {
+                    const int i = 32 * q + lane;
+                    const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, x[q], t);
+                    const bool desc = (i & size) == 0;
+                    const bool lower = (lane & t) == 0;  // the smaller index of the pair
+                    // the lower index keeps the larger key in a descending run
+                    const bool keep_max = desc == lower;
+                    x[q] = keep_max ? (o > x[q] ? o : x[q]) : (o < x[q] ? o : x[q]);
+                }
+            }
+        }
     }
 }
 
-// Warp w's list of column b cut to its best min(n, k), sorted, largest first
-// (keys are unique: a key's rank is its place); the threshold becomes the
-// k-th key once the list holds k.  Warp-collective.
-__device__ __forceinline__ void wl_cut(TopkShared &sm, int w, int b, int cap_w, int k, int lane) {
-    uint64_t *keys = sm.cand + w * kWarpListSlots + b * cap_w;
-    uint64_t *tmp = sm.scratch[w];  // per-warp row (the CTA-wide select is not used in this mode)
-    const int n = sm.wcnt[w][b];
-    for (int i = lane; i < n; i += 32) {
-        const uint64_t key = keys[i];
-        int rank = 0;
-        for (int j = 0; j < n; ++j) rank += keys[j] > key;
-        if (rank < k) tmp[rank] = key;
+// keys[0, n) (n <= 32 KPL) sorted largest first in place, the first min(n, k)
+// written back.  Warp-collective.
+template <int KPL>
+__device__ __forceinline__ void warp_sort_cut(uint64_t *keys, int n, int k, int lane) {
+    uint64_t x[KPL];
+#pragma unroll
+    for (int q = 0; q < KPL; ++q) {
+        const int i = 32 * q + lane;
+        x[q] = i < n ? keys[i] : 0ull;  // 0 is below every key
     }
+    warp_sort_desc<KPL>(x, lane);
     __syncwarp();
     const int m = n < k ? n : k;
-    for (int i = lane; i < m; i += 32) keys[i] = tmp[i];
-    __syncwarp();
-    if (lane == 0) {
-        sm.wcnt[w][b] = m;
-        if (m == k) sm.wtau[w][b] = keys[k - 1];
-    }
-    __syncwarp();
-}
-
-// After a round of the warp's offers: cut the lists that could not take
-// another round.  Warp-collective; ncols and the counts are uniform after
-// the warp barrier.
-__device__ __forceinline__ void wl_round_end(TopkShared &sm, int w, int ncols, int k, int lane) {
-    __syncwarp();
-    const int cap_w = warp_list_cap(ncols), limit = warp_list_limit(ncols, k);
-    for (int b = 0; b < ncols; ++b)
-        if (sm.wcnt[w][b] > limit) wl_cut(sm, w, b, cap_w, k, lane);
-}
-
-// Number of keys greater than `key` in a list sorted largest first.
-__device__ __forceinline__ int count_above(const uint64_t *list, int n, uint64_t key) {
-    int lo = 0, hi = n;  // list[0, lo) > key, list[hi, n) <= key
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (list[mid] > key) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
-
-// End of the pass: every warp sorts (and cuts to k) its lists, then the
-// CTA writes its partial list per column, sorted and padded with 0, and
-// (m, s) from ms_warp, as topk_finish does.  All nthreads consumers call it
-// (warps 0 .. kWarpLists-1 own the lists).
-__device__ __forceinline__ void wl_finish(TopkShared &sm, int tid, int nthreads, int ncols, int k, int b_off,
-                                          int batch_total, uint64_t *part_keys, float2 *part_ms, float invT) {
-    const int w = tid >> 5, lane = tid & 31;
-    const int cap_w = warp_list_cap(ncols);
-    if (w < kWarpLists)
-        for (int b = 0; b < ncols; ++b) wl_cut(sm, w, b, cap_w, k, lane);
-    named_bar_sync(kBarAll, nthreads);
-    // keys: (column b, warp ww, index i) over the columns' lists
-    const int per_col = kWarpLists * k;
-    for (int e = tid; e < ncols * per_col; e += nthreads) {
-        const int b = e / per_col, ww = (e % per_col) / k, i = e % k;
-        if (i >= sm.wcnt[ww][b]) continue;
-        const uint64_t key = sm.cand[ww * kWarpListSlots + b * cap_w + i];
-        int rank = i;
 #pragma unroll
-        for (int o = 0; o < kWarpLists; ++o)
-            if (o != ww) rank += count_above(sm.cand + o * kWarpListSlots + b * cap_w, sm.wcnt[o][b], key);
-        if (rank < k) part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + rank] = key;
-    }
-    for (int e = tid; e < ncols * k; e += nthreads) {
-        const int b = e / k, j = e % k;
-        int total = 0;
-#pragma unroll
-        for (int o = 0; o < kWarpLists; ++o) total += sm.wcnt[o][b];
-        if (j >= total) part_keys[(static_cast<size_t>(blockIdx.x) * batch_total + b_off + b) * k + j] = 0ull;
-    }
-    if (tid < ncols) {
-        const int nw = nthreads / 32;
-        float M = -INFINITY;
-        for (int ww = 0; ww < nw; ++ww) M = fmaxf(M, sm.ms_warp[ww][tid].x);
-        float S = 0.0f;
-#pragma unroll 4
-        for (int ww = 0; ww < nw; ++ww) S += ms_rescaled(sm.ms_warp[ww][tid].x, sm.ms_warp[ww][tid].y, M, invT);
-        part_ms[static_cast<size_t>(blockIdx.x) * batch_total + b_off + tid] = make_float2(M, S);
+    for (int q = 0; q < KPL; ++q)
+        if (32 * q + lane < m) keys[32 * q + lane] = x[q];
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// Selection warp.  The consumer warps of a streaming GEMV only stage each
+// 128-row block's logits, [column][row] f32, in one of two slots (the bytes
+// of scratch / hist) and arrive on the slot's full barrier; one selection
+// warp owns every candidate list of the CTA (column b in cand[b * cap ..],
+// count and threshold in its registers), takes each staged block, folds it
+// into the online softmax (m, s) and its lists, cuts a list back to k with a
+// warp radix select once it holds more than the limit, and releases the
+// slot.  The streaming warps never wait for each other or run the
+// selection; at the end the selection warp writes (m, s) per column and
+// the counts, and after a final barrier the consumers write the lists
+// (topk_write_lists: they have the CTA-wide lists' layout).
+// ---------------------------------------------------------------------------
+constexpr int kSelSlots = 2;
+constexpr int kSelLimitMax = BM;  // lists never exceed kSelLimitMax + BM = 256 keys
+static_assert(sizeof(float) * kSelSlots * kBatchChunk * BM >= sizeof(unsigned) * 256 * kBatchChunk,
+              "the staging slots hold a histogram per column for the final cut");
+static_assert(sizeof(uint64_t) * kBatchChunk * kMaxK >= sizeof(float) * kSelSlots * kBatchChunk * BM,
+              "the staging slots fit in the scratch keys' bytes");
+
+__device__ __forceinline__ float *sel_slot(TopkShared &sm, int blk) {
+    return reinterpret_cast<float *>(sm.scratch) + (blk & 1) * (kBatchChunk * BM);
+}
+// Consumer side: wait until block blk's slot is free (the selection warp has
+// taken block blk - 2); false when the wait ran out.
+__device__ __forceinline__ bool sel_acquire(TopkShared &sm, int blk) {
+    const int n = blk >> 1;
+    return n == 0 || mbar_wait(&sm.sel_empty[blk & 1], (n - 1) & 1, kWaitTimeoutNs);
+}
+// Consumer side: this warp's rows of block blk are staged (every consumer
+// warp arrives once per block, rows or not).
+__device__ __forceinline__ void sel_publish(TopkShared &sm, int blk, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.sel_full[blk & 1]);
+}
+__device__ __forceinline__ void sel_init(TopkShared &sm, int consumer_warps) {
+    for (int i = 0; i < kSelSlots; ++i) {
+        mbar_init(&sm.sel_full[i], consumer_warps);
+        mbar_init(&sm.sel_empty[i], 1);
     }
 }
+
+constexpr int kBarFinal = 14;  // named barrier: consumers + selection warp, end of a pass
+static_assert(sizeof(float2) * kMaxConsumerWarps * kBatchChunk >= sizeof(unsigned) * 256,
+              "ms_warp's bytes hold the selection warp's histogram");
+
+// keys[0, n) (unique, k < n <= 256) cut in place to exactly its k largest,
+// in their original order, by a radix select over 8-bit digits (hist: 256
+// words of shared scratch); returns the k-th largest.  Warp-collective, out
+// of line (its registers stay out of the caller's loop).
+__device__ __noinline__ uint64_t warp_cut_to_k(uint64_t *keys, int n, int k, unsigned *hist, int *sel_digit,
+                                               int *sel_above, int lane) {
+    Group g;
+    g.gtid = lane;
+    g.T = 32;
+    g.bar_id = 0;
+    g.col = 0;
+    uint64_t prefix, mask;
+    group_radix_select(keys, n, k, hist, sel_digit, sel_above, g, prefix, mask);
+    // stable compaction, chunk by chunk: a survivor's new place is at most
+    // its old one, and every lane has read its key before the chunk's writes
+    const unsigned lt = (1u << lane) - 1u;
+    int out = 0;
+    uint64_t kmin = ~0ull;
+    for (int base = 0; base < n; base += 32) {
+        const int i = base + lane;
+        const uint64_t key = i < n ? keys[i] : 0ull;
+        const bool keep = i < n && (key & mask) >= prefix;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+        __syncwarp();
+        if (keep) {
+            keys[out + __popc(bal & lt)] = key;
+            kmin = key < kmin ? key : kmin;
+        }
+        out += __popc(bal);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, kmin, o);
+        kmin = other < kmin ? other : kmin;
+    }
+    __syncwarp();
+    return kmin;
+}
+
+// The selection warp's whole job for one projection pass.  rows_of(blk,
+// row0, rows) gives block blk's first vocab row and row count.  Returns
+// false when it stopped early (timeout or the consumers' abort).
+template <typename RowsOf>
+__device__ __forceinline__ bool sel_run(TopkShared &sm, int nblk, RowsOf rows_of, int ncols, int k, float invT,
+                                        int b_off, int batch_total, float2 *part_ms, int32_t *err, int lane) {
+    const int cap = kCandTotal / pow2_at_least(ncols);
+    int limit = cap - BM;
+    limit = limit < 2 * k + 64 ? limit : 2 * k + 64;
+    limit = limit < kSelLimitMax ? limit : kSelLimitMax;  // >= k for k <= kMaxK
+    uint64_t tau[kBatchChunk];
+    int cnt[kBatchChunk];
+    float ms_m[kBatchChunk], ms_s[kBatchChunk];
+#pragma unroll
+    for (int b = 0; b < kBatchChunk; ++b) {
+        tau[b] = 0ull;
+        cnt[b] = 0;
+        ms_m[b] = -INFINITY;
+        ms_s[b] = 0.0f;
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    bool ok = true;
+    for (int blk = 0; blk < nblk && ok; ++blk) {
+                if (!mbar_wait(&sm.sel_full[blk & 1], (blk >> 1) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+        }
+        int64_t row0;
+        int rows;
+        rows_of(blk, row0, rows);
+        const float *st = sel_slot(sm, blk);
+#pragma unroll
+        for (int b = 0; b < kBatchChunk; ++b) {
+            if (b >= ncols) break;
+#pragma unroll
+            for (int q = 0; q < BM / 32; ++q) {
+                const int r = lane + 32 * q;
+                const bool valid = r < rows;
+                const float v = st[b * BM + r];
+                if (valid) ms_update(ms_m[b], ms_s[b], v, invT);
+                const uint64_t key = topk_key(v, static_cast<int32_t>(row0 + r));
+                const bool pass = valid && key > tau[b];
+                const unsigned mask = __ballot_sync(0xFFFFFFFFu, pass);
+                if (pass) sm.cand[b * cap + cnt[b] + __popc(mask & lt)] = key;
+                cnt[b] += __popc(mask);
+            }
+            if (cnt[b] > limit) {
+                __syncwarp();
+                tau[b] = warp_cut_to_k(sm.cand + b * cap, cnt[b], k, reinterpret_cast<unsigned *>(sm.ms_warp),
+                                       &sm.sel_digit[0], &sm.sel_above[0], lane);
+                cnt[b] = k;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sel_empty[blk & 1]);
+    }
+    if (!ok) {
+        if (lane == 0) {
+            set_err(err, LHS_ERRBIT_TIMEOUT);
+            sm.abort_flag = 1;
+        }
+        __syncwarp();
+        return false;
+    }
+    // (m, s) per column; the counts for the consumers, who sort the lists
+    // after the final barrier (sel_finish)
+#pragma unroll
+    for (int b = 0; b < kBatchChunk; ++b) {
+        if (b >= ncols) break;
+        float M = ms_m[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        float S = ms_rescaled(ms_m[b], ms_s[b], M, invT);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
+        if (lane == 0) {
+            part_ms[static_cast<size_t>(blockIdx.x) * batch_total + b_off + b] = make_float2(M, S);
+            sm.cnt[b] = cnt[b];
+        }
+    }
+    return true;
+}
+
 
 // Row range of CTA c: 16-row units split evenly.
 __device__ __forceinline__ void cta_rows(int64_t V, int G, int c, int64_t &r0, int64_t &r1) {
