@@ -172,6 +172,29 @@ def test_embed_wire_empty_and_nonfinite_rows():
         assert int(err.item()) == (e_ref | e2)
 
 
+@pytest.mark.parametrize("H", [128, 768, 832])
+def test_embed_wire_q8_nonfinite_scales_and_odd_counts(H):
+    # Q8_0 rows whose block scale d is inf or NaN, values that overflow
+    # under a large scale, bad ids, and an odd number of tokens (the i8 path
+    # quantises two tokens per warp)
+    V = 300
+    T = wl.make_table(orc.Q8_0, V, H, cid=620 + H, threads=1)
+    rb = H // 32 * 34
+    T = T.reshape(V, rb).copy()
+    T[3, 34 * 1:34 * 1 + 2] = np.frombuffer(np.uint16(0x7C00).tobytes(), np.uint8)   # d = +inf
+    T[5, 34 * 2:34 * 2 + 2] = np.frombuffer(np.uint16(0x7E00).tobytes(), np.uint8)   # d = NaN
+    T[7, 34 * 0:34 * 0 + 2] = np.frombuffer(np.uint16(0x7BFF).tobytes(), np.uint8)   # d = 65504
+    tab = upload_table(T, orc.Q8_0, V, H)
+    ids = np.concatenate([[3, 5, 7, -2, V + 1, 0], wl.zipf_ids(630 + H, 31, V)]).astype(np.int32)
+    assert len(ids) % 2 == 1
+    for scale in (float(np.float32(np.sqrt(np.float64(H)))), 3e33):
+        x_ref, e_ref = orc.embed(T, orc.Q8_0, V, H, ids, scale)
+        ref_buf, e2 = orc.wire_encode(orc.WIRE_I8, x_ref, layer=1, flags=0, top_k=0)
+        buf, err = lhs.lhs_embed_wire(tab, to_dev(ids), scale, orc.WIRE_I8, 1, 0, 0)
+        assert np.array_equal(buf.cpu().numpy(), ref_buf), scale
+        assert int(err.item()) == (e_ref | e2), scale
+
+
 def test_embed_wire_full_size_gemma_q8():
     w = wl.WORKLOADS["gemma_q8"]
     T = wl.table_for(w)
