@@ -11,6 +11,11 @@ that alternate from call to call, so no call finds its table in L2; smaller
 tables are preceded by an L2 flush outside the timed events; larger ones
 are streamed as they are.
 
+The device step and the lm_head roofline loops replay CUDA graphs of the
+C-ABI calls (captured once; --eager times eager calls), as a serving loop
+would, so the host's launch cost and the per-launch submission gaps stay
+out of the device figures.
+
 Prints one JSON line.  `value` is lm_head top-k residuals per second of the
 headline workload (qwen05b) for the whole job (all ranks).  Under torchrun
 every rank runs its own replica (weak scaling; the path needs no exchange
@@ -75,6 +80,8 @@ def parse_args(argv=None):
                     help="lm_head on a second table of the same shape (an untied lm_head)")
     ap.add_argument("--e2e-eager", action="store_true",
                     help="time the end-to-end step as eager calls instead of replaying it as a CUDA graph")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the device step and the lm_head loops as eager calls instead of CUDA graph replays")
     ap.add_argument("--raw-logits", action="store_true",
                     help="the step's lm_head call returns the full logits (raw-logits mode)")
     ap.add_argument("--wire-accuracy", action="store_true",
@@ -432,6 +439,28 @@ def call(fn_args):
         raise RuntimeError(f"{fn.__name__} -> {rc}")
 
 
+GRAPH_CALLS = 20  # lm_head calls per replayed graph in the roofline loops
+EAGER = False     # --eager: no graphs in the device step and roofline loops
+
+
+def graph_of(calls):
+    """A CUDA graph of direct C-ABI calls ((fn, args) with the stream handle
+    last), captured on torch's capture stream; replay() re-issues them on the
+    current stream, without the host's per-launch cost."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sp = torch.cuda.current_stream().cuda_stream
+        for fn, args in calls:
+            args = list(args)
+            args[-1] = sp
+            rc = fn(*args)
+            if rc != 0:
+                raise RuntimeError(f"{fn.__name__} -> {rc} during capture")
+    torch.cuda.synchronize()
+    return g
+
+
 def run_step(c, i=0):
     for fa in c.steps_by_copy[i % len(c.steps_by_copy)]:
         call(fa)
@@ -513,10 +542,11 @@ def chunk_size(per_call_s: float, flush: bool) -> int:
     return max(1, int(500e-6 / max(per_call_s, 1e-7)))
 
 
-def measure(c, body, seconds=ROOFLINE_SECONDS, sampler=None, min_iters=50, warm=5):
+def measure(c, body, seconds=ROOFLINE_SECONDS, sampler=None, min_iters=50, warm=5, calls_per_body=1):
     """Time `body(i)` for >= `seconds` of device time.  Returns per-call
     mean (over all calls), median and min (over chunks of calls between two
-    events), the iteration count and the clocks sampled while it ran."""
+    events), the iteration count and the clocks sampled while it ran.  One
+    body(i) may issue several calls (a graph replay): calls_per_body."""
     import torch
     for i in range(warm):
         body(i)
@@ -551,8 +581,9 @@ def measure(c, body, seconds=ROOFLINE_SECONDS, sampler=None, min_iters=50, warm=
     t1 = time.time()
     if int(c.err.item()) != 0:
         raise RuntimeError(f"error word {int(c.err.item())} in a timing loop")
+    per = [x / calls_per_body for x in per]
     return {"avg_us": sum(per) / len(per), "median_us": statistics.median(per), "min_us": min(per),
-            "iters": n, "chunk": chunk, "device_s": sum(per) * chunk * 1e-6,
+            "iters": n * calls_per_body, "chunk": chunk * calls_per_body, "device_s": sum(per) * chunk * calls_per_body * 1e-6,
             "clocks": (sampler or NoSampler()).window(t0, t1)}
 
 
@@ -597,10 +628,24 @@ def time_device(c, steps, warmup, world):
     torch.cuda.synchronize()
     if int(c.err.item()) != 0:
         raise RuntimeError(f"error word {int(c.err.item())} during warm-up")
+    per = 1  # steps per timed body
+    if EAGER or c.policy == "flush":
+        step = lambda i: run_step(c, i)
+    else:
+        # graphs of `per` consecutive steps (per divides `steps`), the table
+        # copies alternating inside, so that the steps of one replay overlap
+        # as eager launches do; one graph per starting copy
+        per = next(d for d in (10, 8, 5, 4, 2, 1) if steps % d == 0)
+        nc = len(c.steps_by_copy)
+        graphs = [graph_of([cl for j in range(per) for cl in c.steps_by_copy[(s0 + j) % nc]]) for s0 in range(nc)]
+        step = lambda r: graphs[(r * per) % nc].replay()
+        for r in range(max(1, warmup // per)):
+            step(r)
+        torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    ms = timed_loop(c, lambda i: run_step(c, i), steps)
+    ms = timed_loop(c, step, steps // per) / per
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(world)
@@ -826,10 +871,21 @@ def _free():
 
 
 def lm_measure(c, key, peak, peak_src, seconds, sampler, records, label=None):
-    """The lm_head call of context `c` as a roofline measurement."""
-    m = measure(c, lambda i: call(c.lm_by_copy[i % len(c.lm_by_copy)]), seconds, sampler)
+    """The lm_head call of context `c` as a roofline measurement: a CUDA graph
+    of GRAPH_CALLS back-to-back calls (table copies alternating) replayed,
+    or eager calls when the table is flushed from L2 before every call or
+    --eager asks for them."""
+    if c.policy == "flush" or EAGER:
+        m = measure(c, lambda i: call(c.lm_by_copy[i % len(c.lm_by_copy)]), seconds, sampler)
+    else:
+        g = graph_of([c.lm_by_copy[i % len(c.lm_by_copy)] for i in range(GRAPH_CALLS)])
+        m = measure(c, lambda i: g.replay(), seconds, sampler, calls_per_body=GRAPH_CALLS)
+        del g
+    launch = (f"a CUDA graph of {GRAPH_CALLS} back-to-back calls, replayed"
+              if not (c.policy == "flush" or EAGER) else "eager calls")
     kern = f"{'lhs_logits' if c.raw else 'lhs_logits_topk'} call ({c.lm_launches} kernels)"
     e = roofline_entry(key, kern, m, lm_bytes(c.w, c.B, c.k, c.raw), peak, peak_src, records)
+    e["launch"] = launch
     e["batch"], e["k"] = c.B, c.k
     e["residuals_per_s"] = c.B / (m["avg_us"] * 1e-6)
     return e
@@ -1162,7 +1218,9 @@ def run_wire_accuracy(dev):
 
 
 def main(argv=None):
+    global EAGER
     args = parse_args(argv)
+    EAGER = args.eager
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
@@ -1210,6 +1268,9 @@ def main(argv=None):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+            "launch": ("eager calls" if (args.eager or c.policy == "flush") else
+                       "CUDA graphs of up to 10 consecutive steps (their calls captured once), replayed "
+                       "to make exactly `steps` steps"),
             "scaling": "weak", "vs_baseline": None,
             "dtype": {wl.F32: "f32", wl.F16: "f16", wl.BF16: "bf16", wl.Q8_0: "q8_0"}[c.w.dtype]
                      + "-table/f32-accumulate",
