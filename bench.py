@@ -80,6 +80,10 @@ def parse_args(argv=None):
                     help="lm_head on a second table of the same shape (an untied lm_head)")
     ap.add_argument("--e2e-eager", action="store_true",
                     help="time the end-to-end step as eager calls instead of replaying it as a CUDA graph")
+    ap.add_argument("--profile-case", default=None,
+                    help="run a few calls of one measurement and exit, for an ncu launch list: "
+                         "lm_head:<workload>[:<vocab>[:<batch>]], gather:<workload>, embed_wire_i8:<workload>, "
+                         "codec:<f16|i8>:<encode|decode>")
     ap.add_argument("--eager", action="store_true",
                     help="time the device step and the lm_head loops as eager calls instead of CUDA graph replays")
     ap.add_argument("--raw-logits", action="store_true",
@@ -241,7 +245,8 @@ class NoSampler:
 # ---------------------------------------------------------------------------
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-_LM = ("embedding_lookup_tied_gb300/csrc/lm_head.cu", "embedding_lookup_tied_gb300/csrc/lhs_internal.cuh")
+_LM = ("embedding_lookup_tied_gb300/csrc/lm_head.cu", "embedding_lookup_tied_gb300/csrc/lm_topk.cuh",
+       "embedding_lookup_tied_gb300/csrc/lhs_internal.cuh")
 # the files each recorded measurement's kernels are compiled from: a change
 # to any of them voids its record
 KERNEL_SOURCES = {
@@ -1217,6 +1222,68 @@ def run_wire_accuracy(dev):
     return 0
 
 
+def run_profile_case(case, dev, warm=3, calls=2):
+    """`warm` then `calls` eager calls of one measurement (the sizes of the
+    timed loops), for an ncu launch list; prints what ran."""
+    import ctypes
+
+    import torch
+
+    import embedding_lookup_tied_gb300 as lhs
+    parts = case.split(":")
+    kind = parts[0]
+    L = lhs.lib()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    if kind == "lm_head":
+        vocab = int(parts[2]) if len(parts) > 2 and parts[2] else None
+        batch = int(parts[3]) if len(parts) > 3 else None
+        c = setup(parts[1], batch, dev, vocab)
+        fn = lambda i: call(c.lm_by_copy[i % len(c.lm_by_copy)])
+        what = {"workload": c.w.name, "vocab": c.w.vocab, "batch": c.B, "k": c.k,
+                "kernels_per_call": c.lm_launches}
+    elif kind in ("gather", "embed_wire_i8"):
+        w = wl.WORKLOADS[parts[1]]
+        tab = lhs.lhs_table_init(up(wl.table_for(w), dev), w.vocab, w.hidden, w.dtype)
+        n_ids = 1 << 20
+        ids = up(wl.zipf_ids(w.cid, n_ids, w.vocab, w.zipf_s, w.session_vocab), dev)
+        scale = ctypes.c_float(float(w.embed_scale))
+        if kind == "gather":
+            out = torch.empty((n_ids, w.hidden), dtype=torch.float32, device=dev)
+            args = (ctypes.byref(tab.c), ids.data_ptr(), n_ids, scale, out.data_ptr(), err.data_ptr(), sp)
+            fn = lambda i: L.lhs_embed(*args)
+        else:
+            nb = lhs.lhs_wire_bytes(lhs.LHS_WIRE_I8, n_ids, w.hidden)
+            buf = torch.empty(nb, dtype=torch.uint8, device=dev)
+            args = (ctypes.byref(tab.c), ids.data_ptr(), n_ids, scale, lhs.LHS_WIRE_I8, 0, 0, 0, buf.data_ptr(),
+                    nb, err.data_ptr(), sp)
+            fn = lambda i: L.lhs_embed_wire(*args)
+        what = {"workload": w.name, "ids": n_ids, "kernels_per_call": 1}
+    elif kind == "codec":
+        fmt = {"f16": lhs.LHS_WIRE_F16, "i8": lhs.LHS_WIRE_I8}[parts[1]]
+        seq, H = 65536, 5376
+        x = torch.from_numpy(wl.residuals(77, seq, H, (0.5, 8.0))).to(dev)
+        nb = lhs.lhs_wire_bytes(fmt, seq, H)
+        buf = torch.empty(nb, dtype=torch.uint8, device=dev)
+        enc = (x.data_ptr(), lhs.LHS_F32, seq, H, 0, 0, 0, buf.data_ptr(), nb, err.data_ptr(), sp)
+        dec_out = torch.empty((seq, H), dtype=torch.float32, device=dev)
+        dec = (buf.data_ptr(), nb, seq, H, dec_out.data_ptr(), err.data_ptr(), sp)
+        assert L.lhs_wire_encode(fmt, *enc) == 0
+        fn = (lambda i: L.lhs_wire_encode(fmt, *enc)) if parts[2] == "encode" else (lambda i: L.lhs_wire_decode(fmt, *dec))
+        what = {"format": parts[1], "op": parts[2], "seq_len": seq, "hidden": H, "kernels_per_call": 1}
+    else:
+        raise SystemExit(f"unknown profile case {case}")
+    for i in range(warm + calls):
+        rc = fn(i)
+        if rc not in (None, 0):
+            raise RuntimeError(f"{case}: call returned {rc}")
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"{case}: error word {int(err.item())}")
+    print(json.dumps({"profile_case": case, "warm_calls": warm, "calls": calls, **what}), flush=True)
+    return 0
+
+
 def main(argv=None):
     global EAGER
     args = parse_args(argv)
@@ -1228,6 +1295,10 @@ def main(argv=None):
         import torch
         torch.cuda.set_device(local)
         return run_sweep(torch.device("cuda", local), load_peaks()[0])
+    if args.profile_case:
+        import torch
+        torch.cuda.set_device(local)
+        return run_profile_case(args.profile_case, torch.device("cuda", local))
     if args.wire_accuracy:
         import torch
         torch.cuda.set_device(local)
