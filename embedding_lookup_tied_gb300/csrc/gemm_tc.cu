@@ -23,21 +23,33 @@
 // on the leader's barrier; the leader's commits free the stage, and hand an
 // accumulator to the epilogue, in both CTAs.
 //
-// Top-k in two passes, so that the main pass keeps almost nothing:
-//  * sample pass: every cluster computes ONE tile (a stratified sample of
-//    clusters x 256 vocab rows); each epilogue thread keeps, for each of 32
-//    column groups of the tile, the largest logit, and a merge takes the
-//    exact top-k of all clusters' group maxima.  The k-th of those is a
-//    lower bound of the final k-th logit (the k-th largest of any subset of
-//    the logits never exceeds the k-th largest of all of them), and close
-//    to it: the sample's best logits almost never share a group.  The
-//    sample tile is the first of each cluster's range, and its logits are
-//    kept in global memory (256 KB per cluster), so the main pass reads
-//    them instead of recomputing that tile.
-//  * main pass: every logit below that bound is dropped at once; the few
-//    others go to a per-(cluster, residual) candidate buffer in global
-//    memory, cut back to k by a warp-cooperative bitonic sort if it would
-//    overflow.  The merge selects the final top-k from the buffers.
+// Top-k in one pass with a bound taken from a sample of the logits, so that
+// almost nothing is kept:
+//  * every cluster's first tile is the sample (clusters x 256 vocab rows,
+//    spread evenly over the vocabulary).  Each epilogue thread folds its
+//    residual's 256 logits of that tile into 16 column-group maxima and
+//    publishes them; the tile's accumulator stays in TMEM while the tensor
+//    cores go on with the second tile in the other buffer.
+//  * once every CTA has published (an arrival counter in global memory),
+//    one warp per residual finds the k-th largest of that residual's
+//    clusters x 16 group maxima.  It is a lower bound of the final k-th
+//    logit (the k-th largest of any subset of the logits never exceeds the
+//    k-th largest of all of them), and close to it, since the sample's best
+//    logits rarely share a group.  A second counter tells every thread that
+//    all bounds are written.
+//  * every logit below its residual's bound is then dropped at once, the
+//    first tile's included (read again from TMEM); the few others go to a
+//    per-(cluster, residual) candidate buffer in global memory, cut back to
+//    k by a warp-cooperative bitonic sort if it would overflow.  A merge
+//    kernel selects the final top-k from the buffers.
+// The exchange needs every CTA of the grid resident at once, which the
+// launch sizes for (one wave of clusters); its waits are bounded, and a wait
+// that runs out only drops the bound (every logit is then a candidate), so
+// the result stays exact.  A CTA lets the next kernel launch only after it
+// has published, so a dependent kernel never takes the SM of a CTA that the
+// exchange still waits for.  The two counters are zeroed by a one-thread
+// kernel launched just before, so the workspace may hold anything on entry.
+// Vocabularies under two tiles per cluster skip the sample: no bound.
 //
 // Roles (192 threads): warp 0 — TMA producer; warp 1 — TMEM allocation
 // (with the peer's warp 1) and, in the leader, the single MMA-issuing
@@ -57,33 +69,38 @@ namespace {
 constexpr int GM = 128;                      // residuals per CTA (TMEM lanes)
 constexpr int GN = 256;                      // vocab rows per tile
 constexpr int GK = 64;                       // k per stage: 128 bytes of bf16
-constexpr int kStagesG = 7;
 constexpr int kGemmThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kAccCols = 256;                // f32 columns per accumulator buffer
 constexpr int kTmemCols = 512;               // two buffers
 constexpr int kAStageBytes = GM * GK * 2;    // 16 KB: this CTA's residuals
 constexpr int kBHalfBytes = GN / 2 * GK * 2; // 16 KB: this CTA's half of the table tile
+constexpr int kStagesG = 7;                  // ring stages (a residual box and a table box each)
 constexpr int kPairStageBytes = 2 * (kAStageBytes + kBHalfBytes);  // one stage of both CTAs
 
-enum { kModeRaw = 0, kModeSample = 1, kModeMain = 2 };
-constexpr int kSampleLen = 32;               // sample keys per (cluster, residual)
+enum { kModeRaw = 0, kModeMain = 1, kModeFused = 2 };
+constexpr int kSampleGroups = 16;            // group maxima per (residual, cluster)
+constexpr int kBoundPerLane = 48;            // sample entries per lane of a bound warp: all of them
+                                             // up to 96 clusters, the first 1,536 beyond (a subset
+                                             // still bounds the k-th logit from below)
 
 struct GemmParams {
     int64_t V;
     int K;
     int B;                       // residuals in the call
-    int k;                       // top-k (sample / main)
+    int k;                       // top-k
     float invT;
     int tiles;                   // ceil(V / GN)
     int clusters;                // clusters in the grid
     float *raw;                  // raw: [B x V]
-    uint64_t *keys;              // sample: [clusters][B][32]; main: [clusters][B][cap]
+    uint64_t *keys;              // main / fused: candidate buffers [clusters][B][cap]
     float2 *ms;                  // [clusters][B]
-    const float *sample_logits;  // main: [B][k] top-k logits of the sample, or null
-    int cap;                     // main: candidate buffer entries per (cluster, residual)
-    float *tile_logits;          // sample: writes, main: reads the logits of each cluster's first
-                                 // tile [clusters][2][GM][GN] (null: main computes that tile)
+    int cap;                     // candidate buffer entries per (cluster, residual)
+    uint32_t *sample;            // fused: [B][clusters][kSampleGroups] order keys of the first tile's
+                                 // group maxima
+    uint32_t *bound;             // fused: [B] order key of each residual's bound (0: none)
+    uint32_t *sync;              // fused: arrival counters sync[0] (CTAs that published their
+                                 // sample) and sync[32] (bound warps done), zeroed before the launch
     int32_t *err;
 };
 
@@ -300,6 +317,69 @@ __device__ __forceinline__ uint64_t warp_cut(uint64_t *buf, int n, int kk, int l
     return sel;
 }
 
+// Grid-wide arrival counters of the fused pass (global memory, gpu scope).
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Warp-collective: wait until *ctr >= target, for at most kWaitTimeoutNs.
+// Lane 0 polls; every lane then takes its own acquire, so its later loads
+// see what the arrivals published.  False when the limit ran out.
+__device__ __forceinline__ bool wait_count(const uint32_t *ctr, uint32_t target, int lane) {
+    int ok = 1;
+    if (lane == 0 && ld_acquire_u32(ctr) < target) {
+        const uint64_t t0 = global_ns();
+        while (ld_acquire_u32(ctr) < target) {
+            if (global_ns() - t0 > kWaitTimeoutNs) {
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (ok) (void)ld_acquire_u32(ctr);
+    return ok != 0;
+}
+// Warp-collective: the k-th largest of the n order keys at src, counted with
+// multiplicity (0 when fewer than k are nonzero).  Each lane holds up to
+// kBoundPerLane of them; the result is built bit by bit from the top, a bit
+// kept when at least k keys are >= the prefix with it set.
+__device__ __forceinline__ uint32_t sample_kth(const uint32_t *src, int n, int k, int lane) {
+    uint32_t v[kBoundPerLane];
+#pragma unroll
+    for (int e = 0; e < kBoundPerLane; ++e) {
+        const int i = e * 32 + lane;
+        v[e] = i < n ? __ldcg(src + i) : 0u;
+    }
+    uint32_t T = 0u;
+#pragma unroll 1
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t c = T | (1u << bit);
+        uint32_t cnt = 0u;
+#pragma unroll
+        for (int e = 0; e < kBoundPerLane; ++e) cnt += v[e] >= c ? 1u : 0u;
+        cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+        if (cnt >= static_cast<uint32_t>(k)) T = c;
+    }
+    return T;
+}
+
+// Zeroes the fused pass's two arrival counters, after every earlier kernel
+// of the stream (the previous call's pass and merge) has completed.
+__global__ void gemm_sync_reset_kernel(uint32_t *sync) {
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        sync[0] = 0u;
+        sync[32] = 0u;
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_t,
@@ -310,20 +390,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();          // residual half
     const int cl = blockIdx.x >> 1;                   // cluster index
-    int t0, t1;
-    if (MODE == kModeSample) {  // the first tile of each cluster's range
-        t0 = static_cast<int>((static_cast<int64_t>(p.tiles) * cl) / p.clusters);
-        t1 = t0 + 1;
-    } else {
-        t0 = static_cast<int>((static_cast<int64_t>(p.tiles) * cl) / p.clusters);
-        t1 = static_cast<int>((static_cast<int64_t>(p.tiles) * (cl + 1)) / p.clusters);
-    }
-    // main pass after a sample pass: the first tile's logits are already in
-    // global memory, so the tensor cores start at the second
-    const bool reuse = MODE == kModeMain && p.tile_logits != nullptr && t1 > t0;
-    const int tS = reuse ? t0 + 1 : t0;
+    const int t0 = static_cast<int>((static_cast<int64_t>(p.tiles) * cl) / p.clusters);
+    const int t1 = static_cast<int>((static_cast<int64_t>(p.tiles) * (cl + 1)) / p.clusters);
     const int nk = (p.K + GK - 1) / GK;
-    const uint32_t total = static_cast<uint32_t>(t1 - tS) * nk;
+    const uint32_t total = static_cast<uint32_t>(t1 - t0) * nk;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -345,7 +415,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     cluster_sync_all();  // the peer's barriers exist before anything is multicast to them
-    pdl_trigger();
+    if (MODE != kModeFused) pdl_trigger();  // fused: after this CTA has published its sample
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
@@ -356,34 +426,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // each CTA loads its residuals and its half of the table tile
             // into its own shared memory; both complete on the leader's
             // barrier, which the leader's producer arms for the pair
-            auto full_lead = [&](int s) { return cluster_addr(smem_u32(&sm.full[s]), 0); };
-            auto issue_t = [&](uint32_t j) {
+            auto issue = [&](uint32_t j, bool table, bool resid) {
                 const int s = j % S;
-                const int tile = tS + static_cast<int>(j / nk), kc = static_cast<int>(j % nk);
-                tma_load_2d_pair(sm.b[s], &tm_t, full_lead(s), kc * GK,
-                                 tile * GN + static_cast<int>(rank) * (GN / 2));
+                const int tile = t0 + static_cast<int>(j / nk), kc = static_cast<int>(j % nk);
+                const uint32_t bar = cluster_addr(smem_u32(&sm.full[s]), 0);
+                if (table) {
+                    if (rank == 0) mbar_arrive_expect_tx(&sm.full[s], kPairStageBytes);
+                    tma_load_2d_pair(sm.b[s], &tm_t, bar, kc * GK, tile * GN + static_cast<int>(rank) * (GN / 2));
+                }
+                if (resid) tma_load_2d_pair(sm.a[s], &tm_x, bar, kc * GK, static_cast<int>(rank) * GM);
             };
-            auto issue_x = [&](uint32_t j) {
-                const int s = j % S;
-                tma_load_2d_pair(sm.a[s], &tm_x, full_lead(s), static_cast<int>(j % nk) * GK,
-                                 static_cast<int>(rank) * GM);
-            };
-            // table tiles first (never written by an earlier kernel), then
+            // table boxes first (never written by an earlier kernel), then
             // wait for the residuals' producer
             const uint32_t pre = total < static_cast<uint32_t>(S) ? total : S;
-            for (uint32_t j = 0; j < pre; ++j) {
-                if (rank == 0) mbar_arrive_expect_tx(&sm.full[j], kPairStageBytes);
-                issue_t(j);
-            }
+            for (uint32_t j = 0; j < pre; ++j) issue(j, true, false);
             pdl_wait();
-            for (uint32_t j = 0; j < pre; ++j) issue_x(j);
+            for (uint32_t j = 0; j < pre; ++j) issue(j, false, true);
             uint32_t it = pre;
             for (; it < total; ++it) {
-                const int s = it % S;
-                if (!wait_or_abort(&sm.empty[s], ((it / S) & 1) ^ 1, &sm.abort_flag, p.err)) break;
-                if (rank == 0) mbar_arrive_expect_tx(&sm.full[s], kPairStageBytes);
-                issue_t(it);
-                issue_x(it);
+                if (!wait_or_abort(&sm.empty[it % S], ((it / S) & 1) ^ 1, &sm.abort_flag, p.err)) break;
+                issue(it, true, true);
             }
             // drain: the pair has consumed every issued stage, so no copy,
             // completion or commit is still headed for either CTA
@@ -395,7 +457,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0 && rank == 0) {
             uint32_t it = 0;
             const uint16_t both = 0x3;
-            for (int tile = tS, ti = 0; tile < t1; ++tile, ++ti) {
+            for (int tile = t0, ti = 0; tile < t1; ++tile, ++ti) {
                 const int buf = ti & 1;
                 if (!wait_or_abort(&sm.tmem_empty[buf], ((ti >> 1) & 1) ^ 1, &sm.abort_flag, p.err)) break;
                 tc_fence_after();
@@ -449,51 +511,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&sm.tmem_empty[buf]), 0));
             }
-        } else if (MODE == kModeSample) {
-            // the single tile's logits -> for each of the 32 column groups
-            // {j, j+32, ..., j+224} the largest (logit, row) key.  Any set of
-            // real logits gives a lower bound on the k-th largest; the
-            // group maxima hold nearly all of the tile's top logits.
-            const bool ok = t0 < t1 && wait_or_abort(&sm.tmem_full[0], 0, &sm.abort_flag, p.err);
-            if (__all_sync(0xFFFFFFFFu, ok)) {
-                tc_fence_after();
-                const int64_t v0 = static_cast<int64_t>(t0) * GN;
-                uint64_t best[kSampleLen];
-#pragma unroll
-                for (int j = 0; j < kSampleLen; ++j) best[j] = 0ull;
-                float *keep = p.tile_logits ? p.tile_logits + ((static_cast<size_t>(cl) * 2 + rank) * GM + row) * GN
-                                            : nullptr;
-                for (int c = 0; c < kAccCols / 32; ++c) {
-                    float vals[32];
-                    tmem_ld32(tmem + lane_base + c * 32, vals);
-                    const int64_t vc = v0 + c * 32;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const uint64_t key = topk_key(vals[j], static_cast<int32_t>(vc + j));
-                        if (vc + j < p.V && key > best[j]) best[j] = key;
-                    }
-                    if (keep) {
-                        float4 *d4 = reinterpret_cast<float4 *>(keep + c * 32);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            d4[j] = make_float4(vals[4 * j], vals[4 * j + 1], vals[4 * j + 2], vals[4 * j + 3]);
-                    }
-                }
-                if (valid) {
-                    uint64_t *dst = p.keys + (static_cast<size_t>(cl) * p.B + b) * kSampleLen;
-#pragma unroll
-                    for (int j = 0; j < kSampleLen; ++j) dst[j] = best[j];
-                    p.ms[static_cast<size_t>(cl) * p.B + b] = make_float2(-INFINITY, 0.0f);
-                }
-            }
         } else {
-            // main pass: running softmax; candidates above the sample's k-th
-            // logit into this residual's buffer in global memory
+            // running softmax; candidates not below the bound into this
+            // residual's buffer in global memory
             float m_run = -INFINITY, s_run = 0.0f;
             int cnt = 0;
             uint64_t tau = 0ull;       // exact key every kept entry beats (after a cut)
             float tau_val = -INFINITY; // the logit below which nothing can be kept
-            if (valid && p.sample_logits) tau_val = ld_dep(p.sample_logits + static_cast<size_t>(b) * p.k + p.k - 1);
             const float l2e_invT = 1.4426950408889634f * p.invT;
             uint64_t *cand = p.keys + (static_cast<size_t>(cl) * p.B + (valid ? b : 0)) * p.cap;
             uint64_t *cand_lane0 =
@@ -552,25 +576,80 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if ((mask >> j) & 1u) cand[cnt++] = topk_key(vals[j], static_cast<int32_t>(vc + j));
                 }
             };
-            if (reuse) {
-                // the first tile, from the logits the sample pass kept
-                const float *src = p.tile_logits + ((static_cast<size_t>(cl) * 2 + rank) * GM + row) * GN;
+            int ti_first = 0;  // first tile the loop below takes from TMEM
+            if (MODE == kModeFused) {
+                // (1) the first tile's 16 column-group maxima (groups
+                // {j, j+16, j+32, ...}) as order keys: this thread's part of
+                // the sample.  The accumulator stays in TMEM.
+                const bool ok = t1 > t0 && wait_or_abort(&sm.tmem_full[0], 0, &sm.abort_flag, p.err);
+                const bool ok_all = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld is warp-collective
                 const int64_t v0 = static_cast<int64_t>(t0) * GN;
-                for (int c = 0; c < kAccCols / 32; ++c) {
-                    float vals[32];
-                    const float4 *s4 = reinterpret_cast<const float4 *>(src + c * 32);
+                uint32_t g[kSampleGroups];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float4 f = __ldcg(s4 + j);
-                        vals[4 * j] = f.x;
-                        vals[4 * j + 1] = f.y;
-                        vals[4 * j + 2] = f.z;
-                        vals[4 * j + 3] = f.w;
+                for (int j = 0; j < kSampleGroups; ++j) g[j] = 0u;
+                if (ok_all) {
+                    tc_fence_after();
+                    for (int c = 0; c < kAccCols / 32; ++c) {
+                        float vals[32];
+                        tmem_ld32(tmem + lane_base + c * 32, vals);
+                        const int64_t vc = v0 + c * 32;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (vc + j < p.V) g[j % kSampleGroups] = max(g[j % kSampleGroups], order_key32(vals[j]));
                     }
-                    chunk(vals, v0 + c * 32);
                 }
+                if (valid) {  // zeros (no entry) if the pipeline gave up
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        p.sample + (static_cast<size_t>(b) * p.clusters + cl) * kSampleGroups);
+#pragma unroll
+                    for (int j = 0; j < kSampleGroups / 4; ++j)
+                        dst[j] = make_uint4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
+                }
+                __threadfence();
+                named_bar_sync(1, kEpiThreads);  // the CTA's sample is written
+                if (tid == 2 * 32) {
+                    red_release_add(p.sync, 1u);
+                    pdl_trigger();
+                }
+                // (2) one warp per residual: its bound, once every CTA has
+                // published
+                const int nw = static_cast<int>(gridDim.x) * (kEpiThreads / 32);
+                const int gw = static_cast<int>(blockIdx.x) * (kEpiThreads / 32) + (warp - 2);
+                if (gw < p.B) {
+                    const bool all_in = wait_count(p.sync, gridDim.x, lane);
+                    for (int rb = gw; rb < p.B; rb += nw) {
+                        const uint32_t T =
+                            all_in ? sample_kth(p.sample + static_cast<size_t>(rb) * p.clusters * kSampleGroups,
+                                                p.clusters * kSampleGroups, p.k, lane)
+                                   : 0u;
+                        if (lane == 0) p.bound[rb] = T;
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence();
+                        red_release_add(p.sync + 32, 1u);
+                    }
+                }
+                // (3) this residual's bound (none if the exchange ran out of time)
+                const bool bounds_in = wait_count(p.sync + 32, static_cast<uint32_t>(p.B < nw ? p.B : nw), lane);
+                if (bounds_in && valid) {
+                    const uint32_t T = __ldcg(p.bound + b);
+                    if (T) tau_val = key_value(static_cast<uint64_t>(T) << 32);
+                }
+                // (4) the first tile, filtered by the bound
+                if (ok_all) {
+                    for (int c = 0; c < kAccCols / 32; ++c) {
+                        float vals[32];
+                        tmem_ld32(tmem + lane_base + c * 32, vals);
+                        chunk(vals, v0 + c * 32);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&sm.tmem_empty[0]), 0));
+                }
+                ti_first = 1;
             }
-            for (int tile = tS, ti = 0; tile < t1; ++tile, ++ti) {
+            for (int tile = t0 + ti_first, ti = ti_first; tile < t1; ++tile, ++ti) {
                 const int buf = ti & 1;
                 const bool ok = wait_or_abort(&sm.tmem_full[buf], (ti >> 1) & 1, &sm.abort_flag, p.err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;  // tcgen05.ld is warp-collective
@@ -688,13 +767,7 @@ int gemm_lm_head_clusters(const DeviceInfo &dev) {
     return n;
 }
 
-int gemm_lm_head_sample_len() { return kSampleLen; }
-
-// The sample pass keeps its tile's logits (both CTAs: 2 x GM residuals x GN
-// columns of f32 per cluster) so that the main pass need not recompute them.
-size_t gemm_lm_head_tile_logits_bytes(int clusters) {
-    return static_cast<size_t>(clusters) * 2 * GM * GN * sizeof(float);
-}
+int gemm_lm_head_sample_groups() { return kSampleGroups; }
 
 cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch, int k, float invT,
                                 float *raw, const GemmBuffers &bufs, int32_t *err, int clusters,
@@ -713,31 +786,21 @@ cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch
     p.tiles = static_cast<int>((t.vocab + GN - 1) / GN);
     p.clusters = clusters;
     p.err = err;
+
     if (raw) {
         p.raw = raw;
         return launch_mode<kModeRaw>(tm_x, tm_t, p, dev, stream);
     }
-    cudaError_t e;
-    const float *bound = nullptr;
-    if (bufs.sample_keys) {
-        // sample pass and its merge: the exact top-k of one tile per cluster
-        GemmParams ps = p;
-        ps.keys = bufs.sample_keys;
-        ps.ms = bufs.sample_ms;
-        ps.tile_logits = bufs.tile_logits;
-        e = launch_mode<kModeSample>(tm_x, tm_t, ps, dev, stream);
-        if (e != cudaSuccess) return e;
-        e = launch_merge(bufs.sample_keys, bufs.sample_ms, clusters, kSampleLen, kSampleLen, batch, k,
-                         invT, bufs.sample_ids, bufs.sample_logits, nullptr, dev, stream);
-        if (e != cudaSuccess) return e;
-        bound = bufs.sample_logits;
-    }
     p.keys = bufs.cand;
     p.ms = bufs.ms;
     p.cap = bufs.cap;
-    p.sample_logits = bound;
-    p.tile_logits = bound ? bufs.tile_logits : nullptr;
-    return launch_mode<kModeMain>(tm_x, tm_t, p, dev, stream);
+    if (!bufs.sample) return launch_mode<kModeMain>(tm_x, tm_t, p, dev, stream);
+    p.sample = bufs.sample;
+    p.bound = bufs.bound;
+    p.sync = bufs.sync;
+    const cudaError_t e = launch_pdl(gemm_sync_reset_kernel, dim3(1), dim3(32), 0, stream, bufs.sync);
+    if (e != cudaSuccess) return e;
+    return launch_mode<kModeFused>(tm_x, tm_t, p, dev, stream);
 }
 
 }  // namespace lhs

@@ -535,10 +535,9 @@ struct LmHeadPlan {
     size_t off_x;      // workspace offsets (bytes)
     size_t off_keys;   // partial lists (GEMM: candidate buffers)
     size_t off_ms;
-    size_t off_sample_keys, off_sample_ms, off_sample_ids, off_sample_logits;  // GEMM sample pass
-    size_t off_tile_logits;  // GEMM: the sampled tile's logits, reused by the main pass
+    size_t off_sample, off_bound, off_sync;  // GEMM: first-tile sample, bounds, arrival counters
     int key_stride;    // entries between consecutive partial lists
-    bool sample;       // GEMM: run the sample pass
+    bool sample;       // GEMM: bound the candidates by a first-tile sample
     bool xres;         // tensor-core GEMV: residual operand resident in shared memory (no prep kernel)
     int nst;           // tensor-core GEMVs: TMA ring stages
     size_t bytes;      // total workspace
@@ -584,11 +583,9 @@ cudaError_t launch_merge(const uint64_t *part_keys, const float2 *part_ms, int G
 // Batched lm_head on tcgen05 (bf16 table, bf16 residuals): clusters of two
 // CTAs; see gemm_tc.cu.
 struct GemmBuffers {
-    uint64_t *sample_keys;   // [clusters][batch][32], null: no sample pass
-    float2 *sample_ms;       // [clusters][batch]
-    int32_t *sample_ids;     // [batch][k]
-    float *sample_logits;    // [batch][k]
-    float *tile_logits;      // [clusters][256][256] logits of each cluster's sampled tile
+    uint32_t *sample;        // [batch][clusters][16] first-tile group maxima, null: no sample
+    uint32_t *bound;         // [batch] each residual's bound (order key)
+    uint32_t *sync;          // two arrival counters, 128 bytes apart
     uint64_t *cand;          // [clusters][batch][cap]
     float2 *ms;              // [clusters][batch]
     int cap;
@@ -596,8 +593,7 @@ struct GemmBuffers {
 size_t gemm_lm_head_smem();
 int gemm_lm_head_max_batch();
 int gemm_lm_head_cap(int k);
-int gemm_lm_head_sample_len();
-size_t gemm_lm_head_tile_logits_bytes(int clusters);
+int gemm_lm_head_sample_groups();
 int gemm_lm_head_clusters(const DeviceInfo &dev);
 cudaError_t launch_gemm_lm_head(const lhs_table &t, const void *resid, int batch, int k, float invT,
                                 float *raw, const GemmBuffers &bufs, int32_t *err, int clusters,

@@ -1570,21 +1570,17 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
     off += align_up(static_cast<size_t>(p.grid) * wb * p.key_stride * 8, 256);
     p.off_ms = off;
     off += align_up(static_cast<size_t>(p.grid) * wb * 8, 256);
-    // GEMM sample pass: one tile per cluster, worth it when each cluster
-    // owns at least two tiles
+    // GEMM sample: the first tile of each cluster, worth it when each
+    // cluster owns at least two tiles
     p.sample = gemm && k > 0 && (t.vocab + 255) / 256 >= 2 * static_cast<int64_t>(p.grid);
-    p.off_sample_keys = p.off_sample_ms = p.off_sample_ids = p.off_sample_logits = p.off_tile_logits = off;
+    p.off_sample = p.off_bound = p.off_sync = off;
     if (p.sample) {
-        p.off_sample_keys = off;
-        off += align_up(static_cast<size_t>(p.grid) * wb * gemm_lm_head_sample_len() * 8, 256);
-        p.off_sample_ms = off;
-        off += align_up(static_cast<size_t>(p.grid) * wb * 8, 256);
-        p.off_sample_ids = off;
-        off += align_up(static_cast<size_t>(wb) * k * 4, 256);
-        p.off_sample_logits = off;
-        off += align_up(static_cast<size_t>(wb) * k * 4, 256);
-        p.off_tile_logits = off;
-        off += align_up(gemm_lm_head_tile_logits_bytes(p.grid), 256);
+        p.off_sample = off;
+        off += align_up(static_cast<size_t>(wb) * p.grid * gemm_lm_head_sample_groups() * 4, 256);
+        p.off_bound = off;
+        off += align_up(static_cast<size_t>(wb) * 4, 256);
+        p.off_sync = off;
+        off += 256;
     }
     p.bytes = off;
     *plan = p;
@@ -1593,7 +1589,7 @@ int plan_lm_head(const lhs_table &t, int32_t batch, int32_t k, int32_t resid_dty
 
 int lm_head_launches(const LmHeadPlan &plan, int32_t batch, bool raw) {
     const int chunks = (batch + plan.batch_chunk - 1) / plan.batch_chunk;
-    if (plan.path == 2) return chunks * (raw ? 1 : (plan.sample ? 4 : 2));
+    if (plan.path == 2) return chunks * (raw ? 1 : (plan.sample ? 3 : 2));  // (counter reset +) GEMM + merge
     const int per_chunk = (plan.path == 0 && !plan.xres) ? 2 : 1;  // (prep +) projection
     return chunks * per_chunk + (raw ? 0 : 1);
 }
@@ -1614,11 +1610,9 @@ cudaError_t launch_lm_head(const lhs_table &t, const LmHeadPlan &plan, const voi
 
     if (plan.path == 2) {
         GemmBuffers gb;
-        gb.sample_keys = plan.sample ? reinterpret_cast<uint64_t *>(wsb + plan.off_sample_keys) : nullptr;
-        gb.sample_ms = reinterpret_cast<float2 *>(wsb + plan.off_sample_ms);
-        gb.sample_ids = reinterpret_cast<int32_t *>(wsb + plan.off_sample_ids);
-        gb.sample_logits = reinterpret_cast<float *>(wsb + plan.off_sample_logits);
-        gb.tile_logits = plan.sample ? reinterpret_cast<float *>(wsb + plan.off_tile_logits) : nullptr;
+        gb.sample = plan.sample ? reinterpret_cast<uint32_t *>(wsb + plan.off_sample) : nullptr;
+        gb.bound = reinterpret_cast<uint32_t *>(wsb + plan.off_bound);
+        gb.sync = reinterpret_cast<uint32_t *>(wsb + plan.off_sync);
         gb.cand = part_keys;
         gb.ms = part_ms;
         gb.cap = plan.key_stride;

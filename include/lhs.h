@@ -233,8 +233,8 @@ LHS_API int lhs_logits(const lhs_table *t, const void *d_resid, int32_t resid_dt
  * into the library (each GPU that loads the library holds it until exit).
  * A request whose lhs_logits_topk_workspace() size exceeds that limit
  * returns LHS_ERR_BUFFER_TOO_SMALL and enqueues nothing (with 152 SMs, every
- * batch <= 8 with k <= 128 and hidden <= 65536 fits; a batched bf16 call
- * that runs the sampling pass never does).  The first call on each device
+ * batch <= 8 with k <= 128 and hidden <= 65536 fits, and so does a batched
+ * bf16 call of up to 50 residuals with k <= 96, or 26 with a larger k).  The first call on each device
  * looks up the array's device address (cudaGetSymbolAddress, with that
  * device current), and so does the first call after the device's context
  * has changed (cudaDeviceReset): make those first calls before any stream

@@ -524,7 +524,7 @@ def test_launch_count_follows_the_plan():
     tab4 = upload_table(T4, orc.F16, 512, 4096)
     assert lhs.lhs_logits_topk_launches(tab4, 1, 10, lhs.LHS_F32) == 2
     assert lhs.lhs_logits_topk_launches(tab4, 4, 10, lhs.LHS_F32) == 3
-    assert n(64, 10, lhs.LHS_BF16) in (2, 4)               # GEMM (+ sample pass and its merge)
+    assert n(64, 10, lhs.LHS_BF16) in (2, 3)               # (counter reset +) GEMM + merge
     assert n(64, 0, lhs.LHS_BF16) == 1
     Tq = wl.make_table(orc.Q8_0, 1000, 512, 0.02, cid=253, threads=4)
     tabq = upload_table(Tq, orc.Q8_0, 1000, 512)
@@ -590,10 +590,10 @@ GEMM_CASES = [
     (1000, 96, 200, 64),      # hidden % 64 != 0; three stages
     (700, 64, 256, 128),      # k = 128, two stages; both residual halves
     (3000, 256, 130, 5),      # one residual in the second half
-    (40000, 128, 150, 20),    # >= 2 tiles per cluster: sample pass + main pass
-    (39000, 64, 256, 128),    # sample pass with k = 128 (256-entry buffers)
+    (40000, 128, 150, 20),    # >= 2 tiles per cluster: first-tile sample and its bounds
+    (39000, 64, 256, 128),    # sample with k = 128 (256-entry buffers)
     (5000, 64, 300, 10),      # beyond one cluster's 256 residuals: two passes
-    (40000, 64, 513, 50),     # three passes, each with its sample pass
+    (40000, 64, 513, 50),     # three passes, each with its sample
 ]
 
 

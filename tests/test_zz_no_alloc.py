@@ -57,10 +57,10 @@ def test_noalloc_matches_workspace_call_three_in_a_row():
         (wl.BF16, 20000, 512, 3, 12, 1.0, 31, wl.F32),
         # call 2: CUDA-core GEMV (f32 table), 8 residuals, k 40, other inputs
         (wl.F32, 9000, 256, 8, 40, 0.8, 32, wl.F32),
-        # call 3: tcgen05 GEMM (bf16 table, 16 bf16 residuals), k 8; a vocab
-        # below two tiles per cluster, so no sampling pass (that pass keeps
-        # 256 KB of logits per cluster, more than the array holds)
-        (wl.BF16, 30000, 256, 16, 8, 1.3, 33, wl.BF16),
+        # call 3: tcgen05 GEMM (bf16 table, 16 bf16 residuals), k 8, a vocab
+        # of two tiles per cluster or more: the first-tile sample, its bounds
+        # and the arrival counters live in the array too
+        (wl.BF16, 40000, 256, 16, 8, 1.3, 33, wl.BF16),
     ]
     for dtype, V, H, B, k, T, seed, rdt in cases:
         table_np = wl.make_table(dtype, V, H, 0.02, cid=seed, threads=4)
@@ -77,12 +77,12 @@ def test_noalloc_matches_workspace_call_three_in_a_row():
         assert torch.equal(probs, ref_probs)
 
 
-@pytest.mark.parametrize("case", ["gemv", "gemm_with_sampling_pass"])
+@pytest.mark.parametrize("case", ["gemv", "gemm_full_batch"])
 def test_noalloc_rejects_requests_beyond_its_scratch(case):
     if case == "gemv":
         V, H, B, k, rdt = 262144, 64, 64, 128, lhs.LHS_F32   # partial lists alone > 4 MiB
     else:
-        V, H, B, k, rdt = 100000, 64, 16, 8, lhs.LHS_BF16    # the sampled tiles' logits > 4 MiB
+        V, H, B, k, rdt = 100000, 64, 256, 8, lhs.LHS_BF16   # candidate buffers of 256 residuals > 4 MiB
     table = lhs.lhs_table_init(torch.zeros((V, H), dtype=torch.bfloat16, device="cuda"), V, H,
                                lhs.LHS_BF16)
     need = lhs.lhs_logits_topk_workspace(table, B, k, rdt)
