@@ -666,10 +666,15 @@ def time_e2e(c, steps, graph=False):
     host mirror) laid out [ids | residuals | error word | lm_head outputs |
     wire message | decoded residuals | embeddings], so a step is one
     host-to-device copy (ids, residuals and the zeroed error word), the
-    calls (embed, lm_head, wire encode, wire decode), and one device-to-host
-    copy (the error word and every output), all on the stream of the calls.
-    graph=True captures one step — copies and calls — in a CUDA graph and
-    replays it, so the host's per-call launch cost leaves the loop."""
+    calls (embed, lm_head, wire encode, wire decode), and two device-to-host
+    copies: the embeddings, on a second stream as soon as the gather has
+    written them (so they travel while the lm_head streams its table), and
+    the error word with the other outputs after the last call.  The step
+    ends when both copies have landed (the calls' stream waits for the
+    second one), so the next step's gather never overwrites embeddings still
+    in flight.  graph=True captures one step — copies and calls, both streams
+    — in a CUDA graph and replays it, so the host's per-call launch cost
+    leaves the loop."""
     import torch
     lhs = c.lhs
     dev = c.ids.device
@@ -712,17 +717,28 @@ def time_e2e(c, steps, graph=False):
         d_tlg = view(d_io, "tlg", c.B * c.k * 4, torch.float32, (c.B, c.k))
         d_tpr = view(d_io, "tpr", c.B * c.k * 4, torch.float32, (c.B, c.k))
     in_end = off["err"] + 4              # ids, residuals, error word
-    out0 = off["err"]                    # error word and every output
+    out0 = off["err"]                    # error word and the lm_head / wire outputs
+    emb0 = off["emb"]                    # the embeddings
     out1 = off["emb"] + c.n_ids * H * 4
     h2d = in_end
-    d2h = out1 - out0
+    d2h = (emb0 - out0) + (out1 - emb0)
 
     ncopy = len(c.tables)
+    side = torch.cuda.Stream(device=dev)
+    ev_emb = torch.cuda.Event()
+    ev_back = torch.cuda.Event()
 
     def one(i):
         tab, lmt = c.tables[i % ncopy], c.lm_tables[i % ncopy]
+        main = torch.cuda.current_stream(dev)
         d_io[:in_end].copy_(h_io[:in_end], non_blocking=True)
         lhs.lhs_embed(tab, d_ids, c.scale, out=d_emb, err=d_err)
+        if c.n_ids:
+            ev_emb.record(main)
+            with torch.cuda.stream(side):
+                side.wait_event(ev_emb)
+                h_io[emb0:out1].copy_(d_io[emb0:out1], non_blocking=True)
+                ev_back.record(side)
         if c.raw:
             lhs.lhs_logits(lmt, d_res, out=d_raw, ws=c.ws, err=d_err)
         else:
@@ -730,7 +746,9 @@ def time_e2e(c, steps, graph=False):
                                 err=d_err)
         lhs.lhs_wire_encode(c.fmt, d_res, 0, 0, c.k, buf=d_buf, err=d_err)
         lhs.lhs_wire_decode(c.fmt, d_buf, c.B, H, out=d_dec, err=d_err)
-        h_io[out0:out1].copy_(d_io[out0:out1], non_blocking=True)
+        h_io[out0:emb0].copy_(d_io[out0:emb0], non_blocking=True)
+        if c.n_ids:
+            main.wait_event(ev_back)
 
     for i in range(6):
         one(i)
@@ -1354,7 +1372,8 @@ def main(argv=None):
             "e2e": {"value": world * c.B / (e2e_ms / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "ms_per_step": e2e_ms,
-                    "step": "embed, lm_head top-k, wire encode and wire decode, as in the device step",
+                    "step": "embed, lm_head top-k, wire encode and wire decode, as in the device step; "
+                            "the embeddings copied back on a second stream while the lm_head runs",
                     "launch": ("one CUDA graph per step (the copies and the calls, captured once)" if e2e_graph
                                else "eager calls")},
         }
