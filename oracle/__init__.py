@@ -92,6 +92,10 @@ def _load():
                                                ctypes.c_uint32, ctypes.c_uint32,
                                                ctypes.c_uint32, P, P]),
             "orc_wire_decode": (ctypes.c_int, [ctypes.c_int, P, i64, i32, i32, P, P]),
+            "orc_wire_response_bytes": (i64, [ctypes.c_int, i32, i32]),
+            "orc_wire_encode_response": (ctypes.c_int, [ctypes.c_int, P, i32, i32, ctypes.c_uint32,
+                                                        ctypes.c_float, P, P]),
+            "orc_wire_decode_response": (ctypes.c_int, [ctypes.c_int, P, i64, i32, i32, P, P]),
             "orc_fp8_e4m3_value": (f64, [ctypes.c_uint8]),
             "orc_mixed_row_bytes": (i64, [ctypes.c_int, i32]),
             "orc_embed_mixed": (None, [P, i64, P, P, i64, i32, P, i64, f32, P, P]),
@@ -316,6 +320,39 @@ def wire_encode(fmt: int, x, layer: int = 0, flags: int = 0, top_k: int = 0):
     if rc:
         raise ValueError(f"orc_wire_encode rc={rc}")
     return buf, int(err.value)
+
+
+def wire_response_bytes(fmt: int, seq_len: int, hidden: int) -> int:
+    return int(_load().orc_wire_response_bytes(fmt, seq_len, hidden))
+
+
+def wire_encode_response(fmt: int, x, layer: int = 0, latency_ms: float = 0.0):
+    """Encode float32 [seq_len, hidden] as a single-layer response message
+    ([layer][seq_len][latency_ms] header) -> (bytes as uint8 array, err bits)."""
+    x = _c(x, np.float32)
+    if x.ndim != 2:
+        raise ValueError("x must be [seq_len, hidden]")
+    s, h = x.shape
+    buf = np.zeros(wire_response_bytes(fmt, s, h), np.uint8)
+    err = ctypes.c_int32(0)
+    rc = _load().orc_wire_encode_response(fmt, _ptr(x), s, h, layer, latency_ms, _ptr(buf),
+                                          ctypes.byref(err))
+    if rc:
+        raise ValueError(f"orc_wire_encode_response rc={rc}")
+    return buf, int(err.value)
+
+
+def wire_decode_response(fmt: int, buf, seq_len: int, hidden: int, out=None):
+    """Decode a single-layer response -> (float32 [seq_len, hidden], err
+    bits).  On a malformed message ``out`` is returned untouched."""
+    buf = _c(buf, np.uint8).reshape(-1)
+    x = np.zeros((seq_len, hidden), np.float32) if out is None else out
+    err = ctypes.c_int32(0)
+    rc = _load().orc_wire_decode_response(fmt, _ptr(buf), buf.size, seq_len, hidden, _ptr(x),
+                                          ctypes.byref(err))
+    if rc:
+        raise ValueError(f"orc_wire_decode_response rc={rc}")
+    return x, int(err.value)
 
 
 def wire_decode(fmt: int, buf, seq_len: int, hidden: int, out=None):

@@ -643,6 +643,63 @@ int orc_wire_decode(int fmt, const uint8_t *buf, int64_t buf_bytes, int32_t seq_
     return 0;
 }
 
+/* Single-layer response ([ADR-0009] Wire Layout, "Single-layer response"):
+ * [layer u32 LE][seq_len u32 LE][latency_ms f32 LE], then the payload the
+ * request carries (the same f32 / f16 arrays, the same i8 positions).
+ * Reading: the three formats share this 12-byte header, since the page
+ * keeps every header field unchanged across the formats and calls the i8
+ * response "the same structure" as the request's positions.  The payload
+ * is produced and read by the request codecs above, so the two layouts
+ * cannot drift apart. */
+#define ORC_WIRE_RESPONSE_HEADER 12
+
+int64_t orc_wire_response_bytes(int fmt, int32_t seq_len, int32_t hidden)
+{
+    int64_t req = orc_wire_bytes(fmt, seq_len, hidden);
+    return req < 0 ? -1 : req - ORC_WIRE_HEADER + ORC_WIRE_RESPONSE_HEADER;
+}
+
+int orc_wire_encode_response(int fmt, const float *x, int32_t seq_len, int32_t hidden,
+                             uint32_t layer, float latency_ms, uint8_t *buf, int32_t *err_bits)
+{
+    int64_t req = orc_wire_bytes(fmt, seq_len, hidden);
+    uint8_t *tmp;
+    int rc;
+    if (req < 0) return -1;
+    tmp = (uint8_t *)malloc((size_t)req);
+    if (!tmp) return -3;
+    rc = orc_wire_encode(fmt, x, seq_len, hidden, layer, 0u, 0u, tmp, err_bits);
+    if (rc == 0) {
+        orc_store_u32le(buf + 0, layer);
+        orc_store_u32le(buf + 4, (uint32_t)seq_len);
+        orc_store_u32le(buf + 8, orc_bits_from_f32(latency_ms));
+        memcpy(buf + ORC_WIRE_RESPONSE_HEADER, tmp + ORC_WIRE_HEADER, (size_t)(req - ORC_WIRE_HEADER));
+    }
+    free(tmp);
+    return rc;
+}
+
+/* Decode a response: the same readings as orc_wire_decode (seq_len checked,
+ * i8 zero_point 0). */
+int orc_wire_decode_response(int fmt, const uint8_t *buf, int64_t buf_bytes, int32_t seq_len,
+                             int32_t hidden, float *x, int32_t *err_bits)
+{
+    int64_t need = orc_wire_response_bytes(fmt, seq_len, hidden);
+    uint8_t *tmp;
+    int rc;
+    if (need < 0) return -1;
+    if (buf_bytes < need) return -2;
+    tmp = (uint8_t *)calloc((size_t)(need - ORC_WIRE_RESPONSE_HEADER + ORC_WIRE_HEADER), 1);
+    if (!tmp) return -3;
+    memcpy(tmp, buf, 8);                          /* layer, seq_len */
+    memcpy(tmp + ORC_WIRE_HEADER, buf + ORC_WIRE_RESPONSE_HEADER,
+           (size_t)(need - ORC_WIRE_RESPONSE_HEADER));
+    rc = orc_wire_decode(fmt, tmp, need - ORC_WIRE_RESPONSE_HEADER + ORC_WIRE_HEADER, seq_len, hidden,
+                         x, err_bits);
+    free(tmp);
+    return rc;
+}
+
 /* Array forms of the binary16 helpers (test convenience). */
 void orc_f16_value_array(const uint16_t *src, int64_t n, double *out)
 {

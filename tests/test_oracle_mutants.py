@@ -84,6 +84,10 @@ MUTANTS = [
     ("i8 codes unsigned on decode", "float q = (float)(int8_t)pos[8 + j];", "float q = (float)pos[8 + j];", 1),
     ("i8 zero point unchecked", "if (zp != 0.0f) {", "if (zp != zp) {", 1),
     ("i8 non-finite kept", "if (!isfinite(x[j])) nonfinite = 1;", "if (isnan(x[j])) nonfinite = 1;", 1),
+    ("wire response header order", "orc_store_u32le(buf + 4, (uint32_t)seq_len);\n        orc_store_u32le(buf + 8, orc_bits_from_f32(latency_ms));",
+     "orc_store_u32le(buf + 8, (uint32_t)seq_len);\n        orc_store_u32le(buf + 4, orc_bits_from_f32(latency_ms));", 1),
+    ("wire response latency as an integer", "orc_store_u32le(buf + 8, orc_bits_from_f32(latency_ms));",
+     "orc_store_u32le(buf + 8, (uint32_t)latency_ms);", 1),
     ("wire seq_len unchecked", "if (orc_load_u32le(buf + 4) != (uint32_t)seq_len) {",
      "if (orc_load_u32le(buf + 4) != orc_load_u32le(buf + 4)) {", 1),
     ("wire i8 position stride", "orc_i8_encode_position(x + p * hidden, hidden,\n                                   buf + 16 + p * (8 + (int64_t)hidden), err_bits);",

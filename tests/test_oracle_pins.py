@@ -453,6 +453,64 @@ def test_wire_i8_nonfinite_and_malformed():
         orc.wire_decode(orc.WIRE_F16, orc.wire_encode(orc.WIRE_F16, x)[0], 4, 16)
 
 
+def test_wire_response_header_and_payloads():
+    # ADR-0009 Wire Layout, "Single-layer response": [layer u32][seq_len u32]
+    # [latency_ms f32] (little-endian), then the request's payload
+    g = np.random.default_rng(11)
+    x = g.standard_normal((3, 8)).astype(np.float32) * 3
+    assert orc.wire_response_bytes(orc.WIRE_F32, 3, 8) == 12 + 3 * 8 * 4
+    assert orc.wire_response_bytes(orc.WIRE_F16, 3, 8) == 12 + 3 * 8 * 2
+    assert orc.wire_response_bytes(orc.WIRE_I8, 3, 8) == 12 + 3 * (8 + 8)
+    buf, err = orc.wire_encode_response(orc.WIRE_F32, x, layer=9, latency_ms=2.1)
+    assert err == 0 and buf.size == 12 + 96
+    assert buf[:12].tobytes() == struct.pack("<IIf", 9, 3, 2.1)
+    assert buf[12:].tobytes() == x.astype("<f4").tobytes()
+    y, err = orc.wire_decode_response(orc.WIRE_F32, buf, 3, 8)
+    assert err == 0 and np.array_equal(y.view(np.uint32), x.view(np.uint32))
+    buf, err = orc.wire_encode_response(orc.WIRE_F16, x, layer=4, latency_ms=0.1)
+    assert err == 0 and buf[:12].tobytes() == struct.pack("<IIf", 4, 3, 0.1)
+    assert np.array_equal(np.frombuffer(buf[12:].tobytes(), "<u2"),
+                          x.astype(np.float16).view(np.uint16).reshape(-1))
+    y, err = orc.wire_decode_response(orc.WIRE_F16, buf, 3, 8)
+    assert err == 0 and np.array_equal(y, x.astype(np.float16).astype(np.float32))
+
+
+def test_wire_response_i8_worked_example(golden_dir):
+    ex = _golden(golden_dir, "wire_worked_examples.json")["i8"]
+    x = np.array(ex["x"], np.float32)
+    s, h = x.shape
+    buf, err = orc.wire_encode_response(orc.WIRE_I8, x, layer=ex["layer"], latency_ms=1.5)
+    assert err == 0 and buf.size == 12 + s * (8 + h)
+    assert buf[:12].tobytes() == struct.pack("<IIf", ex["layer"], s, 1.5)
+    for p in range(s):
+        off = 12 + p * (8 + h)
+        scale_bits, zp_bits = struct.unpack("<II", buf[off:off + 8].tobytes())
+        assert scale_bits == int(ex["scale_bits"][p], 16) and zp_bits == 0
+        assert list(buf[off + 8: off + 8 + h].view(np.int8)) == ex["q"][p]
+    y, err = orc.wire_decode_response(orc.WIRE_I8, buf, s, h)
+    assert err == 0
+    assert [[int(v) for v in row] for row in y.view(np.uint32)] == \
+        [[int(b, 16) for b in row] for row in ex["decoded_bits"]]
+
+
+def test_wire_response_malformed():
+    x = np.ones((2, 16), np.float32)
+    canary = np.full((2, 16), 7.0, np.float32)
+    buf, _ = orc.wire_encode_response(orc.WIRE_I8, x, layer=1, latency_ms=0.5)
+    # the header's seq_len (its second word) must match the caller's
+    bad = buf.copy()
+    bad[4:8] = np.frombuffer(struct.pack("<I", 3), np.uint8)
+    y, err = orc.wire_decode_response(orc.WIRE_I8, bad, 2, 16, out=canary.copy())
+    assert err == orc.ERR_MALFORMED and np.all(y == 7.0)
+    # a non-zero zero_point: that position flagged and left untouched
+    bad = buf.copy()
+    bad[12 + 24 + 4:12 + 24 + 8] = np.frombuffer(struct.pack("<f", 0.5), np.uint8)
+    y, err = orc.wire_decode_response(orc.WIRE_I8, bad, 2, 16, out=canary.copy())
+    assert err == orc.ERR_MALFORMED and np.all(y[1] == 7.0) and np.all(y[0] == 1.0)
+    with pytest.raises(ValueError):       # buffer shorter than the message
+        orc.wire_decode_response(orc.WIRE_F16, orc.wire_encode_response(orc.WIRE_F16, x)[0], 4, 16)
+
+
 # ---------------------------------------------------------------------------
 # Mixed-precision rows (HELIX §3 sidecar) and dedup (HELIX Appendix B)
 # ---------------------------------------------------------------------------
