@@ -36,7 +36,8 @@ ABI_SYMBOLS = (
     "lhs_logits_topk_workspace",
     "lhs_logits_topk_launches", "lhs_logits_topk", "lhs_logits", "lhs_logits_topk_noalloc", "lhs_wire_bytes",
     "lhs_wire_encode",
-    "lhs_wire_decode", "lhs_selftest_bounded_wait", "lhs_strerror",
+    "lhs_wire_decode", "lhs_wire_response_bytes", "lhs_wire_encode_response", "lhs_wire_decode_response",
+    "lhs_selftest_bounded_wait", "lhs_strerror",
     "lhs_last_cuda_error", "lhs_version",
 )
 
@@ -93,6 +94,10 @@ def lib() -> ctypes.CDLL:
         "lhs_wire_encode": (ctypes.c_int, [i32, P, i32, i32, i32, u32, u32, u32, P, sz,
                                            P, P]),
         "lhs_wire_decode": (ctypes.c_int, [i32, P, sz, i32, i32, P, P, P]),
+        "lhs_wire_response_bytes": (i64, [i32, i32, i32]),
+        "lhs_wire_encode_response": (ctypes.c_int, [i32, P, i32, i32, i32, u32, ctypes.c_float, P, sz,
+                                                    P, P]),
+        "lhs_wire_decode_response": (ctypes.c_int, [i32, P, sz, i32, i32, P, P, P]),
         "lhs_selftest_bounded_wait": (ctypes.c_int, [P, i64, P]),
         "lhs_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "lhs_last_cuda_error": (ctypes.c_int, []),
@@ -388,6 +393,42 @@ def lhs_wire_decode(fmt: int, buf: torch.Tensor, seq_len: int, hidden: int, out=
     _check(lib().lhs_wire_decode(fmt, _dev(buf, "buf"), buf.numel(), seq_len, hidden,
                                  _dev(out, "x") if seq_len else None, _dev(err, "err"),
                                  _stream(stream)), "lhs_wire_decode")
+    return out, err
+
+
+def lhs_wire_response_bytes(fmt: int, seq_len: int, hidden: int) -> int:
+    return int(lib().lhs_wire_response_bytes(fmt, seq_len, hidden))
+
+
+def lhs_wire_encode_response(fmt: int, x: torch.Tensor, layer: int = 0, latency_ms: float = 0.0,
+                             buf=None, err=None, stream=None):
+    """Encode residuals [seq_len, hidden] (f32 or bf16) as a single-layer
+    response message ([layer][seq_len][latency_ms] header).  Without ``buf``
+    the message is a view 4 bytes into a fresh buffer, so that its payload
+    is 16-byte aligned.  Returns (buf, err word)."""
+    s, h = x.shape
+    n = lhs_wire_response_bytes(fmt, s, h)
+    if n < 0:
+        raise ValueError("bad wire format or shape")
+    if buf is None:
+        buf = torch.empty(n + 4, dtype=torch.uint8, device=x.device)[4:]
+    err = _err_word(err, x.device)
+    _check(lib().lhs_wire_encode_response(fmt, _dev(x, "x") if s else None, _resid_dtype(x), s, h,
+                                          layer, float(latency_ms), _dev(buf, "buf"), buf.numel(),
+                                          _dev(err, "err"), _stream(stream)), "lhs_wire_encode_response")
+    return buf, err
+
+
+def lhs_wire_decode_response(fmt: int, buf: torch.Tensor, seq_len: int, hidden: int, out=None,
+                             err=None, stream=None):
+    """Decode a single-layer response message into f32 [seq_len, hidden].
+    Returns (x, err word)."""
+    if out is None:
+        out = torch.empty((seq_len, hidden), dtype=torch.float32, device=buf.device)
+    err = _err_word(err, buf.device)
+    _check(lib().lhs_wire_decode_response(fmt, _dev(buf, "buf"), buf.numel(), seq_len, hidden,
+                                          _dev(out, "x") if seq_len else None, _dev(err, "err"),
+                                          _stream(stream)), "lhs_wire_decode_response")
     return out, err
 
 

@@ -5,6 +5,8 @@
 #include <cmath>
 #include <mutex>
 
+#include <cstring>
+
 #include "lhs_internal.cuh"
 
 namespace lhs {
@@ -271,8 +273,9 @@ int lhs_wire_encode(int32_t fmt, const void *d_x, int32_t x_dtype, int32_t seq_l
     if (!d_buf || !d_err || !aligned(d_buf, 16) || !aligned(d_err, 4)) return LHS_ERR_INVALID_ARG;
     if (seq_len > 0 && (!d_x || !aligned(d_x, 16))) return LHS_ERR_INVALID_ARG;
     if (buf_bytes < static_cast<size_t>(need)) return LHS_ERR_BUFFER_TOO_SMALL;
-    return cuda_status(launch_wire_encode(fmt, d_x, x_dtype, seq_len, hidden, layer, flags, top_k, d_buf,
-                                          d_err, static_cast<cudaStream_t>(stream)));
+    const WireHdr hdr = {{layer, static_cast<uint32_t>(seq_len), flags, top_k}, 4};
+    return cuda_status(launch_wire_encode(fmt, d_x, x_dtype, seq_len, hidden, hdr, d_buf, d_err,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 int lhs_wire_decode(int32_t fmt, const void *d_buf, size_t buf_bytes, int32_t seq_len, int32_t hidden,
@@ -282,7 +285,39 @@ int lhs_wire_decode(int32_t fmt, const void *d_buf, size_t buf_bytes, int32_t se
     if (!d_buf || !d_err || !aligned(d_buf, 16) || !aligned(d_err, 4)) return LHS_ERR_INVALID_ARG;
     if (seq_len > 0 && (!d_x || !aligned(d_x, 16))) return LHS_ERR_INVALID_ARG;
     if (buf_bytes < static_cast<size_t>(need)) return LHS_ERR_BUFFER_TOO_SMALL;
-    return cuda_status(launch_wire_decode(fmt, d_buf, seq_len, hidden, d_x, d_err,
+    return cuda_status(launch_wire_decode(fmt, d_buf, 16, seq_len, hidden, d_x, d_err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int64_t lhs_wire_response_bytes(int32_t fmt, int32_t seq_len, int32_t hidden) {
+    const int64_t request = lhs_wire_bytes(fmt, seq_len, hidden);
+    return request < 0 ? -1 : request - 16 + 12;  // a 12-byte header instead of 16
+}
+
+int lhs_wire_encode_response(int32_t fmt, const void *d_x, int32_t x_dtype, int32_t seq_len, int32_t hidden,
+                             uint32_t layer, float latency_ms, void *d_buf, size_t buf_bytes, int32_t *d_err,
+                             void *stream) {
+    const int64_t need = lhs_wire_response_bytes(fmt, seq_len, hidden);
+    if (need < 0) return LHS_ERR_INVALID_ARG;
+    if (x_dtype != LHS_F32 && x_dtype != LHS_BF16) return LHS_ERR_INVALID_ARG;
+    if (!d_buf || !d_err || !aligned(d_buf, 4) || !aligned(d_err, 4)) return LHS_ERR_INVALID_ARG;
+    if (seq_len > 0 && (!d_x || !aligned(d_x, 16))) return LHS_ERR_INVALID_ARG;
+    if (buf_bytes < static_cast<size_t>(need)) return LHS_ERR_BUFFER_TOO_SMALL;
+    uint32_t lat;
+    memcpy(&lat, &latency_ms, 4);
+    const WireHdr hdr = {{layer, static_cast<uint32_t>(seq_len), lat, 0u}, 3};
+    return cuda_status(launch_wire_encode(fmt, d_x, x_dtype, seq_len, hidden, hdr, d_buf, d_err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int lhs_wire_decode_response(int32_t fmt, const void *d_buf, size_t buf_bytes, int32_t seq_len, int32_t hidden,
+                             float *d_x, int32_t *d_err, void *stream) {
+    const int64_t need = lhs_wire_response_bytes(fmt, seq_len, hidden);
+    if (need < 0) return LHS_ERR_INVALID_ARG;
+    if (!d_buf || !d_err || !aligned(d_buf, 4) || !aligned(d_err, 4)) return LHS_ERR_INVALID_ARG;
+    if (seq_len > 0 && (!d_x || !aligned(d_x, 16))) return LHS_ERR_INVALID_ARG;
+    if (buf_bytes < static_cast<size_t>(need)) return LHS_ERR_BUFFER_TOO_SMALL;
+    return cuda_status(launch_wire_decode(fmt, d_buf, 12, seq_len, hidden, d_x, d_err,
                                           static_cast<cudaStream_t>(stream)));
 }
 

@@ -445,6 +445,17 @@ __device__ __forceinline__ void write_wire_header(uint8_t *buf, uint32_t layer, 
     *reinterpret_cast<uint4 *>(buf) = make_uint4(layer, seq_len, flags, top_k);
 }
 
+// A message header as little-endian u32 words: the request's 4
+// [layer][seq_len][flags][top_k] or the single-layer response's 3
+// [layer][seq_len][latency_ms bits]; the payload follows at 4 * n bytes.
+struct WireHdr {
+    uint32_t w[4];
+    int n;
+};
+__device__ __forceinline__ void write_hdr(uint8_t *buf, const WireHdr &h) {
+    for (int i = 0; i < h.n; ++i) reinterpret_cast<uint32_t *>(buf)[i] = h.w[i];
+}
+
 // Load of data that the preceding kernel in the stream may have written
 // (residuals, token ids, wire messages, intermediate buffers).  A kernel
 // launched as a programmatic dependent starts before its predecessor has
@@ -516,10 +527,13 @@ cudaError_t launch_embed_mixed(const void *data, int64_t data_bytes, const int64
 cudaError_t launch_embed_wire(const lhs_table &t, const int32_t *ids, int64_t n, float scale, int fmt,
                               uint32_t layer, uint32_t flags, uint32_t top_k, void *buf, int32_t *err,
                               cudaStream_t stream);
+// hdr.n words of header, then the payload (vector paths when the payload
+// and x are 16-byte aligned, element-wise ones otherwise); decode reads the
+// payload at buf + hoff
 cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_len,
-                               int32_t hidden, uint32_t layer, uint32_t flags, uint32_t top_k,
-                               void *buf, int32_t *err, cudaStream_t stream);
-cudaError_t launch_wire_decode(int fmt, const void *buf, int32_t seq_len, int32_t hidden,
+                               int32_t hidden, const WireHdr &hdr, void *buf, int32_t *err,
+                               cudaStream_t stream);
+cudaError_t launch_wire_decode(int fmt, const void *buf, int hoff, int32_t seq_len, int32_t hidden,
                                float *x, int32_t *err, cudaStream_t stream);
 
 // lm_head: plan (workspace layout + kernel choice) and launch

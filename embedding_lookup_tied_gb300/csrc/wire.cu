@@ -15,6 +15,11 @@
 // round-half-even of the binary32 quotient x/scale for every element.
 // Positions start at 16 + p*(hidden+8): 8-byte aligned when hidden % 8 == 0,
 // so the codes move as 8-byte words.
+// The single-layer response (Wire Layout, "Single-layer response") has the
+// 12-byte header [layer u32][seq_len u32][latency_ms f32] and the same
+// payload: every kernel takes the header words and finds the payload after
+// them; the vector paths run when the payload is 16-byte aligned, the
+// element-wise ones otherwise.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -58,14 +63,13 @@ __device__ __forceinline__ void load_x8(const void *x, int64_t g, float (&v)[8])
 // ---- f32 / f16 encode ------------------------------------------------------
 template <int FMT, int XDT, bool VEC>
 __global__ void __launch_bounds__(kEwThreads)
-    encode_ew_kernel(const void *__restrict__ x, int64_t n, uint32_t layer, uint32_t seq_len,
-                     uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf) {
+    encode_ew_kernel(const void *__restrict__ x, int64_t n, WireHdr hdr, uint8_t *__restrict__ buf) {
     pdl_trigger();
     pdl_wait();
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    if (tid == 0) write_wire_header(buf, layer, seq_len, flags, top_k);
-    uint8_t *pay = buf + 16;
+    if (tid == 0) write_hdr(buf, hdr);
+    uint8_t *pay = buf + 4 * hdr.n;
     // f16: 8 values per step (a 16-byte store each); f32: 4 values per step
     // (a warp's stores are whole 32-byte sectors)
     const int per = FMT == LHS_WIRE_F16 ? 8 : 4;
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(kEwThreads)
 // ---- f32 / f16 decode ------------------------------------------------------
 template <int FMT, bool VEC>
 __global__ void __launch_bounds__(kEwThreads)
-    decode_ew_kernel(const uint8_t *__restrict__ buf, int64_t n, uint32_t seq_len,
+    decode_ew_kernel(const uint8_t *__restrict__ buf, int hoff, int64_t n, uint32_t seq_len,
                      float *__restrict__ x, int32_t *err) {
     pdl_trigger();
     pdl_wait();
@@ -107,7 +111,7 @@ __global__ void __launch_bounds__(kEwThreads)
         if (tid == 0) set_err(err, LHS_ERRBIT_MALFORMED);
         return;
     }
-    const uint8_t *pay = buf + 16;
+    const uint8_t *pay = buf + hoff;
     // 4 values per unit: a warp's unit loads and stores are contiguous (512
     // bytes written per instruction, whole 32-byte sectors); kDecUnroll units
     // per thread step, every load issued before the first store
@@ -156,17 +160,17 @@ __global__ void __launch_bounds__(kEwThreads)
 // i8 encode, any alignment or hidden: one CTA per position, element by element.
 template <int XDT>
 __global__ void __launch_bounds__(kI8Threads)
-    encode_i8_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
-                     uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    encode_i8_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, WireHdr hdr,
+                     uint8_t *__restrict__ buf, int32_t *err) {
     pdl_trigger();
     pdl_wait();
     __shared__ float sm_m[kI8Threads / 32];
     __shared__ int sm_f[kI8Threads / 32];
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_wire_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
+        write_hdr(buf, hdr);
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
     for (int64_t p = blockIdx.x; p < seq_len; p += gridDim.x) {
-        uint8_t *pos = buf + 16 + p * stride;
+        uint8_t *pos = buf + 4 * hdr.n + p * stride;
         const int64_t xrow = p * static_cast<int64_t>(hidden);
         float m = 0.0f;
         int nonfinite = 0;
@@ -197,17 +201,17 @@ __global__ void __launch_bounds__(kI8Threads)
 // registers between the block max-reduce and the quantisation.
 template <int XDT>
 __global__ void __launch_bounds__(kI8Threads)
-    encode_i8_cta_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
-                         uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    encode_i8_cta_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, WireHdr hdr,
+                         uint8_t *__restrict__ buf, int32_t *err) {
     pdl_trigger();
     pdl_wait();
     __shared__ float sm_m[kI8Threads / 32];
     __shared__ int sm_f[kI8Threads / 32];
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_wire_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
+        write_hdr(buf, hdr);
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
     for (int64_t p = blockIdx.x; p < seq_len; p += gridDim.x) {
-        uint8_t *pos = buf + 16 + p * stride;
+        uint8_t *pos = buf + 4 * hdr.n + p * stride;
         const int64_t xrow = p * static_cast<int64_t>(hidden);
         float m = 0.0f;
         int nonfinite = 0;
@@ -275,8 +279,8 @@ constexpr int64_t kI8BulkMaxSmem = 200 * 1024;  // kI8Bufs rows: f32 rows up to 
 
 template <int XDT>
 __global__ void __launch_bounds__(kI8BulkThreads)
-    encode_i8_bulk_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
-                          uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    encode_i8_bulk_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, WireHdr hdr,
+                          uint8_t *__restrict__ buf, int32_t *err) {
     extern __shared__ __align__(128) uint8_t rows[];  // [kI8Bufs][row bytes]
     __shared__ uint64_t bar[kI8Bufs];
     __shared__ float sm_m[2][kI8BulkThreads / 32];
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(kI8BulkThreads)
     }
     __syncthreads();
     pdl_wait();
-    if (blockIdx.x == 0 && tid == 0) write_wire_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
+    if (blockIdx.x == 0 && tid == 0) write_hdr(buf, hdr);
     // thread 0: copy of the CTA's j-th position into buffer j % kI8Bufs
     int64_t issued = 0;
     auto issue = [&](int64_t j) {
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kI8BulkThreads)
         }
         const float scale = nonfinite ? 0.0f : __fdiv_rn(m, 127.0f);
         const float rcp = __frcp_rn(scale);
-        uint8_t *pos = buf + 16 + p * stride;
+        uint8_t *pos = buf + 4 * hdr.n + p * stride;
         if (tid == 0) {
             *reinterpret_cast<uint2 *>(pos) = make_uint2(__float_as_uint(scale), 0u);
             if (nonfinite) set_err(err, LHS_ERRBIT_NONFINITE);
@@ -391,12 +395,12 @@ __global__ void __launch_bounds__(kI8BulkThreads)
 // position, two passes (i8_position_warp).
 template <int XDT>
 __global__ void __launch_bounds__(128)
-    encode_i8_warp_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, uint32_t layer,
-                          uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+    encode_i8_warp_kernel(const void *__restrict__ x, int32_t seq_len, int32_t hidden, WireHdr hdr,
+                          uint8_t *__restrict__ buf, int32_t *err) {
     pdl_trigger();
     pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_wire_header(buf, layer, static_cast<uint32_t>(seq_len), flags, top_k);
+        write_hdr(buf, hdr);
     const int lane = threadIdx.x & 31;
     const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -415,14 +419,14 @@ __global__ void __launch_bounds__(128)
                     v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xFFFF0000u);
                 }
             },
-            n4, buf + 16 + p * stride, lane, err);
+            n4, buf + 4 * hdr.n + p * stride, lane, err);
     }
 }
 
 // ---- i8 decode -------------------------------------------------------------
 template <bool VEC>
 __global__ void __launch_bounds__(kI8Threads)
-    decode_i8_kernel(const uint8_t *__restrict__ buf, int32_t seq_len, int32_t hidden,
+    decode_i8_kernel(const uint8_t *__restrict__ buf, int hoff, int32_t seq_len, int32_t hidden,
                      float *__restrict__ x, int32_t *err) {
     pdl_trigger();
     pdl_wait();
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__(kI8Threads)
     }
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
     for (int64_t p = blockIdx.x; p < seq_len; p += gridDim.x) {
-        const uint8_t *pos = buf + 16 + p * stride;
+        const uint8_t *pos = buf + hoff + p * stride;
         float scale, zp;
         uint32_t pre[VEC ? kI8DecCache : 1];
         if (VEC) {
@@ -519,15 +523,15 @@ int resident_ctas_128(const void *kernel, int device) {
 }
 
 cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_len,
-                               int32_t hidden, uint32_t layer, uint32_t flags, uint32_t top_k,
-                               void *buf, int32_t *err, cudaStream_t stream) {
+                               int32_t hidden, const WireHdr &hdr, void *buf, int32_t *err,
+                               cudaStream_t stream) {
     DeviceInfo dev;
     cudaError_t e = device_info(&dev);
     if (e != cudaSuccess) return e;
     uint8_t *b = static_cast<uint8_t *>(buf);
     const int64_t n = static_cast<int64_t>(seq_len) * hidden;
-    const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(buf)) % 16) == 0;
-    const uint32_t s = static_cast<uint32_t>(seq_len);
+    // the vector paths need the payload (and x) on 16-byte boundaries
+    const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(b + 4 * hdr.n)) % 16) == 0;
     const int64_t i8_row = static_cast<int64_t>(hidden) * (x_dtype == LHS_F32 ? 4 : 2);
     if (fmt == LHS_WIRE_I8 && aligned && hidden % 8 == 0 && hidden > 1024 && kI8Bufs * i8_row <= kI8BulkMaxSmem) {
         // rows staged in shared memory, kI8Bufs per CTA; as many CTAs per SM
@@ -553,34 +557,30 @@ cudaError_t launch_wire_encode(int fmt, const void *x, int x_dtype, int32_t seq_
         if (per_sm < 1) per_sm = 1;
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * per_sm;
         const int grid = static_cast<int>(seq_len < 1 ? 1 : (seq_len < cap ? seq_len : cap));
-        return launch_pdl(kern, dim3(grid), dim3(kI8BulkThreads), smem, stream, x, seq_len, hidden, layer, flags,
-                          top_k, b, err);
+        return launch_pdl(kern, dim3(grid), dim3(kI8BulkThreads), smem, stream, x, seq_len, hidden, hdr, b, err);
     }
     if (fmt == LHS_WIRE_I8 && aligned && hidden % 8 == 0 && hidden > 1024) {
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
         const int grid = static_cast<int>(seq_len < 1 ? 1 : (seq_len < cap ? seq_len : cap));
         auto kern = x_dtype == LHS_F32 ? encode_i8_cta_kernel<LHS_F32> : encode_i8_cta_kernel<LHS_BF16>;
-        return launch_pdl(kern, dim3(grid), dim3(kI8Threads), 0, stream, x, seq_len, hidden, layer, flags, top_k,
-                          b, err);
+        return launch_pdl(kern, dim3(grid), dim3(kI8Threads), 0, stream, x, seq_len, hidden, hdr, b, err);
     }
     if (fmt == LHS_WIRE_I8 && aligned && hidden % 8 == 0) {
         const int wps = i8_warps_per_sm(static_cast<int64_t>(hidden) * (x_dtype == LHS_F32 ? 4 : 2));
         auto kern = x_dtype == LHS_F32 ? encode_i8_warp_kernel<LHS_F32> : encode_i8_warp_kernel<LHS_BF16>;
         const int grid = warp_kernel_grid(kern, seq_len, wps, dev.num_sms, dev.device);
-        return launch_pdl(kern, dim3(grid), dim3(128), 0, stream, x, seq_len, hidden, layer, flags, top_k, b,
-                          err);
+        return launch_pdl(kern, dim3(grid), dim3(128), 0, stream, x, seq_len, hidden, hdr, b, err);
     }
     if (fmt == LHS_WIRE_I8) {
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
         int grid = static_cast<int>(seq_len < cap ? seq_len : cap);
         if (grid < 1) grid = 1;
         auto kern = x_dtype == LHS_F32 ? encode_i8_kernel<LHS_F32> : encode_i8_kernel<LHS_BF16>;
-        return launch_pdl(kern, dim3(grid), dim3(kI8Threads), 0, stream, x, seq_len, hidden, layer,
-                          flags, top_k, b, err);
+        return launch_pdl(kern, dim3(grid), dim3(kI8Threads), 0, stream, x, seq_len, hidden, hdr, b, err);
     }
     const bool vec = aligned;
     const int grid = ew_grid(vec ? (n + 7) / 8 : n, dev.num_sms);
-void (*kern)(const void *, int64_t, uint32_t, uint32_t, uint32_t, uint32_t, uint8_t *);
+    void (*kern)(const void *, int64_t, WireHdr, uint8_t *);
     if (fmt == LHS_WIRE_F16) {
         if (x_dtype == LHS_F32) kern = vec ? encode_ew_kernel<LHS_WIRE_F16, LHS_F32, true> : encode_ew_kernel<LHS_WIRE_F16, LHS_F32, false>;
         else kern = vec ? encode_ew_kernel<LHS_WIRE_F16, LHS_BF16, true> : encode_ew_kernel<LHS_WIRE_F16, LHS_BF16, false>;
@@ -588,31 +588,31 @@ void (*kern)(const void *, int64_t, uint32_t, uint32_t, uint32_t, uint32_t, uint
         if (x_dtype == LHS_F32) kern = vec ? encode_ew_kernel<LHS_WIRE_F32, LHS_F32, true> : encode_ew_kernel<LHS_WIRE_F32, LHS_F32, false>;
         else kern = vec ? encode_ew_kernel<LHS_WIRE_F32, LHS_BF16, true> : encode_ew_kernel<LHS_WIRE_F32, LHS_BF16, false>;
     }
-    return launch_pdl(kern, dim3(grid), dim3(kEwThreads), 0, stream, x, n, layer, s, flags, top_k, b);
+    return launch_pdl(kern, dim3(grid), dim3(kEwThreads), 0, stream, x, n, hdr, b);
 }
 
-cudaError_t launch_wire_decode(int fmt, const void *buf, int32_t seq_len, int32_t hidden,
+cudaError_t launch_wire_decode(int fmt, const void *buf, int hoff, int32_t seq_len, int32_t hidden,
                                float *x, int32_t *err, cudaStream_t stream) {
     DeviceInfo dev;
     cudaError_t e = device_info(&dev);
     if (e != cudaSuccess) return e;
     const uint8_t *b = static_cast<const uint8_t *>(buf);
     const int64_t n = static_cast<int64_t>(seq_len) * hidden;
-    const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(buf)) % 16) == 0;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(b + hoff)) % 16) == 0;
     if (fmt == LHS_WIRE_I8) {
         const bool vec = aligned && (hidden % 8 == 0);
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 16;
         int grid = static_cast<int>(seq_len < cap ? seq_len : cap);
         if (grid < 1) grid = 1;
         return launch_pdl(vec ? decode_i8_kernel<true> : decode_i8_kernel<false>, dim3(grid),
-                          dim3(kI8Threads), 0, stream, b, seq_len, hidden, x, err);
+                          dim3(kI8Threads), 0, stream, b, hoff, seq_len, hidden, x, err);
     }
     const int grid = ew_grid(aligned ? (n + 3) / 4 : n, dev.num_sms);
     const uint32_t s = static_cast<uint32_t>(seq_len);
-    void (*kern)(const uint8_t *, int64_t, uint32_t, float *, int32_t *);
+    void (*kern)(const uint8_t *, int, int64_t, uint32_t, float *, int32_t *);
     if (fmt == LHS_WIRE_F16) kern = aligned ? decode_ew_kernel<LHS_WIRE_F16, true> : decode_ew_kernel<LHS_WIRE_F16, false>;
     else kern = aligned ? decode_ew_kernel<LHS_WIRE_F32, true> : decode_ew_kernel<LHS_WIRE_F32, false>;
-    return launch_pdl(kern, dim3(grid), dim3(kEwThreads), 0, stream, b, n, s, x, err);
+    return launch_pdl(kern, dim3(grid), dim3(kEwThreads), 0, stream, b, hoff, n, s, x, err);
 }
 
 }  // namespace lhs

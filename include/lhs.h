@@ -281,6 +281,37 @@ LHS_API int lhs_wire_encode(int32_t fmt, const void *d_x, int32_t x_dtype, int32
 LHS_API int lhs_wire_decode(int32_t fmt, const void *d_buf, size_t buf_bytes, int32_t seq_len,
                     int32_t hidden, float *d_x, int32_t *d_err, void *stream);
 
+/* Step 4, response side — the single-layer response message ("ADR-0009 —
+ * Wire Format Evolution", Wire Layout, "Single-layer response"): a 12-byte
+ * header [layer u32][seq_len u32][latency_ms f32] (little-endian) followed
+ * by the same payload as the request message of the same format (binary32,
+ * binary16, or the i8 positions, with the same rounding, saturation and
+ * error rules).  lhs_wire_response_bytes returns 12 + the payload bytes, or
+ * -1 for bad arguments. */
+LHS_API int64_t lhs_wire_response_bytes(int32_t fmt, int32_t seq_len, int32_t hidden);
+
+/* Encode d_x [seq_len x hidden] of x_dtype (LHS_F32 or LHS_BF16) as a
+ * response message in d_buf (buf_bytes >= lhs_wire_response_bytes).  d_buf
+ * needs 4-byte alignment only; the payload starts 12 bytes in, so a buffer
+ * that starts 4 bytes past a 16-byte boundary puts it on one and takes the
+ * vectorised kernels (any other 4-byte-aligned buffer takes element-wise
+ * ones, with the same bytes).  d_x must be 16-byte aligned.  Errors as for
+ * lhs_wire_encode. */
+LHS_API int lhs_wire_encode_response(int32_t fmt, const void *d_x, int32_t x_dtype,
+                                     int32_t seq_len, int32_t hidden, uint32_t layer,
+                                     float latency_ms, void *d_buf, size_t buf_bytes,
+                                     int32_t *d_err, void *stream);
+
+/* Decode a response message (d_buf 4-byte aligned, d_x 16-byte aligned)
+ * into d_x f32 [seq_len x hidden], with lhs_wire_decode's checks: a header
+ * seq_len other than `seq_len` sets LHS_ERRBIT_MALFORMED and leaves d_x
+ * unwritten; an i8 position whose zero_point is not 0 is flagged and left
+ * unwritten.  Errors as for lhs_wire_decode (against
+ * lhs_wire_response_bytes). */
+LHS_API int lhs_wire_decode_response(int32_t fmt, const void *d_buf, size_t buf_bytes,
+                                     int32_t seq_len, int32_t hidden, float *d_x,
+                                     int32_t *d_err, void *stream);
+
 /* Diagnostic: launch one tiny kernel whose wait on an on-chip barrier is
  * never satisfied, bounded by timeout_ns; the kernel gives up, sets
  * LHS_ERRBIT_TIMEOUT in *d_err and exits normally.  This exercises the same

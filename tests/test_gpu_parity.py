@@ -6,6 +6,7 @@ within 1e-5 (relative) of the oracle evaluated on the GPU's own logits.
 """
 import functools
 import math
+import struct
 
 import numpy as np
 import pytest
@@ -128,6 +129,56 @@ def test_wire_parity(shape, xdt, fmt):
     y, derr = lhs.lhs_wire_decode(fmt, buf, s, h)
     assert same_f32(y.cpu().numpy(), ref_x)
     assert int(derr.item()) == ref_derr == 0
+
+
+@pytest.mark.parametrize("off", [4, 0], ids=["payload16", "payload12"])
+@pytest.mark.parametrize("shape", [(4, 256), (1, 896), (3, 100), (2, 9), (0, 64), (40, 1024),
+                                   (300, 2048), (200, 5376)])
+@pytest.mark.parametrize("xdt", [orc.F32, orc.BF16])
+@pytest.mark.parametrize("fmt", [orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8])
+def test_wire_response_parity(shape, xdt, fmt, off):
+    # single-layer response messages (ADR-0009 Wire Layout): a buffer 4 bytes
+    # past a 16-byte boundary puts the payload on one (vector kernels), a
+    # 16-byte-aligned buffer leaves it 12 bytes past one (element-wise ones)
+    s, h = shape
+    g = np.random.default_rng(7 + s * 1000 + h)
+    x = (g.standard_normal(shape).astype(np.float32) *
+         g.uniform(0.5, 8, (s, 1)).astype(np.float32))
+    if fmt != orc.WIRE_I8:
+        x = _special(x)
+    elif s >= 3:
+        x[1] = 0.0
+        x[2, min(3, h - 1)] = np.inf
+    if xdt == orc.BF16:
+        xs = wl.f32_to_bf16_bits(np.nan_to_num(x, nan=0.0, posinf=3e38, neginf=-3e38))
+        xv = orc.bf16_to_f32(xs).reshape(shape)
+        xd = to_dev(xs).view(torch.bfloat16).reshape(shape)
+    else:
+        xv = x
+        xd = to_dev(x)
+    ref_buf, ref_err = orc.wire_encode_response(fmt, xv, layer=9, latency_ms=2.5)
+    assert lhs.lhs_wire_response_bytes(fmt, s, h) == ref_buf.size
+    pad, n = 256, ref_buf.size
+    raw = torch.full((n + 2 * pad + off,), 0x5A, dtype=torch.uint8, device="cuda")
+    buf = raw[pad + off:pad + off + n]
+    _, err = lhs.lhs_wire_encode_response(fmt, xd, 9, 2.5, buf=buf)
+    assert np.array_equal(buf.cpu().numpy(), ref_buf)
+    assert int(err.item()) == ref_err
+    r = raw.cpu().numpy()
+    assert np.all(r[:pad + off] == 0x5A) and np.all(r[pad + off + n:] == 0x5A)
+    ref_x, ref_derr = orc.wire_decode_response(fmt, ref_buf, s, h)
+    y, derr = lhs.lhs_wire_decode_response(fmt, buf, s, h)
+    assert same_f32(y.cpu().numpy(), ref_x)
+    assert int(derr.item()) == ref_derr == 0
+    if s:
+        # a header seq_len other than the caller's: flagged, output untouched
+        bad = buf.clone() if off == 0 else torch.empty(n + 4, dtype=torch.uint8, device="cuda")[4:]
+        bad.copy_(buf)
+        bad[4:8] = torch.from_numpy(np.frombuffer(struct.pack("<I", s + 1), np.uint8).copy()).cuda()
+        out = torch.full((s, h), 7.0, dtype=torch.float32, device="cuda")
+        _, derr = lhs.lhs_wire_decode_response(fmt, bad, s, h, out=out)
+        assert int(derr.item()) == orc.ERR_MALFORMED
+        assert bool(torch.all(out == 7.0))
 
 
 # ---------------------------------------------------------------------------
