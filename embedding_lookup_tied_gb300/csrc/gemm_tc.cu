@@ -714,19 +714,15 @@ cudaError_t launch_mode(const CUtensorMap &tm_x, const CUtensorMap &tm_t, const 
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = kGemmSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[3];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    // the fused pass's CTAs wait for one another: a cooperative launch,
-    // whose grid the driver makes resident as a whole
-    attr[2].id = cudaLaunchAttributeCooperative;
-    attr[2].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = MODE == kModeFused ? 3 : 2;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_t, p);
 }
 

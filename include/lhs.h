@@ -205,9 +205,10 @@ LHS_API int lhs_logits_topk_launches(const lhs_table *t, int32_t batch, int32_t 
  * LHS_ERR_BUFFER_TOO_SMALL, LHS_ERR_UNSUPPORTED (table dtype / residual
  * dtype pair not served), LHS_ERR_CUDA.  An f16 table with a residual whose
  * magnitude reaches 65504 sets LHS_ERRBIT_NONFINITE.  A bf16 table with
- * more than 8 bf16 residuals runs as a cooperative kernel whose CTAs
- * exchange a top-k bound: it takes every SM at once, so kernels holding SMs
- * on other streams delay its start. */
+ * more than 8 bf16 residuals runs one kernel of one CTA per SM whose CTAs
+ * exchange a top-k bound: kernels holding SMs on other streams hold that
+ * exchange back (for at most 2 s, after which it goes on without the bound,
+ * with the same results). */
 LHS_API int lhs_logits_topk(const lhs_table *t, const void *d_resid, int32_t resid_dtype,
                     int32_t batch, int32_t k, float temperature, int32_t *d_ids,
                     float *d_logits, float *d_probs, void *d_ws, size_t ws_bytes,
