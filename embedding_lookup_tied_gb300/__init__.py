@@ -31,7 +31,8 @@ LIB_PATH = _build.LIB
 
 # Exported symbols of the C-ABI, in declaration order.
 ABI_SYMBOLS = (
-    "lhs_table_init", "lhs_table_info", "lhs_embed", "lhs_embed_wire", "lhs_unique_ids_workspace",
+    "lhs_table_init", "lhs_table_info", "lhs_embed", "lhs_embed_wire", "lhs_embed_wire_response",
+    "lhs_unique_ids_workspace",
     "lhs_unique_ids", "lhs_embed_dedup_workspace", "lhs_embed_dedup", "lhs_embed_mixed",
     "lhs_logits_topk_workspace",
     "lhs_logits_topk_launches", "lhs_logits_topk", "lhs_logits", "lhs_logits_topk_noalloc", "lhs_wire_bytes",
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
         "lhs_embed": (ctypes.c_int, [T, P, i64, ctypes.c_float, P, P, P]),
         "lhs_embed_wire": (ctypes.c_int, [T, P, i64, ctypes.c_float, i32, u32, u32, u32, P,
                                           ctypes.c_size_t, P, P]),
+        "lhs_embed_wire_response": (ctypes.c_int, [T, P, i64, ctypes.c_float, i32, u32, ctypes.c_float, P,
+                                                   sz, P, P]),
         "lhs_unique_ids_workspace": (i64, [i64]),
         "lhs_unique_ids": (ctypes.c_int, [i64, P, i64, P, P, P, P, sz, P, P]),
         "lhs_embed_dedup_workspace": (i64, [T, i64]),
@@ -210,6 +213,28 @@ def lhs_embed_wire(table: Table, ids: torch.Tensor, scale: float, fmt: int, laye
     _check(lib().lhs_embed_wire(ctypes.byref(table.c), _dev(ids, "ids") if n else None, n,
                                 float(scale), fmt, layer, flags, top_k, _dev(buf, "buf"),
                                 buf.numel(), _dev(err, "err"), _stream(stream)), "lhs_embed_wire")
+    return buf, err
+
+
+def lhs_embed_wire_response(table: Table, ids: torch.Tensor, scale: float, fmt: int, layer: int = 0,
+                            latency_ms: float = 0.0, buf=None, err=None, stream=None):
+    """Gather rows ``ids`` scaled by ``scale`` straight into a single-layer
+    response message of format ``fmt``.  Without ``buf`` the message is a
+    view 4 bytes into a fresh buffer, so that its payload is 16-byte
+    aligned.  Returns (buf, err word)."""
+    n = ids.numel()
+    if ids.dtype != torch.int32:
+        raise ValueError("ids must be int32")
+    nb = lhs_wire_response_bytes(fmt, n, table.hidden)
+    if nb < 0:
+        raise ValueError("bad wire format or shape")
+    if buf is None:
+        buf = torch.empty(nb + 4, dtype=torch.uint8, device=table.device)[4:]
+    err = _err_word(err, table.device)
+    _check(lib().lhs_embed_wire_response(ctypes.byref(table.c), _dev(ids, "ids") if n else None, n,
+                                         float(scale), fmt, layer, float(latency_ms), _dev(buf, "buf"),
+                                         buf.numel(), _dev(err, "err"), _stream(stream)),
+           "lhs_embed_wire_response")
     return buf, err
 
 

@@ -8,6 +8,11 @@
 // intermediate: the gather's cost is its output write, which the f16 payload
 // halves and the i8 payload cuts to (hidden + 8) / (4 hidden).
 //
+// The message is either the request (16-byte header) or the single-layer
+// response (12-byte header [layer][seq_len][latency_ms]; ADR-0009 Wire
+// Layout): the kernels take the header words and write the payload after
+// them, with the vector paths when the payload is 16-byte aligned.
+//
 // f32 / f16: one warp per token, 8 elements per lane step (16-byte loads and
 // stores).  i8: one warp per token — max|x| of the scaled row, then the
 // codes (the same steps, in the same binary32 operations, as the i8
@@ -32,16 +37,15 @@ __device__ __forceinline__ bool bad_id(int32_t id, int64_t vocab) {
 template <int DT, int FMT, bool VEC>
 __global__ void __launch_bounds__(kWarps * 32)
     embed_wire_ew_kernel(const uint8_t *__restrict__ table, int64_t vocab, int hidden, int64_t row_bytes,
-                         const int32_t *__restrict__ ids, int64_t n, float scale, uint32_t layer,
-                         uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+                         const int32_t *__restrict__ ids, int64_t n, float scale, WireHdr hdr, uint8_t *__restrict__ buf, int32_t *err) {
     pdl_trigger();
     pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_wire_header(buf, layer, static_cast<uint32_t>(n), flags, top_k);
+        write_hdr(buf, hdr);
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    uint8_t *pay = buf + 16;
+    uint8_t *pay = buf + 4 * hdr.n;
     for (int64_t t = warp0; t < n; t += nwarps) {
         const int32_t id = ld_dep(ids + t);
         const bool bad = bad_id(id, vocab);
@@ -91,21 +95,20 @@ __global__ void __launch_bounds__(kWarps * 32)
 template <int DT>
 __global__ void __launch_bounds__(kI8Threads)
     embed_wire_i8_kernel(const uint8_t *__restrict__ table, int64_t vocab, int hidden, int64_t row_bytes,
-                         const int32_t *__restrict__ ids, int64_t n, float scale, uint32_t layer,
-                         uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+                         const int32_t *__restrict__ ids, int64_t n, float scale, WireHdr hdr, uint8_t *__restrict__ buf, int32_t *err) {
     pdl_trigger();
     pdl_wait();
     __shared__ float sm_m[kI8Threads / 32];
     __shared__ int sm_f[kI8Threads / 32];
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_wire_header(buf, layer, static_cast<uint32_t>(n), flags, top_k);
+        write_hdr(buf, hdr);
     const int64_t stride = static_cast<int64_t>(hidden) + 8;
     for (int64_t p = blockIdx.x; p < n; p += gridDim.x) {
         const int32_t id = ld_dep(ids + p);
         const bool bad = bad_id(id, vocab);  // uniform over the block
         if (bad && threadIdx.x == 0) set_err(err, LHS_ERRBIT_BAD_TOKEN);
         const uint8_t *row = table + static_cast<int64_t>(bad ? 0 : id) * row_bytes;
-        uint8_t *pos = buf + 16 + p * stride;
+        uint8_t *pos = buf + 4 * hdr.n + p * stride;
         auto value = [&](int j) { return bad ? 0.0f : __fmul_rn(row_element<DT>(row, j), scale); };
         float m = 0.0f;
         int nonfinite = 0;
@@ -135,12 +138,11 @@ __global__ void __launch_bounds__(kI8Threads)
 template <int DT>
 __global__ void __launch_bounds__(128)
     embed_wire_i8_warp_kernel(const uint8_t *__restrict__ table, int64_t vocab, int hidden, int64_t row_bytes,
-                              const int32_t *__restrict__ ids, int64_t n, float scale, uint32_t layer,
-                              uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+                              const int32_t *__restrict__ ids, int64_t n, float scale, WireHdr hdr, uint8_t *__restrict__ buf, int32_t *err) {
     pdl_trigger();
     pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_wire_header(buf, layer, static_cast<uint32_t>(n), flags, top_k);
+        write_hdr(buf, hdr);
     const int lane = threadIdx.x & 31;
     const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(128)
                     for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], scale);
                 }
             },
-            ng, buf + 16 + p * stride, lane, err);
+            ng, buf + 4 * hdr.n + p * stride, lane, err);
     }
 }
 
@@ -171,12 +173,11 @@ __global__ void __launch_bounds__(128)
 template <int DT>
 __global__ void __launch_bounds__(128)
     embed_wire_i8_warp4_kernel(const uint8_t *__restrict__ table, int64_t vocab, int hidden, int64_t row_bytes,
-                               const int32_t *__restrict__ ids, int64_t n, float scale, uint32_t layer,
-                               uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err) {
+                               const int32_t *__restrict__ ids, int64_t n, float scale, WireHdr hdr, uint8_t *__restrict__ buf, int32_t *err) {
     pdl_trigger();
     pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_wire_header(buf, layer, static_cast<uint32_t>(n), flags, top_k);
+        write_hdr(buf, hdr);
     const int lane = threadIdx.x & 31;
     const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(128)
                     for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(v[i], scale);
                 }
             },
-            n4, buf + 16 + p * stride, lane, err);
+            n4, buf + 4 * hdr.n + p * stride, lane, err);
     }
 }
 
@@ -305,13 +306,12 @@ __device__ __forceinline__ uint32_t i8_quant4_bounded(const float (&v)[4], float
 template <int DT, int KS, bool FULL>
 __global__ void __launch_bounds__(kRingWarps * 32)
     embed_wire_i8_ring_kernel(const uint8_t *__restrict__ table, int64_t vocab, int hidden, int64_t row_bytes,
-                              const int32_t *__restrict__ ids, int64_t n, float scale, uint32_t layer,
-                              uint32_t flags, uint32_t top_k, uint8_t *__restrict__ buf, int32_t *err, int S) {
+                              const int32_t *__restrict__ ids, int64_t n, float scale, WireHdr hdr, uint8_t *__restrict__ buf, int32_t *err, int S) {
     extern __shared__ __align__(16) uint8_t ring_smem[];
     pdl_trigger();
     pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        write_wire_header(buf, layer, static_cast<uint32_t>(n), flags, top_k);
+        write_hdr(buf, hdr);
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int64_t w = static_cast<int64_t>(blockIdx.x) * kRingWarps + wib;
     const int64_t nw = static_cast<int64_t>(gridDim.x) * kRingWarps;
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(kRingWarps * 32)
         const bool nonfinite = mb >= 0x7F800000u;
         const float qs = nonfinite ? 0.0f : __fdiv_rn(__uint_as_float(mb), 127.0f);
         const float rcp = __frcp_rn(qs);
-        uint8_t *pos = buf + 16 + (w + i * nw) * stride;
+        uint8_t *pos = buf + 4 * hdr.n + (w + i * nw) * stride;
         if (lane == 0) {
             *reinterpret_cast<uint2 *>(pos) = make_uint2(__float_as_uint(qs), 0u);
             if (bad) set_err(err, LHS_ERRBIT_BAD_TOKEN);
@@ -436,11 +436,12 @@ __global__ void __launch_bounds__(kRingWarps * 32)
 
 template <int DT>
 cudaError_t launch_dt(const lhs_table &t, const int32_t *ids, int64_t n, float scale, int fmt,
-                      uint32_t layer, uint32_t flags, uint32_t top_k, uint8_t *buf, int32_t *err,
+                      const WireHdr &hdr, uint8_t *buf, int32_t *err,
                       cudaStream_t stream, int num_sms, int device) {
     const uint8_t *tb = static_cast<const uint8_t *>(t.data);
-    // 8-element steps: rows 16-byte aligned (Q8_0: 2-byte) and hidden % 8 == 0
-    bool vec = t.hidden % 8 == 0;
+    // 8-element steps: rows 16-byte aligned (Q8_0: 2-byte), hidden % 8 == 0,
+    // and the payload after the header on a 16-byte boundary
+    bool vec = t.hidden % 8 == 0 && reinterpret_cast<uintptr_t>(buf + 4 * hdr.n) % 16 == 0;
     if (DT != LHS_Q8_0) vec = vec && (reinterpret_cast<uintptr_t>(t.data) % 16 == 0) && (t.row_bytes % 16 == 0);
     // Q8_0 rows staged whole by 16-byte copies (16-byte multiples at 16-byte
     // aligned addresses): the 2-byte-aligned blocks are then read from shared
@@ -451,8 +452,8 @@ cudaError_t launch_dt(const lhs_table &t, const int32_t *ids, int64_t n, float s
     if (fmt == LHS_WIRE_I8 && vec && stage && t.hidden <= 32 * kI8WarpSteps * 4) {
         const int S = t.row_bytes * 8 <= kRingBytesPerWarp ? 8 : (t.row_bytes * 4 <= kRingBytesPerWarp ? 4 : 2);
         const int ks = (t.hidden / 4 + 31) / 32;  // 1 .. 8, rounded up to even below
-        using Kern = void (*)(const uint8_t *, int64_t, int, int64_t, const int32_t *, int64_t, float, uint32_t,
-                              uint32_t, uint32_t, uint8_t *, int32_t *, int);
+        using Kern = void (*)(const uint8_t *, int64_t, int, int64_t, const int32_t *, int64_t, float, WireHdr,
+                              uint8_t *, int32_t *, int);
         static const Kern kTable[2][4] = {
             {embed_wire_i8_ring_kernel<DT, 2, false>, embed_wire_i8_ring_kernel<DT, 4, false>,
              embed_wire_i8_ring_kernel<DT, 6, false>, embed_wire_i8_ring_kernel<DT, 8, false>},
@@ -482,26 +483,26 @@ cudaError_t launch_dt(const lhs_table &t, const int32_t *ids, int64_t n, float s
         const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
         const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
         return launch_pdl(kern, dim3(grid), dim3(kRingWarps * 32), smem, stream, tb, t.vocab, t.hidden,
-                          t.row_bytes, ids, n, scale, layer, flags, top_k, buf, err, S);
+                          t.row_bytes, ids, n, scale, hdr, buf, err, S);
     }
     if (fmt == LHS_WIRE_I8 && vec && t.hidden <= 32 * kI8WarpSteps * 4) {
         const int wps = i8_warps_per_sm(t.row_bytes);
         const int grid = warp_kernel_grid(embed_wire_i8_warp4_kernel<DT>, n, wps, num_sms, device);
         return launch_pdl(embed_wire_i8_warp4_kernel<DT>, dim3(grid), dim3(128), 0, stream, tb, t.vocab, t.hidden,
-                          t.row_bytes, ids, n, scale, layer, flags, top_k, buf, err);
+                          t.row_bytes, ids, n, scale, hdr, buf, err);
     }
     if (fmt == LHS_WIRE_I8 && vec) {
         const int wps = i8_warps_per_sm(t.row_bytes);
         const int grid = warp_kernel_grid(embed_wire_i8_warp_kernel<DT>, n, wps, num_sms, device);
         return launch_pdl(embed_wire_i8_warp_kernel<DT>, dim3(grid), dim3(128), 0, stream, tb, t.vocab, t.hidden,
-                          t.row_bytes, ids, n, scale, layer, flags, top_k, buf, err);
+                          t.row_bytes, ids, n, scale, hdr, buf, err);
     }
     if (fmt == LHS_WIRE_I8) {
         const int64_t cap = static_cast<int64_t>(num_sms) * 16;
         const int grid = static_cast<int>(n < 1 ? 1 : (n < cap ? n : cap));
         return launch_pdl(embed_wire_i8_kernel<DT>, dim3(grid),
                           dim3(kI8Threads), 0, stream, tb, t.vocab, t.hidden, t.row_bytes, ids, n, scale,
-                          layer, flags, top_k, buf, err);
+                          hdr, buf, err);
     }
     const int64_t blocks_needed = (n + kWarps - 1) / kWarps;
     const int64_t cap = static_cast<int64_t>(num_sms) * 32;
@@ -510,26 +511,25 @@ cudaError_t launch_dt(const lhs_table &t, const int32_t *ids, int64_t n, float s
                  ? (vec ? embed_wire_ew_kernel<DT, LHS_WIRE_F16, true> : embed_wire_ew_kernel<DT, LHS_WIRE_F16, false>)
                  : (vec ? embed_wire_ew_kernel<DT, LHS_WIRE_F32, true> : embed_wire_ew_kernel<DT, LHS_WIRE_F32, false>);
     return launch_pdl(k, dim3(grid), dim3(kWarps * 32), 0, stream, tb, t.vocab, t.hidden, t.row_bytes, ids,
-                      n, scale, layer, flags, top_k, buf, err);
+                      n, scale, hdr, buf, err);
 }
 
 }  // namespace
 
 cudaError_t launch_embed_wire(const lhs_table &t, const int32_t *ids, int64_t n, float scale, int fmt,
-                              uint32_t layer, uint32_t flags, uint32_t top_k, void *buf, int32_t *err,
-                              cudaStream_t stream) {
+                              const WireHdr &hdr, void *buf, int32_t *err, cudaStream_t stream) {
     DeviceInfo dev;
     cudaError_t e = device_info(&dev);
     if (e != cudaSuccess) return e;
     uint8_t *b = static_cast<uint8_t *>(buf);
     switch (t.dtype) {
-    case LHS_F32: return launch_dt<LHS_F32>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream,
+    case LHS_F32: return launch_dt<LHS_F32>(t, ids, n, scale, fmt, hdr, b, err, stream,
                                                    dev.num_sms, dev.device);
-    case LHS_F16: return launch_dt<LHS_F16>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream,
+    case LHS_F16: return launch_dt<LHS_F16>(t, ids, n, scale, fmt, hdr, b, err, stream,
                                                    dev.num_sms, dev.device);
-    case LHS_BF16: return launch_dt<LHS_BF16>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream,
+    case LHS_BF16: return launch_dt<LHS_BF16>(t, ids, n, scale, fmt, hdr, b, err, stream,
                                                    dev.num_sms, dev.device);
-    default: return launch_dt<LHS_Q8_0>(t, ids, n, scale, fmt, layer, flags, top_k, b, err, stream,
+    default: return launch_dt<LHS_Q8_0>(t, ids, n, scale, fmt, hdr, b, err, stream,
                                                    dev.num_sms, dev.device);
     }
 }

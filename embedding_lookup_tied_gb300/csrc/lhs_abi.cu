@@ -126,7 +126,26 @@ int lhs_embed_wire(const lhs_table *t, const int32_t *d_ids, int64_t n, float sc
     if (!d_buf || !d_err || !aligned(d_buf, 16) || !aligned(d_err, 4)) return LHS_ERR_INVALID_ARG;
     if (n > 0 && (!d_ids || !aligned(d_ids, 4))) return LHS_ERR_INVALID_ARG;
     if (buf_bytes < static_cast<size_t>(need)) return LHS_ERR_BUFFER_TOO_SMALL;
-    return cuda_status(launch_embed_wire(*t, d_ids, n, scale, fmt, layer, flags, top_k, d_buf, d_err,
+    const WireHdr hdr = {{layer, static_cast<uint32_t>(n), flags, top_k}, 4};
+    return cuda_status(launch_embed_wire(*t, d_ids, n, scale, fmt, hdr, d_buf, d_err,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int lhs_embed_wire_response(const lhs_table *t, const int32_t *d_ids, int64_t n, float scale, int32_t fmt,
+                            uint32_t layer, float latency_ms, void *d_buf, size_t buf_bytes, int32_t *d_err,
+                            void *stream) {
+    int rc = check_table(t);
+    if (rc) return rc;
+    if (n < 0 || n > INT32_MAX || !std::isfinite(scale)) return LHS_ERR_INVALID_ARG;
+    const int64_t need = lhs_wire_response_bytes(fmt, static_cast<int32_t>(n), t->hidden);
+    if (need < 0) return LHS_ERR_INVALID_ARG;
+    if (!d_buf || !d_err || !aligned(d_buf, 4) || !aligned(d_err, 4)) return LHS_ERR_INVALID_ARG;
+    if (n > 0 && (!d_ids || !aligned(d_ids, 4))) return LHS_ERR_INVALID_ARG;
+    if (buf_bytes < static_cast<size_t>(need)) return LHS_ERR_BUFFER_TOO_SMALL;
+    uint32_t lat;
+    memcpy(&lat, &latency_ms, 4);
+    const WireHdr hdr = {{layer, static_cast<uint32_t>(n), lat, 0u}, 3};
+    return cuda_status(launch_embed_wire(*t, d_ids, n, scale, fmt, hdr, d_buf, d_err,
                                          static_cast<cudaStream_t>(stream)));
 }
 

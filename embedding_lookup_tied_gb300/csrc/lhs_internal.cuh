@@ -525,8 +525,7 @@ cudaError_t launch_embed_mixed(const void *data, int64_t data_bytes, const int64
                                const uint8_t *row_dtype, int64_t vocab, int32_t hidden, const int32_t *ids,
                                int64_t n, float scale, float *out, int32_t *err, cudaStream_t stream);
 cudaError_t launch_embed_wire(const lhs_table &t, const int32_t *ids, int64_t n, float scale, int fmt,
-                              uint32_t layer, uint32_t flags, uint32_t top_k, void *buf, int32_t *err,
-                              cudaStream_t stream);
+                              const WireHdr &hdr, void *buf, int32_t *err, cudaStream_t stream);
 // hdr.n words of header, then the payload (vector paths when the payload
 // and x are 16-byte aligned, element-wise ones otherwise); decode reads the
 // payload at buf + hoff

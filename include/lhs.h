@@ -130,6 +130,19 @@ LHS_API int lhs_embed_wire(const lhs_table *t, const int32_t *d_ids, int64_t n, 
                    int32_t fmt, uint32_t layer, uint32_t flags, uint32_t top_k, void *d_buf,
                    size_t buf_bytes, int32_t *d_err, void *stream);
 
+/* lhs_embed_wire writing the single-layer response message instead (the
+ * embed service's reply in the FFN grid's codec; ADR-0009 Wire Layout,
+ * "Single-layer response"): byte for byte what lhs_wire_encode_response(fmt,
+ * x, LHS_F32, n, hidden, layer, latency_ms, ...) writes for the rows
+ * x = lhs_embed(t, d_ids, n, scale) — the 12-byte header
+ * [layer][n][latency_ms], then the same payload.  d_buf needs 4-byte
+ * alignment; one 4 bytes past a 16-byte boundary puts the payload on one
+ * and takes the vectorised kernels.  buf_bytes >=
+ * lhs_wire_response_bytes(fmt, n, hidden).  Otherwise as lhs_embed_wire. */
+LHS_API int lhs_embed_wire_response(const lhs_table *t, const int32_t *d_ids, int64_t n,
+                                    float scale, int32_t fmt, uint32_t layer, float latency_ms,
+                                    void *d_buf, size_t buf_bytes, int32_t *d_err, void *stream);
+
 /* Dedup (HELIX Columnar Embedding, Appendix B: tokenize, dedupe, then fetch
  * the distinct rows).  For ids d_ids[0..n) and a vocabulary of `vocab` rows:
  *   d_unique  int32 [min(n, vocab)]: the distinct ids in [0, vocab), ascending;

@@ -204,6 +204,32 @@ def test_embed_wire_matches_embed_then_encode(dtype, H, fmt):
     assert canaries_intact(raw, pad)
 
 
+@pytest.mark.parametrize("off", [4, 0], ids=["payload16", "payload12"])
+@pytest.mark.parametrize("dtype,H", [(orc.F32, 256), (orc.F16, 96), (orc.BF16, 64), (orc.Q8_0, 128),
+                                     (orc.Q8_0, 768), (orc.BF16, 7), (orc.F16, 5376)])
+@pytest.mark.parametrize("fmt", [orc.WIRE_F32, orc.WIRE_F16, orc.WIRE_I8])
+def test_embed_wire_response_matches_embed_then_encode(dtype, H, fmt, off):
+    # the embed reply as a single-layer response message (ADR-0009 Wire
+    # Layout), byte for byte the oracle's encode of the oracle's rows
+    V = 700
+    T = wl.make_table(dtype, V, H, 0.02, cid=650 + H, threads=4)
+    ids = np.concatenate([[0, V - 1, -1, V, 5, 5],
+                          wl.zipf_ids(650 + H, 37, V)]).astype(np.int32)
+    scale = float(np.float32(np.sqrt(np.float64(H))))
+    tab = upload_table(T, dtype, V, H)
+    x_ref, e_ref = orc.embed(T, dtype, V, H, ids, scale)
+    ref_buf, e2 = orc.wire_encode_response(fmt, x_ref, layer=7, latency_ms=0.1)
+    assert lhs.lhs_wire_response_bytes(fmt, len(ids), H) == ref_buf.size
+    pad, n = 256, ref_buf.size
+    raw = torch.full((n + 2 * pad + off,), 0x5A, dtype=torch.uint8, device="cuda")
+    buf = raw[pad + off:pad + off + n]
+    _, err = lhs.lhs_embed_wire_response(tab, to_dev(ids), scale, fmt, 7, 0.1, buf=buf)
+    assert np.array_equal(buf.cpu().numpy(), ref_buf)
+    assert int(err.item()) == (e_ref | e2)
+    r = raw.cpu().numpy()
+    assert np.all(r[:pad + off] == 0x5A) and np.all(r[pad + off + n:] == 0x5A)
+
+
 def test_embed_wire_empty_and_nonfinite_rows():
     V, H = 64, 64
     T = wl.make_table(orc.F16, V, H, 0.02, cid=610, threads=1)
