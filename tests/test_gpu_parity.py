@@ -660,6 +660,31 @@ def test_calls_on_a_dirty_workspace(fill):
         assert np.array_equal(raw2.cpu().numpy().view(np.uint32), Lg.view(np.uint32)), rep
 
 
+@pytest.mark.parametrize("fill", [0x00, 0xA5, 0xFF])
+def test_batched_gemm_on_a_dirty_workspace(fill):
+    # the one-pass GEMM keeps arrival counters, the sample and the bounds in
+    # the workspace: whatever it holds on entry (counters already past their
+    # targets, stale samples), every call gives the top-k of its own logits
+    V, H, B, k = 40000, 128, 20, 12   # two tiles per CTA pair or more: sampled bound
+    T = wl.make_table(orc.BF16, V, H, 0.02, cid=293, threads=4)
+    tab = upload_table(T, orc.BF16, V, H)
+    R = wl.residuals(294, B, H, (0.5, 8.0), orc.BF16)
+    rd = _resid_dev(R, orc.BF16)
+    need = lhs.lhs_logits_topk_workspace(tab, B, k, lhs.LHS_BF16)
+    ws = torch.full((need,), fill, dtype=torch.uint8, device="cuda")
+    raw, err = lhs.lhs_logits(tab, rd)
+    assert int(err.item()) == 0
+    Lg = raw.cpu().numpy()
+    for rep in range(3):
+        ids, vals, _, err = lhs.lhs_logits_topk(tab, rd, k, ws=ws)
+        assert int(err.item()) == 0
+        ids, vals = ids.cpu().numpy(), vals.cpu().numpy()
+        for b in range(B):
+            rid, rv = orc.topk_f32(Lg[b], k)
+            assert np.array_equal(ids[b], rid), (rep, b)
+            assert np.array_equal(vals[b].view(np.uint32), rv.view(np.uint32)), (rep, b)
+
+
 GEMM_CASES = [
     # bf16 table, bf16 residuals, batch > 8: tcgen05 GEMM path
     # V, H, B, k
