@@ -194,8 +194,10 @@ LHS_API int lhs_logits_topk_workspace(const lhs_table *t, int32_t batch, int32_t
 
 /* Kernel launches one lhs_logits_topk call (k >= 1) or lhs_logits call
  * (k == 0) with these arguments enqueues on the current device: the
- * projection's passes over the table plus, where it runs as a kernel of its
- * own, the cross-CTA merge.  For launch accounting and CUDA-graph sizing; no
+ * projection's passes over the table (with the residual-operand prep kernel
+ * where one runs, and the batched GEMM's one-thread counter reset) plus,
+ * where it runs as a kernel of its own, the cross-CTA merge.  For launch
+ * accounting and CUDA-graph sizing; no
  * counterpart in the source pages.  Errors as for
  * lhs_logits_topk_workspace. */
 LHS_API int lhs_logits_topk_launches(const lhs_table *t, int32_t batch, int32_t k,
