@@ -82,8 +82,8 @@ def parse_args(argv=None):
                     help="time the end-to-end step as eager calls instead of replaying it as a CUDA graph")
     ap.add_argument("--profile-case", default=None,
                     help="run a few calls of one measurement and exit, for an ncu launch list: "
-                         "lm_head:<workload>[:<vocab>[:<batch>]], gather:<workload>, embed_wire_i8:<workload>, "
-                         "codec:<f16|i8>:<encode|decode>")
+                         "lm_head:<workload>[:<vocab>[:<batch>]], gather:<workload>[:<ids>], "
+                         "embed_wire_i8:<workload>[:<ids>], codec:<f16|i8>:<encode|decode>[:<positions>]")
     ap.add_argument("--eager", action="store_true",
                     help="time the device step and the lm_head loops as eager calls instead of CUDA graph replays")
     ap.add_argument("--raw-logits", action="store_true",
@@ -1263,7 +1263,7 @@ def run_profile_case(case, dev, warm=3, calls=2):
     elif kind in ("gather", "embed_wire_i8"):
         w = wl.WORKLOADS[parts[1]]
         tab = lhs.lhs_table_init(up(wl.table_for(w), dev), w.vocab, w.hidden, w.dtype)
-        n_ids = 1 << 20
+        n_ids = int(parts[2]) if len(parts) > 2 and parts[2] else 1 << 20
         ids = up(wl.zipf_ids(w.cid, n_ids, w.vocab, w.zipf_s, w.session_vocab), dev)
         scale = ctypes.c_float(float(w.embed_scale))
         if kind == "gather":
@@ -1279,7 +1279,7 @@ def run_profile_case(case, dev, warm=3, calls=2):
         what = {"workload": w.name, "ids": n_ids, "kernels_per_call": 1}
     elif kind == "codec":
         fmt = {"f16": lhs.LHS_WIRE_F16, "i8": lhs.LHS_WIRE_I8}[parts[1]]
-        seq, H = 65536, 5376
+        seq, H = (int(parts[3]) if len(parts) > 3 and parts[3] else 65536), 5376
         x = torch.from_numpy(wl.residuals(77, seq, H, (0.5, 8.0))).to(dev)
         nb = lhs.lhs_wire_bytes(fmt, seq, H)
         buf = torch.empty(nb, dtype=torch.uint8, device=dev)
