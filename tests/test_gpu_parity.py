@@ -696,6 +696,8 @@ GEMM_CASES = [
     (39000, 64, 256, 128),    # sample with k = 128 (256-entry buffers)
     (5000, 64, 300, 10),      # beyond one cluster's 256 residuals: two passes
     (40000, 64, 513, 50),     # three passes, each with its sample
+    (40000, 64, 9, 1),        # smallest batch on the GEMM, k = 1, sampled bound
+    (45000, 256, 129, 3),     # one residual in the second CTA of each pair, sampled bound
 ]
 
 
