@@ -336,31 +336,33 @@ __global__ void __launch_bounds__(kRingWarps * 32)
         }
         return __shfl_sync(0xFFFFFFFFu, idbuf, static_cast<int>(i - idbase));
     };
-    auto issue = [&](int64_t i) {  // copy token i's row into slot i % S (one group per token)
+    // S is 2, 4 or 8: a token's slot is its index's low bits (a 64-bit
+    // remainder by a run-time S would cost a division routine per use)
+    const int64_t smask = S - 1;
+    auto issue = [&](int64_t i) {  // copy token i's row into slot i & (S - 1) (one group per token)
         if (i < mine) {
             const int32_t id = id_of(i);
-            if (lane == 0) slot_id[i % S] = id;
+            const int slot = static_cast<int>(i & smask);
+            if (lane == 0) slot_id[slot] = id;
             if (id >= 0 && static_cast<int64_t>(id) < vocab) {
                 const uint8_t *src = table + static_cast<int64_t>(id) * row_bytes;
-                uint8_t *dst = ring + static_cast<size_t>(i % S) * row_bytes;
+                uint8_t *dst = ring + static_cast<size_t>(slot) * row_bytes;
                 for (int c = lane; c < nc; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
             }
         }
         cp_async_commit();
     };
-    // Q8_0: per step, the byte offsets of its block's d and of the aligned
-    // words around its four codes (2-byte aligned), and the byte selector
-    int q8_off_d[KS], q8_off_w[KS];
-    uint32_t q8_sel[KS];
+    // Q8_0: the byte offsets, in step 0, of its block's d and of the aligned
+    // words around its four codes (2-byte aligned), and the byte selector.
+    // Step k (values 4 (lane + 32 k) ..) lies 4 k blocks further on, 136 k
+    // bytes, at the same place in its block: one selector for every step.
+    int q8_d0 = 0, q8_w0 = 0;
+    uint32_t q8_sel = 0x3210u;
     if constexpr (DT == LHS_Q8_0) {
-#pragma unroll
-        for (int k = 0; k < KS; ++k) {
-            const int st = lane + 32 * k;
-            const int o = (st >> 3) * 34 + 2 + (st & 7) * 4;
-            q8_off_d[k] = (st >> 3) * 34;
-            q8_off_w[k] = o & ~3;
-            q8_sel[k] = (o & 3) ? 0x5432u : 0x3210u;
-        }
+        const int o = (lane >> 3) * 34 + 2 + (lane & 7) * 4;
+        q8_d0 = (lane >> 3) * 34;
+        q8_w0 = o & ~3;
+        q8_sel = (o & 3) ? 0x5432u : 0x3210u;
     }
     for (int64_t i = 0; i < S - 1; ++i) issue(i);
     for (int64_t i = 0; i < mine; ++i) {
@@ -370,9 +372,10 @@ __global__ void __launch_bounds__(kRingWarps * 32)
         else if (S == 4) cp_async_wait<3>();
         else cp_async_wait<1>();
         __syncwarp();
-        const int32_t id = slot_id[i % S];
+        const int slot = static_cast<int>(i & smask);
+        const int32_t id = slot_id[slot];
         const bool bad = id < 0 || static_cast<int64_t>(id) >= vocab;
-        const uint8_t *row = bad ? zero_row : ring + static_cast<size_t>(i % S) * row_bytes;
+        const uint8_t *row = bad ? zero_row : ring + static_cast<size_t>(slot) * row_bytes;
         // the scaled row in registers; max |x| as the largest magnitude bit
         // pattern (inf and NaN lie above every finite one).  Q8_0: a value is
         // non-finite only through its block's d (inf / NaN) or an overflow to
@@ -385,11 +388,11 @@ __global__ void __launch_bounds__(kRingWarps * 32)
 #pragma unroll
             for (int k = 0; k < KS; ++k) {
                 if (FULL || lane + 32 * k < n4) {
-                    const float d = f16_bits_to_f32(*reinterpret_cast<const unsigned short *>(row + q8_off_d[k]));
+                    const float d = f16_bits_to_f32(*reinterpret_cast<const unsigned short *>(row + q8_d0 + 136 * k));
                     dbad = dbad || !(fabsf(d) <= 3.402823466e38f);
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(row + q8_off_w[k]);
-                    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(row + q8_off_w[k] + 4);
-                    const uint32_t u = __byte_perm(w0, w1, q8_sel[k]) ^ 0x80808080u;
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(row + q8_w0 + 136 * k);
+                    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(row + q8_w0 + 136 * k + 4);
+                    const uint32_t u = __byte_perm(w0, w1, q8_sel) ^ 0x80808080u;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float qv = __int_as_float(static_cast<int>(__byte_perm(u, 0x4B000000u, 0x7440 + q))) - 8388736.0f;
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(kRingWarps * 32)
                 }
             }
         }
-        __syncwarp();  // every lane has read slot i % S before it is refilled
+        __syncwarp();  // every lane has read the slot before it is refilled
         mb = __reduce_max_sync(0xFFFFFFFFu, mb);
         const bool nonfinite = mb >= 0x7F800000u;
         const float qs = nonfinite ? 0.0f : __fdiv_rn(__uint_as_float(mb), 127.0f);
