@@ -60,6 +60,16 @@ def test_wire_bytes_formula(L):
     assert L.lhs_wire_bytes(0, 1, 0) == -1
 
 
+def test_wire_response_bytes_formula(L):
+    # the single-layer response: the request's payload after a 12-byte header
+    for fmt, s, h in ((0, 3, 8), (1, 3, 8), (2, 3, 8), (2, 256, 5120), (1, 0, 64)):
+        assert L.lhs_wire_response_bytes(fmt, s, h) == L.lhs_wire_bytes(fmt, s, h) - 4
+    assert L.lhs_wire_response_bytes(2, 3, 8) == 12 + 3 * 16
+    assert L.lhs_wire_response_bytes(3, 1, 1) == -1
+    assert L.lhs_wire_response_bytes(0, -1, 8) == -1
+    assert L.lhs_wire_response_bytes(0, 1, 0) == -1
+
+
 FAKE = 0x10000  # an aligned address that is never dereferenced by these calls
 
 
@@ -104,6 +114,21 @@ def test_host_checks_reject_before_any_launch(L):
         lhs.LHS_ERR_INVALID_ARG
     assert L.lhs_wire_decode(2, P + 8, 1 << 20, 2, 64, P, P, None) == lhs.LHS_ERR_INVALID_ARG
     assert L.lhs_wire_decode(2, P, 100, 2, 64, P, P, None) == lhs.LHS_ERR_BUFFER_TOO_SMALL
+    # response messages: 4-byte alignment is enough for the buffer (a
+    # payload 12 bytes in), not less; sizes against the response size
+    assert L.lhs_wire_encode_response(1, P, 0, 2, 64, 0, ctypes.c_float(0.5), P + 2, 1 << 20, P,
+                                      None) == lhs.LHS_ERR_INVALID_ARG
+    assert L.lhs_wire_encode_response(1, P, 0, 2, 64, 0, ctypes.c_float(0.5), P + 4, 12 + 255, P,
+                                      None) == lhs.LHS_ERR_BUFFER_TOO_SMALL
+    assert L.lhs_wire_encode_response(1, P + 4, 0, 2, 64, 0, ctypes.c_float(0.5), P, 1 << 20, P,
+                                      None) == lhs.LHS_ERR_INVALID_ARG
+    assert L.lhs_wire_decode_response(2, P + 2, 1 << 20, 2, 64, P, P, None) == lhs.LHS_ERR_INVALID_ARG
+    assert L.lhs_wire_decode_response(2, P + 4, 12 + 2 * 72 - 1, 2, 64, P, P, None) == \
+        lhs.LHS_ERR_BUFFER_TOO_SMALL
+    assert L.lhs_embed_wire_response(ctypes.byref(t), P, 4, ctypes.c_float(1.0), 2, 0, ctypes.c_float(0.0),
+                                     P + 2, 1 << 20, P, None) == lhs.LHS_ERR_INVALID_ARG
+    assert L.lhs_embed_wire_response(ctypes.byref(t), P, 4, ctypes.c_float(1.0), 2, 0, ctypes.c_float(0.0),
+                                     P + 4, 12 + 4 * 72 - 1, P, None) == lhs.LHS_ERR_BUFFER_TOO_SMALL
     assert L.lhs_selftest_bounded_wait(P, -5, None) == lhs.LHS_ERR_INVALID_ARG
 
 
